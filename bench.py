@@ -1,0 +1,404 @@
+"""Benchmark of the W8A8 MoE expert layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode] [--impl reference]
+
+One step = one pass of the whole layer (route sort, token quant, GMM1 with the
+fused gather, SwiGLU + requant, GMM2, Combine + Unpermute) over one batch of the
+workload's seeded synthetic inputs.  With N > 1 (torchrun, one process per GPU)
+every rank runs an independent replica of the layer on its own batch: the path
+has no exchange step, so there is no collective on the data path (weak scaling).
+
+Prints one JSON line on rank 0.  `value` is tokens/s of the whole job with the
+inputs resident in device memory; `e2e` repeats the measurement through the
+host-buffer entry point (moe_layer_fwd_host), host<->device copies included.
+`--impl reference` times the CPU oracle instead (on the host cores, rank 0 only).
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload_desc(w):
+    return "%s MoE layer: M=%d K=%d I=%d (GMM1 2I=%d) E=%d topK=%d, %s routing, seed %d" % (
+        w.name, w.M, w.K, w.I, 2 * w.I, w.E, w.topK, w.routing, w.seed)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+def algorithmic(w, expert_idx):
+    """Bytes and ops each stage must move / perform for one step."""
+    R = w.M * w.topK
+    active = int(np.unique(expert_idx[(expert_idx >= 0) & (expert_idx < w.E)]).size)
+    K, I, M = w.K, w.I, w.M
+    st = {}
+    st["route_sort"] = {"bytes": 4 * R + 8 * R + 8 * w.E}
+    st["quant"] = {"bytes": 2 * M * K + 2 * M * K + 4 * M}
+    st["gmm1"] = {"bytes": active * 2 * I * K + active * 2 * I * 4 + R * K * 2 + R * 2 * I * 2,
+                  "ops": 2 * R * K * 2 * I}
+    st["swiglu"] = {"bytes": R * 2 * I * 2 + R * I * 2 + 8 * R}
+    st["gmm2"] = {"bytes": active * K * I + active * K * 4 + R * I * 2 + R * K * 2,
+                  "ops": 2 * R * I * K}
+    st["combine"] = {"bytes": R * K * 2 + 12 * R + M * K * 2}
+    return st, active
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.lines = []
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        # the busiest half of the samples (the sampler also sees the idle edges)
+        top = sorted(sm)[len(sm) // 2:]
+        return {"sm_mhz": statistics.median(top), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    """The CPU oracle, as it stands, on the host cores: each step evaluates a
+    bounded sample of the workload's tokens (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    w = synth.CONFIGS[args.workload]
+    inp = synth.make_inputs(w)
+    n_tok = min(w.M, 16)
+    toks = np.arange(n_tok, dtype=np.int32)
+    cores = os.cpu_count()
+    oracle.layer_tokens(inp, toks[:2])  # warm-up: page in the weights
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.layer_tokens(inp, toks)
+    dt = time.perf_counter() - t0
+    value = n_tok * args.steps / dt
+    sample = "%d of the %d tokens of the %s workload per step (per-token oracle evaluation)" % (
+        n_tok, w.M, w.name)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic", "config": {"workload": workload_desc(w), "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, inp):
+    """The oracle on the host cores over a bounded sample of the workload."""
+    import oracle
+    n_tok = min(w.M, 32)
+    toks = np.arange(n_tok, dtype=np.int32)
+    oracle.layer_tokens(inp, toks[:1])
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.layer_tokens(inp, toks)
+        reps += 1
+        if time.perf_counter() - t0 > 10.0 or reps >= 8:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n_tok * reps / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d x %d tokens of the %s workload (per-token oracle evaluation, %.1f s)" % (
+                reps, n_tok, w.name, dt)}
+
+
+# ----------------------------------------------------------------------------- ncu traffic record
+def traffic_record(kernel_file):
+    """dram bytes per launch of the dominant kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "gmm1_decode_ncu.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m1 = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    m2 = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m1 and m2):
+        return None
+    src = open(kernel_file, "rb").read()
+    if hashlib.sha256(src).hexdigest() != m2.group(1):
+        return None
+    return int(m1.group(1))
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    import moe_expert_layer_gb300 as moe
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    w = synth.CONFIGS[args.workload]
+    # each rank its own replica batch: same weights, tokens/routing drawn per rank
+    inp = synth.make_inputs(w)
+    if rank:
+        r = synth.Workload(w.name, w.M, w.K, w.I, w.E, w.topK, w.routing, w.seed + 1000 * rank)
+        extra = synth.make_inputs(r, with_weights=False)
+        inp.update(extra)
+    dev = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in inp.items()}
+    d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
+    ws = torch.empty(moe.moe_layer_workspace_size(d), dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.M, w.K), dtype=torch.float16, device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # > L2 (126 MB)
+
+    def step():
+        moe.moe_layer_fwd(d, dev["x"], dev["expert_idx"], dev["probs"], dev["w1"], dev["s1"],
+                          dev["w2"], dev["s2"], out, ws, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    if moe.moe_workspace_status(ws) != 0:
+        raise RuntimeError("device status after warm-up: %d" % moe.moe_workspace_status(ws))
+
+    # ---- timed region: K layer steps, L2 flushed before each, CUDA events on the stream
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * w.M / (ms * 1e-3)
+
+    # ---- per-stage timing through the stage entry points (same kernels), for the roofline
+    R = w.R
+    i32, f16, f32 = torch.int32, torch.float16, torch.float32
+    sorted_, expanded = torch.empty(R, dtype=i32, device="cuda"), torch.empty(R, dtype=i32, device="cuda")
+    tpe, cs = torch.empty(w.E, dtype=i32, device="cuda"), torch.empty(w.E, dtype=i32, device="cuda")
+    sws = torch.empty(max(16, moe.moe_route_sort_workspace_size(d)), dtype=torch.uint8, device="cuda")
+    xq16, pts1 = torch.empty((w.M, w.K), dtype=f16, device="cuda"), torch.empty(w.M, dtype=f32, device="cuda")
+    c1 = torch.empty((R, 2 * w.I), dtype=f16, device="cuda")
+    q2, pts2 = torch.empty((R, w.I), dtype=f16, device="cuda"), torch.empty(R, dtype=f32, device="cuda")
+    c2 = torch.empty((R, w.K), dtype=f16, device="cuda")
+    gws = torch.empty(moe.moe_gmm_workspace_size(d), dtype=torch.uint8, device="cuda")
+    names = ["route_sort", "quant", "gmm1", "swiglu", "gmm2", "combine"]
+
+    def stages(evs):
+        evs[0].record(stream)
+        moe.moe_route_sort(d, dev["expert_idx"], sorted_, expanded, tpe, cs, sws, stream)
+        evs[1].record(stream)
+        moe.moe_quant_tokens(d, dev["x"], None, xq16, pts1, stream)
+        evs[2].record(stream)
+        moe.moe_gmm1(d, xq16, sorted_, cs, dev["w1"], dev["s1"], c1, gws, stream)
+        evs[3].record(stream)
+        moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, None, q2, pts2, stream)
+        evs[4].record(stream)
+        moe.moe_gmm2(d, q2, cs, dev["w2"], dev["s2"], c2, gws, stream)
+        evs[5].record(stream)
+        moe.moe_combine_unpermute(d, c2, pts2, expanded, dev["probs"], out, stream)
+        evs[6].record(stream)
+
+    for _ in range(3):
+        stages([torch.cuda.Event(enable_timing=True) for _ in range(7)])
+    n_stage_steps = max(3, min(args.steps, 50))
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_stage_steps)]
+    barrier()
+    for i in range(n_stage_steps):
+        flush.fill_(i & 0xff)
+        stages(sev[i])
+    barrier()
+    stage_ms = {n: statistics.mean(s[j].elapsed_time(s[j + 1]) for s in sev) for j, n in enumerate(names)}
+
+    alg, active = algorithmic(w, inp["expert_idx"])
+    peaks = load_peaks()
+    stage_report = {}
+    for n in names:
+        t = stage_ms[n] * 1e-3
+        rep = {"us": round(stage_ms[n] * 1e3, 2), "GBps": round(alg[n]["bytes"] / t / 1e9, 1),
+               "hbm_frac": round(alg[n]["bytes"] / t / 1e9 / peaks["hbm_gbs"], 3)}
+        if "ops" in alg[n]:
+            rep["TOPS"] = round(alg[n]["ops"] / t / 1e12, 2)
+        stage_report[n] = rep
+    dom = max(["gmm1", "gmm2"], key=lambda n: stage_ms[n])
+    ach = alg[dom]["bytes"] / (stage_ms[dom] * 1e-3) / 1e9
+    roofline = {"kernel": "grouped_gemm_kernel (%s)" % dom.upper(), "bound": "hbm",
+                "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 3),
+                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": alg[dom]["bytes"],
+                "traffic": traffic_record(os.path.join(ROOT, "moe_expert_layer_gb300", "csrc", "gemm.cu"))}
+    layer_ops = alg["gmm1"]["ops"] + alg["gmm2"]["ops"]
+
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        hws = torch.empty(moe.moe_layer_host_workspace_size(d), dtype=torch.uint8, device="cuda")
+        xh = torch.from_numpy(inp["x"]).pin_memory()
+        eih = torch.from_numpy(inp["expert_idx"]).pin_memory()
+        prh = torch.from_numpy(inp["probs"]).pin_memory()
+        outh = torch.empty((w.M, w.K), dtype=torch.float16).pin_memory()
+
+        def host_step():
+            moe.moe_layer_fwd_host(d, xh, eih, prh, dev["w1"], dev["s1"], dev["w2"], dev["s2"], outh,
+                                   hws, stream)
+
+        for _ in range(3):
+            host_step()
+        n_e2e = max(3, min(args.steps, 100))
+        tot = 0.0
+        barrier()
+        for i in range(n_e2e):
+            flush.fill_(i & 0xff)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            host_step()  # synchronises the stream before returning
+            tot += time.perf_counter() - t0
+        barrier()
+        e_ms = 1e3 * tot / n_e2e
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * w.M / (e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": int(inp["x"].nbytes + inp["expert_idx"].nbytes + inp["probs"].nbytes),
+               "d2h_bytes_per_step": int(w.M * w.K * 2), "ms_per_step": round(e_ms, 4)}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(w, inp)
+
+    launches_per_step = (1 if w.R <= 8192 else 3) + 5
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(w), "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "flushed before every timed step (512 MB write); int8 weights %.2f GB per step"
+                         % ((alg["gmm1"]["bytes"] + alg["gmm2"]["bytes"]) / 1e9),
+                   "active_experts": active},
+        "int8_TOPS": round(layer_ops / (ms * 1e-3) / 1e12, 2),
+        "roofline": roofline,
+        "stages": stage_report,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * moe_layer.h -- C ABI of the GB300 (sm_103a) W8A8 mixture-of-experts expert layer.
+ *
+ * The layer follows the stage contract of the PTO-ISA MegaMoE operator page
+ * ("pto-isa megamoe operator", kernels/manual/a2a3/dispatch_mega_combine/overview,
+ * section "key implementation logic": FrontReorder -> Dispatch -> GMM1 -> SwiGLU ->
+ * GMM2 -> Combine -> Unpermute) on a single GPU: the cross-rank count exchange,
+ * dispatch pull and combine push of that page become gathers inside device memory.
+ *
+ * Conventions shared by every entry point
+ *   - Shapes: M tokens, hidden size K, intermediate size I (GMM1 is 2I wide: the
+ *     first I columns go through silu, the second I multiply it), E experts,
+ *     topK routes per token, R = M * topK routes.  Route r = token * topK + slot.
+ *   - binary16 values are passed as uint16_t bit patterns (IEEE half).
+ *   - Every pointer argument is DEVICE memory owned by the caller, except where a
+ *     parameter name ends in _host.  The library never allocates or frees device
+ *     memory; scratch space comes from the caller's `workspace`.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  No entry point synchronises, except moe_layer_fwd_host and
+ *     moe_workspace_status, which say so.
+ *   - Arrays are dense row-major with the last index contiguous; every pointer must
+ *     be 16-byte aligned.
+ *   - Preconditions checked on the host before anything is launched:
+ *       M >= 1, 1 <= topK <= E <= 1023, K % 128 == 0, 128 <= K <= 16384,
+ *       I % 64 == 0, 64 <= I <= 8192, M * topK < 2^31 / 2I, current device sm_103.
+ *     A violated precondition returns an error and launches nothing.
+ *   - Routes whose expert id lies outside [0, E) are dropped: sorted after all
+ *     valid routes, counted in no expert, expandedRowIdx = -1, and they add
+ *     nothing to the output.  Their number is R - cumsum[E-1].
+ *   - Every fp32 -> binary16 conversion of a stage output (GMM epilogues, Combine,
+ *     Unpermute) rounds to nearest even and saturates at +-65504.
+ *   - Launch failures are reported as MOE_ERR_LAUNCH (cudaGetLastError after the
+ *     launches).  A device-side wait that gives up (a pipeline barrier that never
+ *     completes) makes the kernel record MOE_ERR_TIMEOUT in the workspace status
+ *     word and return early; read it with moe_workspace_status.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int32_t M;    /* tokens                         */
+  int32_t K;    /* hidden size                    */
+  int32_t I;    /* intermediate size (GMM1: 2I)   */
+  int32_t E;    /* experts                        */
+  int32_t topK; /* routes per token               */
+} moe_dims_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = -1,      /* a required pointer is NULL                      */
+  MOE_ERR_SHAPE = -2,     /* dimensions outside the supported ranges         */
+  MOE_ERR_ALIGN = -3,     /* a pointer is not 16-byte aligned                */
+  MOE_ERR_ARCH = -4,      /* current device is not sm_103 / no device       */
+  MOE_ERR_WORKSPACE = -5, /* workspace missing or smaller than required      */
+  MOE_ERR_LAUNCH = -6,    /* a CUDA launch or copy failed                    */
+  MOE_ERR_TIMEOUT = -8    /* a device-side pipeline wait gave up             */
+} moe_status_t;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int32_t status);
+
+/* ------------------------------------------------------------------------ */
+/* Whole layer                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace moe_layer_fwd needs for these dimensions
+ * (0 if the dimensions are invalid). */
+size_t moe_layer_workspace_size(const moe_dims_t* d);
+
+/*
+ * out[t, :] = sum over the token's valid routes of probs[t, j] * FFN_e(x[t, :]),
+ * the W8A8 expert layer of MegaMoe::Process() (all seven stages of the page).
+ *
+ *   x          [M][K]      binary16 tokens
+ *   expert_idx [M][topK]   int32 expert of each route
+ *   probs      [M][topK]   fp32 route weights (used as given, not renormalised)
+ *   w1         [E][2I][K]  int8 GMM1 weights, K contiguous (the page's packed
+ *                          weight1[e][k][n], transposed so the reduction runs along rows)
+ *   s1         [E][2I]     fp32 GMM1 per-channel scales
+ *   w2         [E][K][I]   int8 GMM2 weights, I contiguous
+ *   s2         [E][K]      fp32 GMM2 per-channel scales
+ *   out        [M][K]      binary16 result (written for every token; a token with
+ *                          no valid route gets zeros)
+ *   workspace  >= moe_layer_workspace_size(d) bytes of device memory, 256-byte
+ *              aligned; its contents on entry do not matter.
+ * The intermediates (route tables, quantised tokens, GMM outputs) live in the
+ * workspace until the next call that uses it.
+ */
+int32_t moe_layer_fwd(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx,
+                      const float* probs, const int8_t* w1, const float* s1, const int8_t* w2,
+                      const float* s2, uint16_t* out, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* Bytes of device workspace moe_layer_fwd_host needs (layer workspace plus
+ * staging for the per-call host inputs and the output). */
+size_t moe_layer_host_workspace_size(const moe_dims_t* d);
+
+/*
+ * moe_layer_fwd with the per-call tensors in HOST memory: copies x_host,
+ * expert_idx_host and probs_host to the device (into the workspace), runs the
+ * layer, copies the result to out_host, and synchronises `stream` before
+ * returning.  Weights and scales stay device pointers (model parameters are
+ * resident).  Host buffers should be page-locked for the copies to run at full
+ * speed; pageable memory works but is slower.
+ */
+int32_t moe_layer_fwd_host(const moe_dims_t* d, const uint16_t* x_host,
+                           const int32_t* expert_idx_host, const float* probs_host,
+                           const int8_t* w1, const float* s1, const int8_t* w2, const float* s2,
+                           uint16_t* out_host, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Reads the status word that kernels running on `workspace` (the layer's, or a
+ * GEMM stage's) set when a device-side wait gives up.  Synchronises `stream`.
+ * *host_status receives MOE_OK or MOE_ERR_TIMEOUT. */
+int32_t moe_workspace_status(const void* workspace, int32_t* host_status, void* stream);
+
+/* Clears that status word (asynchronous). */
+int32_t moe_workspace_clear_status(void* workspace, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Stages (same conventions).  Used by the parity tests and benchmarks; the */
+/* layer runs the same kernels.                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes of moe_route_sort (per-block histograms). */
+size_t moe_route_sort_workspace_size(const moe_dims_t* d);
+
+/*
+ * FrontReorder phases 1, 2a, 2b and 4 on one rank (page section "1. FrontReorder"):
+ * stable sort of the routes by expert id (ties by route id), the per-expert counts,
+ * the inverse permutation and the prefix sum.
+ *   sorted_src_route  [R]  out: route placed at expanded row d (the page's sortedSrcRoute)
+ *   expanded_row_idx  [R]  out: expanded row of route r, -1 if r is invalid
+ *   tokens_per_expert [E]  out: routes per expert
+ *   cumsum            [E]  out: inclusive prefix sum of tokens_per_expert
+ */
+int32_t moe_route_sort(const moe_dims_t* d, const int32_t* expert_idx, int32_t* sorted_src_route,
+                       int32_t* expanded_row_idx, int32_t* tokens_per_expert, int32_t* cumsum,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * FrontReorder phase 2c (page section "1. FrontReorder"): per-token dynamic int8
+ * quantisation, once per token: pts1[t] = max_k |x[t,k]| / 127 and
+ * q = round-half-away(x / pts1), clamped to [-127, 127]; an all-zero token gets
+ * pts1 = 0 and zero codes.
+ *   xq_i8  [M][K] int8 codes (may be NULL)
+ *   xq_f16 [M][K] the same codes as binary16 integers, the operand format the
+ *          GEMMs read (may be NULL; at least one of the two must be given)
+ *   pts1   [M]    fp32 scales
+ */
+int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, int8_t* xq_i8, uint16_t* xq_f16,
+                         float* pts1, void* stream);
+
+/* Workspace bytes of moe_gmm1 / moe_gmm2 (status word). */
+size_t moe_gmm_workspace_size(const moe_dims_t* d);
+
+/*
+ * Dispatch + GMM1 (page sections "2. Dispatch" and "3. GMM1"): for each valid
+ * expanded row d of expert e (rows cumsum[e]-count_e .. cumsum[e]-1), token
+ * t = sorted_src_route[d] / topK:
+ *   acc[n]   = sum_k xq[t,k] * w1[e][n][k]                 (exact integer)
+ *   c1[d][n] = binary16(float(acc[n]) * s1[e][n])          n < 2I
+ * The token rows are gathered straight from xq_f16; no dispatched copy is made.
+ *   xq_f16 [M][K] binary16-coded int8 codes; c1 [R][2I] (rows >= cumsum[E-1] untouched)
+ */
+int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* xq_f16, const int32_t* sorted_src_route,
+                 const int32_t* cumsum, const int8_t* w1, const float* s1, uint16_t* c1,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * SwiGLU + dynamic requant (page section "4. SwiGLU"), per valid expanded row d
+ * with token t = sorted_src_route[d] / topK:
+ *   h = float(c1[d]) * pts1[t];  y_j = silu(h_j) * h_{j+I},  silu(v) = v / (1 + exp(-v))
+ *   pts2[d] = max_j |y_j| / 127;  q_j = round-half-even(y_j * (127 / max|y|)), clamped
+ *   q2_i8 [R][I] int8 (may be NULL); q2_f16 [R][I] binary16-coded (may be NULL); pts2 [R]
+ */
+int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* pts1,
+                         const int32_t* sorted_src_route, const int32_t* cumsum, int8_t* q2_i8,
+                         uint16_t* q2_f16, float* pts2, void* stream);
+
+/*
+ * GMM2 (page section "5. GMM2"): for each valid expanded row d of expert e,
+ *   c2[d][k] = binary16(float(sum_i q2[d,i] * w2[e][k][i]) * s2[e][k])
+ *   q2_f16 [R][I] binary16-coded int8 codes; c2 [R][K]
+ */
+int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cumsum,
+                 const int8_t* w2, const float* s2, uint16_t* c2, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/*
+ * Combine + Unpermute (page sections "6. Combine" and "7. Unpermute"), fused:
+ *   D = binary16(float(c2[d][k]) * pts2[d])
+ *   out[t][k] = binary16(sum_{j=0..topK-1, route valid} float(D[expanded_row_idx[t*topK+j]][k]) * probs[t][j])
+ * with an fp32 accumulator, slots in order, multiply then add.
+ */
+int32_t moe_combine_unpermute(const moe_dims_t* d, const uint16_t* c2, const float* pts2,
+                              const int32_t* expanded_row_idx, const float* probs, uint16_t* out,
+                              void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYER_H */

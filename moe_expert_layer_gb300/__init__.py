@@ -1,0 +1,185 @@
+"""GB300 (sm_103a) W8A8 mixture-of-experts expert layer.
+
+Thin Python binding over the C ABI in ``include/moe_layer.h`` (library
+``_build/libmoe_layer.so``, built by ``moe_expert_layer_gb300.build``).  The
+functions below carry the ABI's names and only marshal arguments: torch
+tensors (device memory) become raw pointers, the stream defaults to torch's
+current stream, and a non-zero status raises ``MoeError``.  Every stage of the
+layer runs in the library's CUDA kernels; there is no other code path, and
+importing the binding fails loudly when the library is missing.
+"""
+import ctypes
+import os
+
+from . import build as _build
+
+LIB_PATH = _build.LIB_PATH
+
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_NULL", -2: "MOE_ERR_SHAPE", -3: "MOE_ERR_ALIGN",
+          -4: "MOE_ERR_ARCH", -5: "MOE_ERR_WORKSPACE", -6: "MOE_ERR_LAUNCH",
+          -8: "MOE_ERR_TIMEOUT"}
+
+# every entry point declared in include/moe_layer.h
+EXPORTS = [
+    "moe_status_string", "moe_layer_workspace_size", "moe_layer_fwd",
+    "moe_layer_host_workspace_size", "moe_layer_fwd_host", "moe_workspace_status",
+    "moe_workspace_clear_status", "moe_route_sort_workspace_size", "moe_route_sort",
+    "moe_quant_tokens", "moe_gmm_workspace_size", "moe_gmm1", "moe_swiglu_quant", "moe_gmm2",
+    "moe_combine_unpermute",
+]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS.get(code, "unknown"), code))
+
+
+class moe_dims_t(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int32), ("K", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("topK", ctypes.c_int32)]
+
+
+def dims(M, K, I, E, topK):
+    return moe_dims_t(M, K, I, E, topK)
+
+
+_lib = None
+
+
+def load_library(path=None):
+    """Loads the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError("libmoe_layer.so not built (run moe_expert_layer_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    D = ctypes.POINTER(moe_dims_t)
+    sigs = {
+        "moe_status_string": ([i32], ctypes.c_char_p),
+        "moe_layer_workspace_size": ([D], sz),
+        "moe_layer_host_workspace_size": ([D], sz),
+        "moe_layer_fwd": ([D] + [vp] * 9 + [sz, vp], i32),
+        "moe_layer_fwd_host": ([D] + [vp] * 9 + [sz, vp], i32),
+        "moe_workspace_status": ([vp, ctypes.POINTER(i32), vp], i32),
+        "moe_workspace_clear_status": ([vp, vp], i32),
+        "moe_route_sort_workspace_size": ([D], sz),
+        "moe_route_sort": ([D] + [vp] * 6 + [sz, vp], i32),
+        "moe_quant_tokens": ([D] + [vp] * 5, i32),
+        "moe_gmm_workspace_size": ([D], sz),
+        "moe_gmm1": ([D] + [vp] * 7 + [sz, vp], i32),
+        "moe_swiglu_quant": ([D] + [vp] * 8, i32),
+        "moe_gmm2": ([D] + [vp] * 6 + [sz, vp], i32),
+        "moe_combine_unpermute": ([D] + [vp] * 6, i32),
+    }
+    for name, (args, res) in sigs.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def _p(t):
+    """Raw pointer of a tensor (device or host), or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, code):
+    if code != 0:
+        raise MoeError(fn, code)
+
+
+def moe_layer_workspace_size(d):
+    return load_library().moe_layer_workspace_size(ctypes.byref(d))
+
+
+def moe_layer_host_workspace_size(d):
+    return load_library().moe_layer_host_workspace_size(ctypes.byref(d))
+
+
+def moe_route_sort_workspace_size(d):
+    return load_library().moe_route_sort_workspace_size(ctypes.byref(d))
+
+
+def moe_gmm_workspace_size(d):
+    return load_library().moe_gmm_workspace_size(ctypes.byref(d))
+
+
+def moe_layer_fwd(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspace, stream=None):
+    _check("moe_layer_fwd", load_library().moe_layer_fwd(
+        ctypes.byref(d), _p(x), _p(expert_idx), _p(probs), _p(w1), _p(s1), _p(w2), _p(s2), _p(out),
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_layer_fwd_host(d, x_host, expert_idx_host, probs_host, w1, s1, w2, s2, out_host, workspace,
+                       stream=None):
+    _check("moe_layer_fwd_host", load_library().moe_layer_fwd_host(
+        ctypes.byref(d), _p(x_host), _p(expert_idx_host), _p(probs_host), _p(w1), _p(s1), _p(w2),
+        _p(s2), _p(out_host), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def moe_workspace_status(workspace, stream=None):
+    st = ctypes.c_int32(0)
+    _check("moe_workspace_status",
+           load_library().moe_workspace_status(_p(workspace), ctypes.byref(st), _stream(stream)))
+    return st.value
+
+
+def moe_workspace_clear_status(workspace, stream=None):
+    _check("moe_workspace_clear_status",
+           load_library().moe_workspace_clear_status(_p(workspace), _stream(stream)))
+
+
+def moe_route_sort(d, expert_idx, sorted_src_route, expanded_row_idx, tokens_per_expert, cumsum,
+                   workspace=None, stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("moe_route_sort", load_library().moe_route_sort(
+        ctypes.byref(d), _p(expert_idx), _p(sorted_src_route), _p(expanded_row_idx),
+        _p(tokens_per_expert), _p(cumsum), _p(workspace), nbytes, _stream(stream)))
+
+
+def moe_quant_tokens(d, x, xq_i8, xq_f16, pts1, stream=None):
+    _check("moe_quant_tokens", load_library().moe_quant_tokens(
+        ctypes.byref(d), _p(x), _p(xq_i8), _p(xq_f16), _p(pts1), _stream(stream)))
+
+
+def moe_gmm1(d, xq_f16, sorted_src_route, cumsum, w1, s1, c1, workspace, stream=None):
+    _check("moe_gmm1", load_library().moe_gmm1(
+        ctypes.byref(d), _p(xq_f16), _p(sorted_src_route), _p(cumsum), _p(w1), _p(s1), _p(c1),
+        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_swiglu_quant(d, c1, pts1, sorted_src_route, cumsum, q2_i8, q2_f16, pts2, stream=None):
+    _check("moe_swiglu_quant", load_library().moe_swiglu_quant(
+        ctypes.byref(d), _p(c1), _p(pts1), _p(sorted_src_route), _p(cumsum), _p(q2_i8), _p(q2_f16),
+        _p(pts2), _stream(stream)))
+
+
+def moe_gmm2(d, q2_f16, cumsum, w2, s2, c2, workspace, stream=None):
+    _check("moe_gmm2", load_library().moe_gmm2(
+        ctypes.byref(d), _p(q2_f16), _p(cumsum), _p(w2), _p(s2), _p(c2), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_combine_unpermute(d, c2, pts2, expanded_row_idx, probs, out, stream=None):
+    _check("moe_combine_unpermute", load_library().moe_combine_unpermute(
+        ctypes.byref(d), _p(c2), _p(pts2), _p(expanded_row_idx), _p(probs), _p(out),
+        _stream(stream)))

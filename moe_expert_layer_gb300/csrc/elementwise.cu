@@ -1,0 +1,225 @@
+// The layer's row-wise, HBM-bound stages:
+//   token quant        (PTO-ISA MegaMoE operator page, "1. FrontReorder", phase 2c)
+//   SwiGLU + requant   (same page, "4. SwiGLU")
+//   Combine+Unpermute  (same page, "6. Combine" and "7. Unpermute"), fused
+// Rows are read with 16-byte vector loads kept in registers, so each input byte
+// is read from HBM once; row maxima are warp-shuffle + shared-memory reductions.
+// Arithmetic uses explicitly rounded fp32 intrinsics (no contraction), matching
+// the rounding points the page defines.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+union Vec8h {
+  int4 v;
+  __half2 h2[4];
+  __half h[8];
+};
+
+constexpr int kRowThreads = 256;
+
+// --------------------------------------------------------------------------
+// per-token dynamic quant: pts1 = amax / 127, q = round_half_away(x / pts1)
+// --------------------------------------------------------------------------
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half* __restrict__ x, int K,
+                                                                   int8_t* __restrict__ xq_i8,
+                                                                   __half* __restrict__ xq_f16,
+                                                                   float* __restrict__ pts1) {
+  __shared__ float red[kRowThreads / 32];
+  const int t = blockIdx.x;
+  const int nvec = K >> 3;
+  const int4* row = reinterpret_cast<const int4*>(x + (size_t)t * K);
+  Vec8h v[VPT];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * kRowThreads;
+    if (idx < nvec) {
+      v[i].v = __ldg(row + idx);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(__half2float(v[i].h[j])));
+    }
+  }
+  amax = block_max_nonneg(amax, red);
+  const float scale = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) pts1[t] = scale;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * kRowThreads;
+    if (idx < nvec) {
+      int q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        q[j] = (amax > 0.0f) ? clamp127((int)roundf(__fdiv_rn(__half2float(v[i].h[j]), scale))) : 0;
+      if (xq_i8) {
+        uint2 packed;
+        packed.x = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
+                   ((uint32_t)(q[3] & 0xff) << 24);
+        packed.y = (uint32_t)(q[4] & 0xff) | ((uint32_t)(q[5] & 0xff) << 8) | ((uint32_t)(q[6] & 0xff) << 16) |
+                   ((uint32_t)(q[7] & 0xff) << 24);
+        reinterpret_cast<uint2*>(xq_i8 + (size_t)t * K)[idx] = packed;
+      }
+      if (xq_f16) {
+        Vec8h o;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o.h[j] = __int2half_rn(q[j]);
+        reinterpret_cast<int4*>(xq_f16 + (size_t)t * K)[idx] = o.v;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// SwiGLU + requant over expanded rows d < cumsum[E-1]
+// --------------------------------------------------------------------------
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
+    const __half* __restrict__ c1, int I, int E, int topK, const float* __restrict__ pts1,
+    const int32_t* __restrict__ sorted_src_route, const int32_t* __restrict__ cumsum,
+    int8_t* __restrict__ q2_i8, __half* __restrict__ q2_f16, float* __restrict__ pts2) {
+  __shared__ float red[kRowThreads / 32];
+  const int d = blockIdx.x;
+  if (d >= __ldg(cumsum + E - 1)) return;
+  const float p1 = __ldg(pts1 + __ldg(sorted_src_route + d) / topK);
+  const int nvec = I >> 3;
+  const int4* gate = reinterpret_cast<const int4*>(c1 + (size_t)d * 2 * I);
+  const int4* up = gate + nvec;
+  float y[VPT][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * kRowThreads;
+    if (idx < nvec) {
+      Vec8h g, u;
+      g.v = __ldg(gate + idx);
+      u.v = __ldg(up + idx);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float hg = __fmul_rn(__half2float(g.h[j]), p1);
+        const float hu = __fmul_rn(__half2float(u.h[j]), p1);
+        const float silu = __fdiv_rn(hg, __fadd_rn(1.0f, expf(-hg)));
+        y[i][j] = __fmul_rn(silu, hu);
+        amax = fmaxf(amax, fabsf(y[i][j]));
+      }
+    }
+  }
+  amax = block_max_nonneg(amax, red);
+  const bool nz = amax > 0.0f;
+  const float inv = nz ? __fdiv_rn(127.0f, amax) : 0.0f;
+  if (threadIdx.x == 0) pts2[d] = nz ? __fdiv_rn(amax, 127.0f) : 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * kRowThreads;
+    if (idx < nvec) {
+      int q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) q[j] = nz ? clamp127(__float2int_rn(__fmul_rn(y[i][j], inv))) : 0;
+      if (q2_i8) {
+        uint2 packed;
+        packed.x = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
+                   ((uint32_t)(q[3] & 0xff) << 24);
+        packed.y = (uint32_t)(q[4] & 0xff) | ((uint32_t)(q[5] & 0xff) << 8) | ((uint32_t)(q[6] & 0xff) << 16) |
+                   ((uint32_t)(q[7] & 0xff) << 24);
+        reinterpret_cast<uint2*>(q2_i8 + (size_t)d * I)[idx] = packed;
+      }
+      if (q2_f16) {
+        Vec8h o;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o.h[j] = __int2half_rn(q[j]);
+        reinterpret_cast<int4*>(q2_f16 + (size_t)d * I)[idx] = o.v;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------------
+// Combine (D = sat_f16(C2 * pts2)) fused with Unpermute (prob-weighted sum of
+// the token's topK rows, fp32 accumulator, slot order, multiply then add).
+// grid = (M, ceil(K / (8 * 128))); each thread owns 8 consecutive columns.
+// --------------------------------------------------------------------------
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_unpermute_kernel(
+    const __half* __restrict__ c2, const float* __restrict__ pts2, const int32_t* __restrict__ expanded_row_idx,
+    const float* __restrict__ probs, int K, int topK, __half* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int vec = blockIdx.y * kCombineThreads + threadIdx.x;
+  if (vec * 8 >= K) return;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+  for (int s = 0; s < topK; ++s) {
+    const int d = __ldg(expanded_row_idx + (size_t)t * topK + s);
+    if (d < 0) continue;
+    const float p = __ldg(probs + (size_t)t * topK + s);
+    const float sc = __ldg(pts2 + d);
+    Vec8h c;
+    c.v = __ldg(reinterpret_cast<const int4*>(c2 + (size_t)d * K) + vec);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float dv = __half2float(f2h_sat(__fmul_rn(__half2float(c.h[j]), sc)));
+      acc[j] = __fadd_rn(acc[j], __fmul_rn(dv, p));
+    }
+  }
+  Vec8h o;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) o.h[j] = f2h_sat(acc[j]);
+  reinterpret_cast<int4*>(out + (size_t)t * K)[vec] = o.v;
+}
+
+}  // namespace
+
+cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16, float* pts1,
+                                cudaStream_t stream) {
+  const int nvec = K / 8;
+  const int vpt = (nvec + kRowThreads - 1) / kRowThreads;
+  const __half* xh = reinterpret_cast<const __half*>(x);
+  __half* qf = reinterpret_cast<__half*>(xq_f16);
+  if (vpt <= 1)
+    quant_tokens_kernel<1><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1);
+  else if (vpt <= 2)
+    quant_tokens_kernel<2><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1);
+  else if (vpt <= 4)
+    quant_tokens_kernel<4><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1);
+  else if (vpt <= 8)
+    quant_tokens_kernel<8><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int topK, const float* pts1,
+                                const int32_t* sorted_src_route, const int32_t* cumsum, int8_t* q2_i8,
+                                uint16_t* q2_f16, float* pts2, cudaStream_t stream) {
+  const int nvec = I / 8;
+  const int vpt = (nvec + kRowThreads - 1) / kRowThreads;
+  const __half* ch = reinterpret_cast<const __half*>(c1);
+  __half* qf = reinterpret_cast<__half*>(q2_f16);
+  if (vpt <= 1)
+    swiglu_quant_kernel<1><<<R, kRowThreads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
+                                                          qf, pts2);
+  else if (vpt <= 2)
+    swiglu_quant_kernel<2><<<R, kRowThreads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
+                                                          qf, pts2);
+  else if (vpt <= 4)
+    swiglu_quant_kernel<4><<<R, kRowThreads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
+                                                          qf, pts2);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_unpermute(const uint16_t* c2, const float* pts2, const int32_t* expanded_row_idx,
+                                     const float* probs, int M, int K, int topK, uint16_t* out,
+                                     cudaStream_t stream) {
+  dim3 grid(M, (K / 8 + kCombineThreads - 1) / kCombineThreads);
+  combine_unpermute_kernel<<<grid, kCombineThreads, 0, stream>>>(
+      reinterpret_cast<const __half*>(c2), pts2, expanded_row_idx, probs, K, topK, reinterpret_cast<__half*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

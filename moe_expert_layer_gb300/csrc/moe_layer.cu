@@ -1,0 +1,356 @@
+// C ABI of the expert layer: host-side validation, workspace carving and the
+// launch sequence of MegaMoe::Process() on one GPU (PTO-ISA MegaMoE operator
+// page, section "key implementation logic").  See include/moe_layer.h for the
+// contract of every entry point.
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/moe_layer.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int32_t check_dims(const moe_dims_t* d) {
+  if (!d) return MOE_ERR_NULL;
+  if (d->M < 1 || d->topK < 1 || d->E < d->topK || d->E > 1023) return MOE_ERR_SHAPE;
+  if (d->K < 128 || d->K > 16384 || d->K % 128) return MOE_ERR_SHAPE;
+  if (d->I < 64 || d->I > 8192 || d->I % 64) return MOE_ERR_SHAPE;
+  const int64_t R = (int64_t)d->M * d->topK;
+  if (R >= (int64_t)1 << 24) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+int32_t check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_ARCH;
+  static int cached_dev = -2, cached_ok = 0;
+  if (dev != cached_dev) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MOE_ERR_ARCH;
+    cached_ok = (major == 10 && minor == 3);
+    cached_dev = dev;
+  }
+  return cached_ok ? MOE_OK : MOE_ERR_ARCH;
+}
+
+int32_t launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
+
+// Layout of the layer workspace.
+struct Layout {
+  size_t status, sorted, expanded, tpe, cumsum, sort_ws, xq16, pts1, c1, q2, pts2, c2, total;
+  // host-variant staging
+  size_t hx, hei, hprobs, hout, host_total;
+};
+
+Layout layout_of(const moe_dims_t* d) {
+  const size_t M = d->M, K = d->K, I = d->I, E = d->E, R = M * d->topK;
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  L.status = take(sizeof(int32_t));
+  L.sorted = take(R * 4);
+  L.expanded = take(R * 4);
+  L.tpe = take(E * 4);
+  L.cumsum = take(E * 4);
+  L.sort_ws = take(moe::route_sort_workspace_bytes((int)R, (int)E));
+  L.xq16 = take(M * K * 2);
+  L.pts1 = take(M * 4);
+  L.c1 = take(R * 2 * I * 2);
+  L.q2 = take(R * I * 2);
+  L.pts2 = take(R * 4);
+  L.c2 = take(R * K * 2);
+  L.total = off;
+  L.hx = take(M * K * 2);
+  L.hei = take(R * 4);
+  L.hprobs = take(R * 4);
+  L.hout = take(M * K * 2);
+  L.host_total = off;
+  return L;
+}
+
+template <typename P>
+P* at(void* base, size_t off) {
+  return reinterpret_cast<P*>(static_cast<uint8_t*>(base) + off);
+}
+
+int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx, const float* probs,
+                  const int8_t* w1, const float* s1, const int8_t* w2, const float* s2, uint16_t* out,
+                  void* ws, const Layout& L, cudaStream_t st) {
+  const int M = d->M, K = d->K, I = d->I, E = d->E, topK = d->topK, R = M * topK;
+  int32_t* status = at<int32_t>(ws, L.status);
+  int32_t* sorted = at<int32_t>(ws, L.sorted);
+  int32_t* expanded = at<int32_t>(ws, L.expanded);
+  int32_t* tpe = at<int32_t>(ws, L.tpe);
+  int32_t* cumsum = at<int32_t>(ws, L.cumsum);
+  uint16_t* xq16 = at<uint16_t>(ws, L.xq16);
+  float* pts1 = at<float>(ws, L.pts1);
+  uint16_t* c1 = at<uint16_t>(ws, L.c1);
+  uint16_t* q2 = at<uint16_t>(ws, L.q2);
+  float* pts2 = at<float>(ws, L.pts2);
+  uint16_t* c2 = at<uint16_t>(ws, L.c2);
+
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(status, 0, sizeof(int32_t), st)) != cudaSuccess) return launch_status(e);
+  if ((e = moe::launch_route_sort(expert_idx, R, E, sorted, expanded, tpe, cumsum, at<void>(ws, L.sort_ws), st)) !=
+      cudaSuccess)
+    return launch_status(e);
+  if ((e = moe::launch_quant_tokens(x, M, K, nullptr, xq16, pts1, st)) != cudaSuccess) return launch_status(e);
+
+  moe::GroupedGemmProblem g1{};
+  g1.act = xq16;
+  g1.act_rows = M;
+  g1.sorted_src_route = sorted;
+  g1.topK = topK;
+  g1.cumsum = cumsum;
+  g1.w = w1;
+  g1.scale = s1;
+  g1.C = c1;
+  g1.R = R;
+  g1.E = E;
+  g1.N = 2 * I;
+  g1.Kd = K;
+  g1.gather = true;
+  g1.status = status;
+  if ((e = moe::launch_grouped_gemm(g1, st)) != cudaSuccess) return launch_status(e);
+
+  if ((e = moe::launch_swiglu_quant(c1, R, I, E, topK, pts1, sorted, cumsum, nullptr, q2, pts2, st)) != cudaSuccess)
+    return launch_status(e);
+
+  moe::GroupedGemmProblem g2{};
+  g2.act = q2;
+  g2.act_rows = R;
+  g2.sorted_src_route = nullptr;
+  g2.topK = topK;
+  g2.cumsum = cumsum;
+  g2.w = w2;
+  g2.scale = s2;
+  g2.C = c2;
+  g2.R = R;
+  g2.E = E;
+  g2.N = K;
+  g2.Kd = I;
+  g2.gather = false;
+  g2.status = status;
+  if ((e = moe::launch_grouped_gemm(g2, st)) != cudaSuccess) return launch_status(e);
+
+  e = moe::launch_combine_unpermute(c2, pts2, expanded, probs, M, K, topK, out, st);
+  return launch_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int32_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "null pointer";
+    case MOE_ERR_SHAPE: return "unsupported dimensions";
+    case MOE_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case MOE_ERR_ARCH: return "current device is not sm_103";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_LAUNCH: return "CUDA launch or copy failed";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t moe_layer_workspace_size(const moe_dims_t* d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return layout_of(d).total;
+}
+
+size_t moe_layer_host_workspace_size(const moe_dims_t* d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return layout_of(d).host_total;
+}
+
+int32_t moe_layer_fwd(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx, const float* probs,
+                      const int8_t* w1, const float* s1, const int8_t* w2, const float* s2, uint16_t* out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!x || !expert_idx || !probs || !w1 || !s1 || !w2 || !s2 || !out || !workspace) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(expert_idx) || !aligned16(probs) || !aligned16(w1) || !aligned16(s1) ||
+      !aligned16(w2) || !aligned16(s2) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MOE_ERR_ALIGN;
+  const Layout L = layout_of(d);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  return run_layer(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspace, L, static_cast<cudaStream_t>(stream));
+}
+
+int32_t moe_layer_fwd_host(const moe_dims_t* d, const uint16_t* x_host, const int32_t* expert_idx_host,
+                           const float* probs_host, const int8_t* w1, const float* s1, const int8_t* w2,
+                           const float* s2, uint16_t* out_host, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!x_host || !expert_idx_host || !probs_host || !w1 || !s1 || !w2 || !s2 || !out_host || !workspace)
+    return MOE_ERR_NULL;
+  if (!aligned16(w1) || !aligned16(s1) || !aligned16(w2) || !aligned16(s2) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MOE_ERR_ALIGN;
+  const Layout L = layout_of(d);
+  if (workspace_bytes < L.host_total) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t M = d->M, K = d->K, R = M * d->topK;
+  uint16_t* dx = at<uint16_t>(workspace, L.hx);
+  int32_t* dei = at<int32_t>(workspace, L.hei);
+  float* dpr = at<float>(workspace, L.hprobs);
+  uint16_t* dout = at<uint16_t>(workspace, L.hout);
+  if (cudaMemcpyAsync(dx, x_host, M * K * 2, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dei, expert_idx_host, R * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dpr, probs_host, R * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  rc = run_layer(d, dx, dei, dpr, w1, s1, w2, s2, dout, workspace, L, st);
+  if (rc != MOE_OK) return rc;
+  if (cudaMemcpyAsync(out_host, dout, M * K * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return MOE_OK;
+}
+
+int32_t moe_workspace_status(const void* workspace, int32_t* host_status, void* stream) {
+  if (!workspace || !host_status) return MOE_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return MOE_OK;
+}
+
+int32_t moe_workspace_clear_status(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_NULL;
+  return launch_status(cudaMemsetAsync(workspace, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+}
+
+// ----------------------------------------------------------------------------- stages
+
+size_t moe_route_sort_workspace_size(const moe_dims_t* d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return moe::route_sort_workspace_bytes(d->M * d->topK, d->E);
+}
+
+int32_t moe_route_sort(const moe_dims_t* d, const int32_t* expert_idx, int32_t* sorted_src_route,
+                       int32_t* expanded_row_idx, int32_t* tokens_per_expert, int32_t* cumsum, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!expert_idx || !sorted_src_route || !expanded_row_idx || !tokens_per_expert || !cumsum) return MOE_ERR_NULL;
+  const size_t need = moe::route_sort_workspace_bytes(d->M * d->topK, d->E);
+  if (need && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  return launch_status(moe::launch_route_sort(expert_idx, d->M * d->topK, d->E, sorted_src_route, expanded_row_idx,
+                                              tokens_per_expert, cumsum, workspace,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, int8_t* xq_i8, uint16_t* xq_f16, float* pts1,
+                         void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!x || !pts1 || (!xq_i8 && !xq_f16)) return MOE_ERR_NULL;
+  if (!aligned16(x) || (xq_i8 && !aligned16(xq_i8)) || (xq_f16 && !aligned16(xq_f16))) return MOE_ERR_ALIGN;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  return launch_status(moe::launch_quant_tokens(x, d->M, d->K, xq_i8, xq_f16, pts1, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_gmm_workspace_size(const moe_dims_t* d) {
+  if (check_dims(d) != MOE_OK) return 0;
+  return kAlign;
+}
+
+int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* xq_f16, const int32_t* sorted_src_route, const int32_t* cumsum,
+                 const int8_t* w1, const float* s1, uint16_t* c1, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!xq_f16 || !sorted_src_route || !cumsum || !w1 || !s1 || !c1 || !workspace) return MOE_ERR_NULL;
+  if (!aligned16(xq_f16) || !aligned16(w1) || !aligned16(c1)) return MOE_ERR_ALIGN;
+  if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  moe::GroupedGemmProblem g{};
+  g.act = xq_f16;
+  g.act_rows = d->M;
+  g.sorted_src_route = sorted_src_route;
+  g.topK = d->topK;
+  g.cumsum = cumsum;
+  g.w = w1;
+  g.scale = s1;
+  g.C = c1;
+  g.R = d->M * d->topK;
+  g.E = d->E;
+  g.N = 2 * d->I;
+  g.Kd = d->K;
+  g.gather = true;
+  g.status = static_cast<int32_t*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return launch_status(moe::launch_grouped_gemm(g, st));
+}
+
+int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* pts1, const int32_t* sorted_src_route,
+                         const int32_t* cumsum, int8_t* q2_i8, uint16_t* q2_f16, float* pts2, void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!c1 || !pts1 || !sorted_src_route || !cumsum || !pts2 || (!q2_i8 && !q2_f16)) return MOE_ERR_NULL;
+  if (!aligned16(c1) || (q2_i8 && !aligned16(q2_i8)) || (q2_f16 && !aligned16(q2_f16))) return MOE_ERR_ALIGN;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  return launch_status(moe::launch_swiglu_quant(c1, d->M * d->topK, d->I, d->E, d->topK, pts1, sorted_src_route,
+                                                cumsum, q2_i8, q2_f16, pts2, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cumsum, const int8_t* w2,
+                 const float* s2, uint16_t* c2, void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!q2_f16 || !cumsum || !w2 || !s2 || !c2 || !workspace) return MOE_ERR_NULL;
+  if (!aligned16(q2_f16) || !aligned16(w2) || !aligned16(c2)) return MOE_ERR_ALIGN;
+  if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  moe::GroupedGemmProblem g{};
+  g.act = q2_f16;
+  g.act_rows = d->M * d->topK;
+  g.sorted_src_route = nullptr;
+  g.topK = d->topK;
+  g.cumsum = cumsum;
+  g.w = w2;
+  g.scale = s2;
+  g.C = c2;
+  g.R = d->M * d->topK;
+  g.E = d->E;
+  g.N = d->K;
+  g.Kd = d->I;
+  g.gather = false;
+  g.status = static_cast<int32_t*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return launch_status(moe::launch_grouped_gemm(g, st));
+}
+
+int32_t moe_combine_unpermute(const moe_dims_t* d, const uint16_t* c2, const float* pts2,
+                              const int32_t* expanded_row_idx, const float* probs, uint16_t* out, void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!c2 || !pts2 || !expanded_row_idx || !probs || !out) return MOE_ERR_NULL;
+  if (!aligned16(c2) || !aligned16(out)) return MOE_ERR_ALIGN;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  return launch_status(moe::launch_combine_unpermute(c2, pts2, expanded_row_idx, probs, d->M, d->K, d->topK, out,
+                                                     static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

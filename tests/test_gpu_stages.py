@@ -1,0 +1,222 @@
+"""GPU parity of each stage against the CPU oracle, through the C ABI.
+
+Each stage is fed the oracle's own inputs for that stage, so a mismatch points
+at one kernel.  Index, sort and quant outputs are compared bit for bit; GEMM
+outputs too (identical int8 operands give identical int32 accumulators, and the
+epilogue's rounding points are fixed); SwiGLU's codes within 1 LSB on <= 0.1%
+of elements (exp is evaluated by different libraries on the two sides).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import moe_expert_layer_gb300 as moe
+    from gpu_util import assert_bits_equal, assert_q2_close, dev, empty, host
+
+
+def _dims(w):
+    return moe.dims(w.M, w.K, w.I, w.E, w.topK)
+
+
+def _sort_on_gpu(w, expert_idx):
+    d = _dims(w)
+    R = w.M * w.topK
+    s, x = empty(R, torch.int32), empty(R, torch.int32)
+    tpe, cs = empty(w.E, torch.int32), empty(w.E, torch.int32)
+    nws = moe.moe_route_sort_workspace_size(d)
+    ws = empty(max(nws, 16), torch.uint8)
+    moe.moe_route_sort(d, dev(expert_idx), s, x, tpe, cs, ws)
+    torch.cuda.synchronize()
+    return host(s), host(x), host(tpe), host(cs)
+
+
+# ------------------------------------------------------------------ route sort
+SORT_CASES = [
+    ("tiny", None), ("decode", None), ("mid", None), ("skewed", None), ("prefill", None),
+    ("M1", synth.Workload("M1", 1, 128, 64, 4, 1, "uniform", 21)),
+    ("topk1", synth.Workload("topk1", 333, 128, 64, 7, 1, "uniform", 22)),
+    ("E1", synth.Workload("E1", 100, 128, 64, 1, 1, "uniform", 23)),
+    ("E1023", synth.Workload("E1023", 3000, 128, 64, 1023, 8, "zipf", 24)),
+    ("bigR", synth.Workload("bigR", 20000, 128, 64, 300, 5, "biased", 25)),
+]
+
+
+@pytest.mark.parametrize("name,w", SORT_CASES, ids=[c[0] for c in SORT_CASES])
+def test_route_sort_bit_exact(name, w):
+    w = w or synth.CONFIGS[name]
+    ei, _ = synth.routing(w.seed, w.M, w.E, w.topK, w.routing)
+    ref = oracle.route_sort(ei, w.E)
+    s, x, tpe, cs = _sort_on_gpu(w, ei)
+    assert_bits_equal(s, ref["sorted_src_route"], "sorted_src_route")
+    assert_bits_equal(x, ref["expanded_row_idx"], "expanded_row_idx")
+    assert_bits_equal(tpe, ref["tokens_per_expert"], "tokens_per_expert")
+    assert_bits_equal(cs, ref["cumsum"], "cumsum")
+
+
+@pytest.mark.parametrize("M", [40, 9000])
+def test_route_sort_invalid_ids_and_hot_expert(M):
+    w = synth.Workload("inv", M, 128, 64, 16, 4, "uniform", 31)
+    ei, _ = synth.routing(w.seed, w.M, w.E, w.topK, "uniform")
+    ei[::7, 0] = -3
+    ei[::11, 1] = 16  # == E: out of range
+    ei[1::5, 2] = 5   # hot expert
+    ref = oracle.route_sort(ei, w.E)
+    assert ref["invalid"] > 0
+    s, x, tpe, cs = _sort_on_gpu(w, ei)
+    assert_bits_equal(s, ref["sorted_src_route"], "sorted_src_route")
+    assert_bits_equal(x, ref["expanded_row_idx"], "expanded_row_idx")
+    assert_bits_equal(tpe, ref["tokens_per_expert"], "tokens_per_expert")
+    assert_bits_equal(cs, ref["cumsum"], "cumsum")
+
+
+# ------------------------------------------------------------------ token quant
+@pytest.mark.parametrize("M,K", [(16, 256), (128, 7168), (37, 4096), (5, 16384), (3, 128)])
+def test_quant_tokens_bit_exact(M, K):
+    x = synth.normal_f16(41, 1, (M, K))
+    x[min(2, M - 1)] = 0  # an all-zero token
+    xq_ref, pts_ref = oracle.quant_tokens(x)
+    d = moe.dims(M, K, 64, 4, 1)
+    xq8, xq16, pts = empty((M, K), torch.int8), empty((M, K), torch.float16), empty(M, torch.float32)
+    moe.moe_quant_tokens(d, dev(x), xq8, xq16, pts)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(xq8), xq_ref, "xq")
+    assert_bits_equal(host(pts), pts_ref, "pts1")
+    assert_bits_equal(host(xq16), xq_ref.astype(np.float16), "xq as binary16")
+
+
+# ------------------------------------------------------------------ GEMMs
+def _stage_inputs(w):
+    inp = synth.make_inputs(w)
+    rs = oracle.route_sort(inp["expert_idx"], w.E)
+    xq, pts1 = oracle.quant_tokens(inp["x"])
+    return inp, rs, xq, pts1
+
+
+GEMM_CASES = [
+    synth.Workload("g_small", 40, 256, 128, 8, 2, "uniform", 51),           # T=16 tile
+    synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # T=32 tile, ragged rows
+    synth.Workload("g_big", 384, 1024, 256, 4, 2, "zipf", 53),              # T=64 tile, hot expert
+    synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # many 512-deep chunks
+]
+
+
+@pytest.mark.parametrize("w", GEMM_CASES, ids=[w.name for w in GEMM_CASES])
+def test_gmm1_bit_exact(w):
+    inp, rs, xq, pts1 = _stage_inputs(w)
+    Rv = w.R - rs["invalid"]
+    _, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], inp["expert_idx"], inp["w1"], inp["s1"], Rv)
+    d = _dims(w)
+    c1 = torch.full((w.R, 2 * w.I), float("nan"), dtype=torch.float16, device="cuda")
+    ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
+    moe.moe_gmm1(d, dev(xq.astype(np.float16)), dev(rs["sorted_src_route"]), dev(rs["cumsum"]),
+                 dev(inp["w1"]), dev(inp["s1"]), c1, ws)
+    assert moe.moe_workspace_status(ws) == 0
+    assert_bits_equal(host(c1)[:Rv], c1_ref, "c1")
+
+
+@pytest.mark.parametrize("w", GEMM_CASES, ids=[w.name for w in GEMM_CASES])
+def test_gmm2_bit_exact(w):
+    inp, rs, xq, pts1 = _stage_inputs(w)
+    Rv = w.R - rs["invalid"]
+    q2 = synth.int8_sym127(w.seed, 77, (Rv, w.I))
+    _, c2_ref = oracle.gmm2(q2, rs["sorted_src_route"], inp["expert_idx"], inp["w2"], inp["s2"])
+    d = _dims(w)
+    c2 = empty((w.R, w.K), torch.float16)
+    ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
+    q2f = np.zeros((w.R, w.I), np.float16)
+    q2f[:Rv] = q2
+    moe.moe_gmm2(d, dev(q2f), dev(rs["cumsum"]), dev(inp["w2"]), dev(inp["s2"]), c2, ws)
+    assert moe.moe_workspace_status(ws) == 0
+    assert_bits_equal(host(c2)[:Rv], c2_ref, "c2")
+
+
+def test_gmm_accumulator_exact_beyond_fp32_mantissa():
+    """Partial sums far above 2^24 that cancel to a small integer.  The reduction
+    runs +127*127 terms, then small terms, then -127*127 terms: a single fp32
+    accumulator would reach ~5.6e7 (ulp 4) while adding the small terms and lose
+    them; the exact chunked accumulation must return them bit for bit (scale 1,
+    |acc| < 2048, so binary16 holds the integer exactly)."""
+    M, K, I, E = 8, 7168, 64, 1
+    mid = 168
+    h = (K - mid) // 2
+    rng = np.random.default_rng(5)
+    xq = np.empty((M, K), np.int8)
+    xq[:, :h], xq[:, h + mid:] = 127, -127
+    xq[:, h:h + mid] = rng.integers(-2, 3, (M, mid))
+    w1 = np.empty((E, 2 * I, K), np.int8)
+    w1[0, :, :h], w1[0, :, h + mid:] = 127, 127
+    w1[0, :, h:h + mid] = rng.integers(-3, 4, (2 * I, mid))
+    s1 = np.ones((E, 2 * I), np.float32)
+    ei = np.zeros((M, 1), np.int32)
+    rs = oracle.route_sort(ei, E)
+    acc_ref, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], ei, w1, s1, M, want_acc=True)
+    assert np.abs(acc_ref).max() < 2048 and np.count_nonzero(acc_ref) > acc_ref.size // 2
+    d = moe.dims(M, K, I, E, 1)
+    c1 = empty((M, 2 * I), torch.float16)
+    ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
+    moe.moe_gmm1(d, dev(xq.astype(np.float16)), dev(rs["sorted_src_route"]), dev(rs["cumsum"]),
+                 dev(w1), dev(s1), c1, ws)
+    got = host(c1).astype(np.float64)
+    assert np.array_equal(got, acc_ref.astype(np.float64))
+
+
+def test_gmm_empty_experts_and_single_rows():
+    """Experts with 0 and 1 rows, and a row tile tail of every length."""
+    w = synth.Workload("sparse", 23, 256, 64, 12, 1, "uniform", 61)
+    inp, rs, xq, pts1 = _stage_inputs(w)
+    inp["expert_idx"][:, 0] = np.array([0, 3, 3, 5, 5, 5] + [7] * 17, np.int32)
+    rs = oracle.route_sort(inp["expert_idx"], w.E)
+    _, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], inp["expert_idx"], inp["w1"], inp["s1"], w.R)
+    d = _dims(w)
+    c1 = empty((w.R, 2 * w.I), torch.float16)
+    ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
+    moe.moe_gmm1(d, dev(xq.astype(np.float16)), dev(rs["sorted_src_route"]), dev(rs["cumsum"]),
+                 dev(inp["w1"]), dev(inp["s1"]), c1, ws)
+    assert_bits_equal(host(c1), c1_ref, "c1")
+
+
+# ------------------------------------------------------------------ SwiGLU
+@pytest.mark.parametrize("R,I", [(64, 256), (300, 2048), (77, 1408), (5, 8192)])
+def test_swiglu_quant(R, I):
+    rng = np.random.default_rng(R + I)
+    c1 = (rng.standard_normal((R, 2 * I)) * 1500).astype(np.float16)
+    c1[1] = 0
+    topK = 1
+    M = R
+    pts1 = rng.uniform(0.02, 0.05, M).astype(np.float32)
+    sorted_src = rng.permutation(R).astype(np.int32)
+    cumsum = np.array([R], np.int32)
+    q2_ref, pts2_ref = oracle.swiglu_quant(c1, pts1, sorted_src, topK)
+    d = moe.dims(M, 128, I, 1, 1)
+    q8, q16, p2 = empty((R, I), torch.int8), empty((R, I), torch.float16), empty(R, torch.float32)
+    moe.moe_swiglu_quant(d, dev(c1), dev(pts1), dev(sorted_src), dev(cumsum), q8, q16, p2)
+    torch.cuda.synchronize()
+    assert_q2_close(host(q8), q2_ref)
+    assert np.array_equal(host(q16).astype(np.int8), host(q8))
+    np.testing.assert_allclose(host(p2), pts2_ref, rtol=1e-6, atol=0)
+
+
+# ------------------------------------------------------------------ Combine + Unpermute
+@pytest.mark.parametrize("cfg", ["tiny", "decode", "prefill"])
+def test_combine_unpermute_bit_exact(cfg):
+    w = synth.CONFIGS[cfg]
+    ei, probs = synth.routing(w.seed, w.M, w.E, w.topK, w.routing)
+    ei[0, 0] = -1  # one invalid route
+    rs = oracle.route_sort(ei, w.E)
+    Rv = w.R - rs["invalid"]
+    rng = np.random.default_rng(7)
+    c2 = (rng.standard_normal((w.R, w.K)) * 400).astype(np.float16)
+    pts2 = rng.uniform(20, 200, w.R).astype(np.float32)
+    dmat = oracle.combine(c2[:Rv], pts2[:Rv])
+    out_ref = oracle.unpermute(dmat, rs["expanded_row_idx"], probs)
+    d = _dims(w)
+    out = empty((w.M, w.K), torch.float16)
+    moe.moe_combine_unpermute(d, dev(c2), dev(pts2), dev(rs["expanded_row_idx"]), dev(probs), out)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(out), out_ref, "out")
