@@ -14,7 +14,8 @@
  *   - binary16 values are passed as uint16_t bit patterns (IEEE half).
  *   - Every pointer argument is DEVICE memory owned by the caller, except where a
  *     parameter name ends in _host.  The library never allocates or frees device
- *     memory; scratch space comes from the caller's `workspace`.
+ *     memory; scratch space comes from the caller's `workspace` (moe_route_sort_noalloc
+ *     alone uses a fixed scratch array inside the library instead).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  No entry point synchronises, except moe_layer_fwd_host and
  *     moe_workspace_status, which say so.
@@ -22,7 +23,7 @@
  *     be 16-byte aligned.
  *   - Preconditions checked on the host before anything is launched:
  *       M >= 1, 1 <= topK <= E <= 1023, K % 128 == 0, 128 <= K <= 16384,
- *       I % 64 == 0, 64 <= I <= 8192, M * topK < 2^31 / 2I, current device sm_103.
+ *       I % 64 == 0, 64 <= I <= 8192, M * topK < 2^24, current device sm_103.
  *     A violated precondition returns an error and launches nothing.
  *   - Routes whose expert id lies outside [0, E) are dropped: sorted after all
  *     valid routes, counted in no expert, expandedRowIdx = -1, and they add
@@ -157,6 +158,32 @@ int32_t moe_route_sort(const moe_dims_t* d, const int32_t* expert_idx, int32_t* 
  */
 int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, int8_t* xq_i8, uint16_t* xq_f16,
                          float* pts1, void* stream);
+
+/*
+ * Allocation-free route sort.  The paper has no counterpart: this entry point
+ * exists for callers that cannot allocate device memory when they sort (an
+ * engine plugin whose host engine owns all device memory, a server that
+ * reserved the whole device up front, a loop where cudaMalloc's implicit
+ * synchronisation is not allowed).  It computes exactly what moe_route_sort
+ * computes, but takes no workspace: its scratch is a fixed 512 KiB array in the
+ * library's own device memory, which every GPU that loads the library holds
+ * until the process exits.
+ *   - Supports M * topK <= MOE_ROUTE_SORT_NOALLOC_MAX_ROUTES (and the usual
+ *     E <= 1023); larger sizes return MOE_ERR_SHAPE and launch nothing.
+ *   - Allocates and frees nothing (no cudaMalloc/cudaFree, no library allocator).
+ *   - The first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one scratch array: calls that may overlap on the GPU
+ *     (different streams without ordering between them) race and must not be
+ *     issued.  Calls ordered on one stream are safe; nothing in the scratch needs
+ *     clearing between them.
+ * Arguments as for moe_route_sort, minus the workspace.
+ */
+#define MOE_ROUTE_SORT_NOALLOC_MAX_ROUTES 524288
+int32_t moe_route_sort_noalloc(const moe_dims_t* d, const int32_t* expert_idx, int32_t* sorted_src_route,
+                               int32_t* expanded_row_idx, int32_t* tokens_per_expert, int32_t* cumsum,
+                               void* stream);
 
 /* Workspace bytes of moe_gmm1 / moe_gmm2 (status word). */
 size_t moe_gmm_workspace_size(const moe_dims_t* d);

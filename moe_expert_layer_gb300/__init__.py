@@ -25,7 +25,7 @@ EXPORTS = [
     "moe_layer_host_workspace_size", "moe_layer_fwd_host", "moe_workspace_status",
     "moe_workspace_clear_status", "moe_route_sort_workspace_size", "moe_route_sort",
     "moe_quant_tokens", "moe_gmm_workspace_size", "moe_gmm1", "moe_swiglu_quant", "moe_gmm2",
-    "moe_combine_unpermute",
+    "moe_combine_unpermute", "moe_route_sort_noalloc",
 ]
 
 
@@ -74,6 +74,7 @@ def load_library(path=None):
         "moe_swiglu_quant": ([D] + [vp] * 8, i32),
         "moe_gmm2": ([D] + [vp] * 6 + [sz, vp], i32),
         "moe_combine_unpermute": ([D] + [vp] * 6, i32),
+        "moe_route_sort_noalloc": ([D] + [vp] * 6, i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -183,3 +184,16 @@ def moe_combine_unpermute(d, c2, pts2, expanded_row_idx, probs, out, stream=None
     _check("moe_combine_unpermute", load_library().moe_combine_unpermute(
         ctypes.byref(d), _p(c2), _p(pts2), _p(expanded_row_idx), _p(probs), _p(out),
         _stream(stream)))
+
+
+# Largest route count (M * topK) moe_route_sort_noalloc accepts (its fixed scratch).
+ROUTE_SORT_NOALLOC_MAX_ROUTES = 524288
+
+
+def moe_route_sort_noalloc(d, expert_idx, sorted_src_route, expanded_row_idx, tokens_per_expert,
+                           cumsum, stream=None):
+    """moe_route_sort without a workspace, for callers that cannot allocate device
+    memory; its scratch is a fixed array inside the library (see the header)."""
+    _check("moe_route_sort_noalloc", load_library().moe_route_sort_noalloc(
+        ctypes.byref(d), _p(expert_idx), _p(sorted_src_route), _p(expanded_row_idx),
+        _p(tokens_per_expert), _p(cumsum), _stream(stream)))

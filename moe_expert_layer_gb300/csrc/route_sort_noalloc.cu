@@ -1,0 +1,76 @@
+// Allocation-free variant of the route sort (moe_route_sort_noalloc).
+//
+// Some callers cannot allocate device memory at the moment they need the
+// sort: a plugin's enqueue callback inside an inference engine that has
+// already handed all device memory to its own pool, a server that reserved
+// the whole device up front for its caches, or a latency-critical loop in which
+// a cudaMalloc (which can synchronise the device) is not allowed.  For them,
+// the sort's scratch (per-block histograms and per-block insertion offsets of
+// the multi-block path) lives in a fixed array in this library's device memory
+// instead of a caller-provided workspace.  The caller still passes the inputs
+// and outputs.
+//
+// The array is a file-scope __device__ symbol: every GPU that loads the
+// library holds it until the process exits.  Host code cannot use the
+// symbol's name as a device address, so the first call on each device looks the
+// address up with cudaGetSymbolAddress (with that device current) and caches
+// it; that first call should therefore come before any stream capture.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// Multi-block path: 8192 routes per block, E + 1 <= 1024 buckets, two tables.
+constexpr int kRoutesPerBlock = 8192;
+constexpr int kMaxBlocks = MOE_ROUTE_SORT_NOALLOC_MAX_ROUTES / kRoutesPerBlock;
+constexpr size_t kScratchInts = 2u * kMaxBlocks * 1024u;  // 128 Ki int32 = 512 KiB
+
+static __device__ __align__(256) int32_t g_route_sort_scratch[kScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+int32_t* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once per device).
+cudaError_t scratch_address(int32_t** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_route_sort_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int32_t moe_route_sort_noalloc(const moe_dims_t* d, const int32_t* expert_idx, int32_t* sorted_src_route,
+                                          int32_t* expanded_row_idx, int32_t* tokens_per_expert, int32_t* cumsum,
+                                          void* stream) {
+  if (!d) return MOE_ERR_NULL;
+  if (d->M < 1 || d->topK < 1 || d->E < d->topK || d->E > 1023) return MOE_ERR_SHAPE;
+  const int64_t R = (int64_t)d->M * d->topK;
+  if (R > MOE_ROUTE_SORT_NOALLOC_MAX_ROUTES) return MOE_ERR_SHAPE;  // beyond the fixed scratch
+  if (!expert_idx || !sorted_src_route || !expanded_row_idx || !tokens_per_expert || !cumsum) return MOE_ERR_NULL;
+  int dev = -1, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess || major != 10 ||
+      minor != 3)
+    return MOE_ERR_ARCH;
+  int32_t* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_LAUNCH;
+  // The kernels write every scratch entry they later read (histogram, then
+  // offsets), so the previous call's contents need no clearing.
+  const cudaError_t e = moe::launch_route_sort(expert_idx, (int)R, d->E, sorted_src_route, expanded_row_idx,
+                                               tokens_per_expert, cumsum, scratch, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
