@@ -70,7 +70,7 @@ def algorithmic(w, expert_idx):
     K, I, M = w.K, w.I, w.M
     st = {}
     st["route_sort"] = {"bytes": 4 * R + 8 * R + 8 * w.E}
-    st["quant"] = {"bytes": 2 * M * K + 2 * M * K + 4 * M}
+    st["quant"] = {"bytes": 2 * M * K + 2 * R * K + 4 * M}  # read x, write the expert-major codes
     st["gmm1"] = {"bytes": active * 2 * I * K + active * 2 * I * 4 + R * K * 2 + R * 2 * I * 2,
                   "ops": 2 * R * K * 2 * I}
     st["swiglu"] = {"bytes": R * 2 * I * 2 + R * I * 2 + 8 * R}
@@ -278,7 +278,7 @@ def main():
     sorted_, expanded = torch.empty(R, dtype=i32, device="cuda"), torch.empty(R, dtype=i32, device="cuda")
     tpe, cs = torch.empty(w.E, dtype=i32, device="cuda"), torch.empty(w.E, dtype=i32, device="cuda")
     sws = torch.empty(max(16, moe.moe_route_sort_workspace_size(d)), dtype=torch.uint8, device="cuda")
-    xq16, pts1 = torch.empty((w.M, w.K), dtype=f16, device="cuda"), torch.empty(w.M, dtype=f32, device="cuda")
+    a1, pts1 = torch.empty((R, w.K), dtype=f16, device="cuda"), torch.empty(w.M, dtype=f32, device="cuda")
     c1 = torch.empty((R, 2 * w.I), dtype=f16, device="cuda")
     q2, pts2 = torch.empty((R, w.I), dtype=f16, device="cuda"), torch.empty(R, dtype=f32, device="cuda")
     c2 = torch.empty((R, w.K), dtype=f16, device="cuda")
@@ -289,9 +289,9 @@ def main():
         evs[0].record(stream)
         moe.moe_route_sort(d, dev["expert_idx"], sorted_, expanded, tpe, cs, sws, stream)
         evs[1].record(stream)
-        moe.moe_quant_tokens(d, dev["x"], None, xq16, pts1, stream)
+        moe.moe_quant_dispatch(d, dev["x"], expanded, a1, pts1, stream)
         evs[2].record(stream)
-        moe.moe_gmm1(d, xq16, sorted_, cs, dev["w1"], dev["s1"], c1, gws, stream)
+        moe.moe_gmm1(d, a1, cs, dev["w1"], dev["s1"], c1, gws, stream)
         evs[3].record(stream)
         moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, None, q2, pts2, stream)
         evs[4].record(stream)

@@ -152,8 +152,8 @@ int32_t moe_route_sort(const moe_dims_t* d, const int32_t* expert_idx, int32_t* 
  * q = round-half-away(x / pts1), clamped to [-127, 127]; an all-zero token gets
  * pts1 = 0 and zero codes.
  *   xq_i8  [M][K] int8 codes (may be NULL)
- *   xq_f16 [M][K] the same codes as binary16 integers, the operand format the
- *          GEMMs read (may be NULL; at least one of the two must be given)
+ *   xq_f16 [M][K] the same codes as binary16 integers (may be NULL; at least
+ *          one of the two must be given)
  *   pts1   [M]    fp32 scales
  */
 int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, int8_t* xq_i8, uint16_t* xq_f16,
@@ -185,21 +185,30 @@ int32_t moe_route_sort_noalloc(const moe_dims_t* d, const int32_t* expert_idx, i
                                int32_t* expanded_row_idx, int32_t* tokens_per_expert, int32_t* cumsum,
                                void* stream);
 
+/*
+ * FrontReorder phase 2c with the quant-scatter (page section "1. FrontReorder"):
+ * quantise every token once (as moe_quant_tokens) and write its codes, as
+ * binary16 integers, to each of its expanded rows:
+ *   a1_f16[expanded_row_idx[t*topK + j]][k] = q[t][k]   for every valid route j
+ * giving the expert-major GMM1 operand (rows of invalid routes are not written).
+ *   expanded_row_idx [R] from moe_route_sort; a1_f16 [R][K]; pts1 [M]
+ */
+int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t* expanded_row_idx,
+                           uint16_t* a1_f16, float* pts1, void* stream);
+
 /* Workspace bytes of moe_gmm1 / moe_gmm2 (status word). */
 size_t moe_gmm_workspace_size(const moe_dims_t* d);
 
 /*
- * Dispatch + GMM1 (page sections "2. Dispatch" and "3. GMM1"): for each valid
- * expanded row d of expert e (rows cumsum[e]-count_e .. cumsum[e]-1), token
- * t = sorted_src_route[d] / topK:
- *   acc[n]   = sum_k xq[t,k] * w1[e][n][k]                 (exact integer)
+ * GMM1 (page section "3. GMM1"): for each valid expanded row d of expert e
+ * (rows cumsum[e]-count_e .. cumsum[e]-1):
+ *   acc[n]   = sum_k a1[d][k] * w1[e][n][k]                (exact integer)
  *   c1[d][n] = binary16(float(acc[n]) * s1[e][n])          n < 2I
- * The token rows are gathered straight from xq_f16; no dispatched copy is made.
- *   xq_f16 [M][K] binary16-coded int8 codes; c1 [R][2I] (rows >= cumsum[E-1] untouched)
+ *   a1_f16 [R][K] expert-major binary16-coded int8 codes (moe_quant_dispatch);
+ *   c1 [R][2I] (rows >= cumsum[E-1] untouched)
  */
-int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* xq_f16, const int32_t* sorted_src_route,
-                 const int32_t* cumsum, const int8_t* w1, const float* s1, uint16_t* c1,
-                 void* workspace, size_t workspace_bytes, void* stream);
+int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int8_t* w1,
+                 const float* s1, uint16_t* c1, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * SwiGLU + dynamic requant (page section "4. SwiGLU"), per valid expanded row d

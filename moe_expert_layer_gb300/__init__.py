@@ -24,7 +24,7 @@ EXPORTS = [
     "moe_status_string", "moe_layer_workspace_size", "moe_layer_fwd",
     "moe_layer_host_workspace_size", "moe_layer_fwd_host", "moe_workspace_status",
     "moe_workspace_clear_status", "moe_route_sort_workspace_size", "moe_route_sort",
-    "moe_quant_tokens", "moe_gmm_workspace_size", "moe_gmm1", "moe_swiglu_quant", "moe_gmm2",
+    "moe_quant_tokens", "moe_quant_dispatch", "moe_gmm_workspace_size", "moe_gmm1", "moe_swiglu_quant", "moe_gmm2",
     "moe_combine_unpermute", "moe_route_sort_noalloc",
 ]
 
@@ -70,7 +70,8 @@ def load_library(path=None):
         "moe_route_sort": ([D] + [vp] * 6 + [sz, vp], i32),
         "moe_quant_tokens": ([D] + [vp] * 5, i32),
         "moe_gmm_workspace_size": ([D], sz),
-        "moe_gmm1": ([D] + [vp] * 7 + [sz, vp], i32),
+        "moe_quant_dispatch": ([D] + [vp] * 5, i32),
+        "moe_gmm1": ([D] + [vp] * 6 + [sz, vp], i32),
         "moe_swiglu_quant": ([D] + [vp] * 8, i32),
         "moe_gmm2": ([D] + [vp] * 6 + [sz, vp], i32),
         "moe_combine_unpermute": ([D] + [vp] * 6, i32),
@@ -162,10 +163,15 @@ def moe_quant_tokens(d, x, xq_i8, xq_f16, pts1, stream=None):
         ctypes.byref(d), _p(x), _p(xq_i8), _p(xq_f16), _p(pts1), _stream(stream)))
 
 
-def moe_gmm1(d, xq_f16, sorted_src_route, cumsum, w1, s1, c1, workspace, stream=None):
+def moe_quant_dispatch(d, x, expanded_row_idx, a1_f16, pts1, stream=None):
+    _check("moe_quant_dispatch", load_library().moe_quant_dispatch(
+        ctypes.byref(d), _p(x), _p(expanded_row_idx), _p(a1_f16), _p(pts1), _stream(stream)))
+
+
+def moe_gmm1(d, a1_f16, cumsum, w1, s1, c1, workspace, stream=None):
     _check("moe_gmm1", load_library().moe_gmm1(
-        ctypes.byref(d), _p(xq_f16), _p(sorted_src_route), _p(cumsum), _p(w1), _p(s1), _p(c1),
-        _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+        ctypes.byref(d), _p(a1_f16), _p(cumsum), _p(w1), _p(s1), _p(c1), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def moe_swiglu_quant(d, c1, pts1, sorted_src_route, cumsum, q2_i8, q2_f16, pts2, stream=None):

@@ -1,5 +1,6 @@
 // The layer's row-wise, HBM-bound stages:
-//   token quant        (PTO-ISA MegaMoE operator page, "1. FrontReorder", phase 2c)
+//   token quant (+ scatter of each token's codes to its expert-major rows)
+//                      (PTO-ISA MegaMoE operator page, "1. FrontReorder", phase 2c)
 //   SwiGLU + requant   (same page, "4. SwiGLU")
 //   Combine+Unpermute  (same page, "6. Combine" and "7. Unpermute"), fused
 // Rows are read with 16-byte vector loads kept in registers, so each input byte
@@ -24,11 +25,16 @@ constexpr int kRowThreads = 256;
 // --------------------------------------------------------------------------
 // per-token dynamic quant: pts1 = amax / 127, q = round_half_away(x / pts1)
 // --------------------------------------------------------------------------
+// With `expanded_row_idx` set, the codes of token t are also written (as binary16)
+// to row expanded_row_idx[t*topK + j] of `a1` for every valid route j: the
+// expert-major GMM1 operand (FrontReorder's quant-scatter into offsetA).
 template <int VPT>
 __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half* __restrict__ x, int K,
                                                                    int8_t* __restrict__ xq_i8,
                                                                    __half* __restrict__ xq_f16,
-                                                                   float* __restrict__ pts1) {
+                                                                   float* __restrict__ pts1,
+                                                                   const int32_t* __restrict__ expanded_row_idx,
+                                                                   int topK, __half* __restrict__ a1) {
   __shared__ float red[kRowThreads / 32];
   const int t = blockIdx.x;
   const int nvec = K >> 3;
@@ -63,11 +69,17 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
                    ((uint32_t)(q[7] & 0xff) << 24);
         reinterpret_cast<uint2*>(xq_i8 + (size_t)t * K)[idx] = packed;
       }
-      if (xq_f16) {
+      if (xq_f16 || expanded_row_idx) {
         Vec8h o;
 #pragma unroll
         for (int j = 0; j < 8; ++j) o.h[j] = __int2half_rn(q[j]);
-        reinterpret_cast<int4*>(xq_f16 + (size_t)t * K)[idx] = o.v;
+        if (xq_f16) reinterpret_cast<int4*>(xq_f16 + (size_t)t * K)[idx] = o.v;
+        if (expanded_row_idx) {
+          for (int s = 0; s < topK; ++s) {
+            const int d = __ldg(expanded_row_idx + (size_t)t * topK + s);
+            if (d >= 0) reinterpret_cast<int4*>(a1 + (size_t)d * K)[idx] = o.v;
+          }
+        }
       }
     }
   }
@@ -174,19 +186,20 @@ __global__ void __launch_bounds__(kCombineThreads) combine_unpermute_kernel(
 }  // namespace
 
 cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16, float* pts1,
-                                cudaStream_t stream) {
+                                const int32_t* expanded_row_idx, int topK, uint16_t* a1, cudaStream_t stream) {
   const int nvec = K / 8;
   const int vpt = (nvec + kRowThreads - 1) / kRowThreads;
   const __half* xh = reinterpret_cast<const __half*>(x);
   __half* qf = reinterpret_cast<__half*>(xq_f16);
+  __half* ah = reinterpret_cast<__half*>(a1);
   if (vpt <= 1)
-    quant_tokens_kernel<1><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1);
+    quant_tokens_kernel<1><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
   else if (vpt <= 2)
-    quant_tokens_kernel<2><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1);
+    quant_tokens_kernel<2><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
   else if (vpt <= 4)
-    quant_tokens_kernel<4><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1);
+    quant_tokens_kernel<4><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
   else if (vpt <= 8)
-    quant_tokens_kernel<8><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1);
+    quant_tokens_kernel<8><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -1,0 +1,425 @@
+// Grouped W8A8 GEMM of the expert layer on warp-level tensor-core MMAs
+// (PTO-ISA MegaMoE operator page, sections "3. GMM1" and "5. GMM2"): the engine
+// for row tiles of up to 32 rows (decode-sized batches, a few rows per expert).
+//
+// For expert e with rows [cumsum[e]-cnt_e, cumsum[e]) of the expert-major row
+// space and every output channel n < N:
+//     acc        = sum_k a[row][k] * W[e][n][k]          exact integer
+//     C[row][n]  = sat_f16(float(acc) * scale[e][n])
+//
+// Engine.  GB300 runs int8 tensor-core and dp4a arithmetic at a small fraction
+// of its binary16 rate, so the int8 operands are multiplied on the fp16 tensor
+// path: every int8 value is exact in binary16, every product (|p| <= 127^2) is
+// exact, and an fp32 accumulator is exact as long as all partial sums stay
+// below 2^24 in magnitude.  The reduction is therefore split into chunks of 512
+// (512 * 127^2 < 2^23); each chunk's fp32 sum is converted to int32 and added in
+// integer registers, which makes the int32 accumulator bit-exact for any K.
+//
+// Data movement.  Weights stay int8 in HBM (they dominate the traffic): a TMA
+// box of 128 channels x 64 k lands in shared memory and each thread converts its
+// fragment to binary16 in registers (byte-permute into the 1024+v encoding, one
+// subtract).  Activations are binary16-coded int8 (produced so by the quant and
+// SwiGLU kernels), loaded by TMA with the 128-byte swizzle; for GMM1 each token
+// row is fetched by its own 1-row TMA box at the token index taken from the sort,
+// so no dispatched copy of the tokens is ever written.
+//
+// Tiling.  One CTA computes 128 channels x T rows of one expert.  The work list
+// (expert, row tile) is derived by each CTA from cumsum; CTAs whose index lies
+// beyond the number of row tiles exit at once.  The reduction is swapped so that
+// weights are the MMA's M operand (16 channels per m16n8k16) and token rows its
+// N operand, which keeps the tensor work proportional to the real row count for
+// the 1-16 rows per expert of decode-sized batches.
+#include "common.cuh"
+#include "kernels.h"
+#include "tensor_map.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;  // 8 MMA warps + 1 TMA producer warp
+constexpr int kBN = 128;         // channels per work item
+constexpr int kBK = 128;         // reduction depth per pipeline stage (128-byte weight rows)
+constexpr int kChunkStages = 4;  // 4 * 128 = 512-deep exact fp32 chunks
+constexpr int kMaxExperts = 1024;
+
+template <int T>
+struct TileShape;
+template <>
+struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 8; };
+template <>
+struct TileShape<32> { static constexpr int WM = 4, WN = 2, STAGES = 7; };
+template <>
+struct TileShape<64> { static constexpr int WM = 4, WN = 2, STAGES = 6; };
+
+template <int T>
+struct GemmCfg {
+  static constexpr int WARPS_M = TileShape<T>::WM;
+  static constexpr int WARPS_N = TileShape<T>::WN;
+  static constexpr int STAGES = TileShape<T>::STAGES;
+  static constexpr int MT = kBN / (16 * WARPS_M);  // m16 tiles per warp
+  static constexpr int NT = T / (8 * WARPS_N);     // n8 tiles per warp
+  // independent fp32 partial accumulators per output fragment (k-slices are dealt
+  // round-robin), so that at least 8 MMA chains are in flight per warp
+  static constexpr int P = (MT * NT >= 8) ? 1 : 8 / (MT * NT);
+  static constexpr int X_HALF_BYTES = T * 128;     // [T][64] binary16, 128-B swizzled rows
+  static constexpr int X_BYTES = 2 * X_HALF_BYTES;
+  static constexpr int W_BYTES = kBN * kBK;        // [128][128] int8, 128-B swizzled rows
+  static constexpr int STAGE_BYTES = X_BYTES + W_BYTES;
+  static constexpr int EPI_BYTES = T * kBN * 2;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
+  static_assert(WARPS_M * WARPS_N == kConsumerWarps, "warp grid");
+  static_assert(X_HALF_BYTES % 1024 == 0, "1024-B alignment of swizzled tiles");
+  static_assert(SMEM_BYTES + 9 * 1024 <= 227 * 1024, "shared memory");
+};
+
+struct GemmArgs {
+  const int32_t* cumsum;
+  const float* scale;
+  __half* C;
+  int32_t* status;
+  int E, N, Kd;
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// 4 int8 (one 32-bit word) -> two half2 {b0,b1}, {b2,b3}, exactly.
+// Byte v+128 placed in the mantissa of 0x6400 (=1024) gives 1024+v+128;
+// subtracting 1152 leaves v.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a = __byte_perm(u, 0x6464u, 0x5140u);
+  uint32_t b = __byte_perm(u, 0x6464u, 0x5342u);
+  const uint32_t bias = 0x64806480u;  // half2(1152, 1152)
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
+
+// MMA row i of an m16 tile reads weight channel perm(i) of the tile, chosen so
+// that the two rows an 8-lane shared-memory phase reads differ in bit 2: with the
+// 128-byte swizzle their 16-byte chunks then land in disjoint bank groups.
+__device__ __forceinline__ int mrow_perm(int g) { return (g >> 1) + ((g & 1) << 2); }
+
+struct Item {
+  int e, cb, row0, rows;
+};
+
+// Work item j -> (expert, channel block, first row, rows).  Items are ordered
+// expert-major, then channel block, then row tile, so CTAs that run at the
+// same time share weight blocks through L2.
+template <int T>
+__device__ __forceinline__ Item decode_item(int j, const int* s_pref, const int* s_end, int E, int n_cb) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_pref[mid] <= j) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int start = e ? s_end[e - 1] : 0;
+  const int cnt = s_end[e] - start;
+  const int n_rt = (cnt + T - 1) / T;
+  const int local = j - s_pref[e];
+  const int cb = local / n_rt, rt = local - cb * n_rt;
+  Item it;
+  it.e = e;
+  it.cb = cb;
+  it.row0 = start + rt * T;
+  it.rows = min(T, cnt - rt * T);
+  return it;
+}
+
+template <int T>
+__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
+                                                                       const __grid_constant__ CUtensorMap tm_x,
+                                                                       const GemmArgs args) {
+  using Cfg = GemmCfg<T>;
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[S];
+  __shared__ __align__(8) uint64_t empty_bar[S];
+  __shared__ int s_pref[kMaxExperts + 1];  // first work item of each expert
+  __shared__ int s_end[kMaxExperts];       // cumsum
+  __shared__ int s_wsum[kConsumerWarps];
+  __shared__ int s_abort, s_issued, s_consumed;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = args.E, n_cb = args.N / kBN;
+  const int nk = (args.Kd + kBK - 1) / kBK;  // a 64-deep tail reads TMA zero fill
+
+  // ---- work list: s_pref[e] = sum over e' < e of ceil(cnt_e' / T) * n_cb
+  if (threadIdx.x < kConsumerWarps * 32) {
+    const int per = (E + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+    const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+    int local = 0;
+    for (int e = e0; e < e1; ++e) {
+      const int hi = __ldg(args.cumsum + e), lo = e ? __ldg(args.cumsum + e - 1) : 0;
+      s_end[e] = hi;
+      local += (hi - lo + T - 1) / T * n_cb;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    consumer_bar();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += s_wsum[w];
+    for (int e = e0; e < e1; ++e) {
+      s_pref[e] = run;
+      const int lo = e ? s_end[e - 1] : 0;
+      run += (s_end[e] - lo + T - 1) / T * n_cb;
+    }
+    if (e0 < E && e1 == E) s_pref[E] = run;
+  } else if (lane == 0) {
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_x);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    s_abort = 0;
+    s_issued = 0;
+    s_consumed = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int total = s_pref[E];
+
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
+
+  if (warp == kConsumerWarps) {
+    // ================= TMA producer warp =================
+    int slot = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    for (int j = blockIdx.x; j < total; j += gridDim.x) {
+      const Item it = decode_item<T>(j, s_pref, s_end, E, n_cb);
+      const int w_row = it.e * args.N + it.cb * kBN;
+      const uint32_t tx = (uint32_t)Cfg::W_BYTES + (uint32_t)T * 256u;
+      for (int kb = 0; kb < nk; ++kb) {
+        bool ok = true;
+        if (lane == 0) {
+          ok = !*(volatile int*)&s_abort && mbar_wait_bounded(&empty_bar[slot], phase ^ 1u);
+          if (!ok) {
+            s_abort = 1;
+            record_status(args.status, MOE_ERR_TIMEOUT);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) goto producer_done;
+        uint8_t* xs = smem_gen + slot * Cfg::STAGE_BYTES;
+        uint8_t* ws = xs + Cfg::X_BYTES;
+        const int kx = kb * kBK;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full_bar[slot], tx);
+          tma_load_2d(ws, &tm_w, kx, w_row, &full_bar[slot]);
+          tma_load_2d(xs, &tm_x, kx, it.row0, &full_bar[slot]);
+          tma_load_2d(xs + Cfg::X_HALF_BYTES, &tm_x, kx + 64, it.row0, &full_bar[slot]);
+        }
+        ++issued;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  producer_done:
+    if (lane == 0) s_issued = issued;
+  } else {
+    // ================= MMA consumer warps =================
+    const int warp_m = warp % Cfg::WARPS_M, warp_n = warp / Cfg::WARPS_M;
+    const int g = lane >> 2, tq = lane & 3;
+    const int pg = mrow_perm(g);
+    __half* stile = reinterpret_cast<__half*>(smem_gen + S * Cfg::STAGE_BYTES);
+    int slot = 0;
+    uint32_t phase = 0;
+    int consumed = 0;
+    bool ok = true;
+    for (int j = blockIdx.x; j < total && ok; j += gridDim.x) {
+      const Item it = decode_item<T>(j, s_pref, s_end, E, n_cb);
+      // channel scales of this item, loaded early so the k-loop hides their latency
+      const float* sc = args.scale + (size_t)it.e * args.N + it.cb * kBN;
+      float s_lo[Cfg::MT], s_hi[Cfg::MT];
+#pragma unroll
+      for (int mt = 0; mt < Cfg::MT; ++mt) {
+        const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
+        s_lo[mt] = __ldg(sc + m);
+        s_hi[mt] = __ldg(sc + m + 8);
+      }
+      float accf[Cfg::P][Cfg::MT][Cfg::NT][4];
+      int acci[Cfg::MT][Cfg::NT][4];
+#pragma unroll
+      for (int mt = 0; mt < Cfg::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < Cfg::NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int q = 0; q < Cfg::P; ++q) accf[q][mt][nt][i] = 0.0f;
+            acci[mt][nt][i] = 0;
+          }
+      // n8 tiles of this warp that hold real rows (the rest are skipped)
+      const int live_nt = min(Cfg::NT, max(0, (it.rows - warp_n * Cfg::NT * 8 + 7) / 8));
+
+      for (int kb = 0; kb < nk; ++kb) {
+        ok = !*(volatile int*)&s_abort && mbar_wait_bounded(&full_bar[slot], phase);
+        if (!ok) {
+          s_abort = 1;
+          record_status(args.status, MOE_ERR_TIMEOUT);
+          break;
+        }
+        const uint32_t xs = smem_base + slot * Cfg::STAGE_BYTES;
+        const uint32_t ws = xs + Cfg::X_BYTES;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t xh = xs + h * Cfg::X_HALF_BYTES;
+          // B fragments: binary16 k = 64h + 16tq .. +15 of token row n (swizzled chunks 2tq, 2tq+1)
+          uint4 bfrag[Cfg::NT][2];
+#pragma unroll
+          for (int nt = 0; nt < Cfg::NT; ++nt) {
+            if (nt >= live_nt) break;
+            const int n = warp_n * Cfg::NT * 8 + nt * 8 + g;
+            const uint32_t rb = xh + n * 128;
+            bfrag[nt][0] = lds128(rb + (((2 * tq) ^ (n & 7)) << 4));
+            bfrag[nt][1] = lds128(rb + (((2 * tq + 1) ^ (n & 7)) << 4));
+          }
+#pragma unroll
+          for (int mt = 0; mt < Cfg::MT; ++mt) {
+            // A fragments: int8 k = 64h + 16tq .. +15 of channels perm(g) and 8 + perm(g)
+            const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
+            const uint4 alo = lds128(ws + m * kBK + (((4 * h + tq) ^ (m & 7)) << 4));
+            const uint4 ahi = lds128(ws + (m + 8) * kBK + (((4 * h + tq) ^ (m & 7)) << 4));
+            const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
+            const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+#pragma unroll
+            for (int sl = 0; sl < 4; ++sl) {
+              uint32_t a0, a2, a1, a3;
+              i8x4_to_f16x4(aw_lo[sl], a0, a2);  // row perm(g):   k 4sl,4sl+1 | 4sl+2,4sl+3
+              i8x4_to_f16x4(aw_hi[sl], a1, a3);  // row 8+perm(g)
+#pragma unroll
+              for (int nt = 0; nt < Cfg::NT; ++nt) {
+                if (nt >= live_nt) break;
+                const uint4& bv = bfrag[nt][sl >> 1];
+                const uint32_t b0 = (sl & 1) ? bv.z : bv.x;
+                const uint32_t b1 = (sl & 1) ? bv.w : bv.y;
+                mma_f16_16816(accf[sl % Cfg::P][mt][nt], a0, a1, a2, a3, b0, b1);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+        ++consumed;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        // drain the exact fp32 chunk into the int32 accumulators
+        if ((kb + 1) % kChunkStages == 0 || kb + 1 == nk) {
+#pragma unroll
+          for (int mt = 0; mt < Cfg::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < Cfg::NT; ++nt)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int q = 0; q < Cfg::P; ++q) {
+                  acci[mt][nt][i] += __float2int_rn(accf[q][mt][nt][i]);
+                  accf[q][mt][nt][i] = 0.0f;
+                }
+              }
+        }
+      }
+      // ---- epilogue: scale, convert, stage [T][128] binary16, coalesced stores
+      consumer_bar();  // the previous item's stores have read the staging tile
+      if (ok) {
+#pragma unroll
+        for (int mt = 0; mt < Cfg::MT; ++mt) {
+          const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
+#pragma unroll
+          for (int nt = 0; nt < Cfg::NT; ++nt) {
+            const int n = warp_n * Cfg::NT * 8 + nt * 8 + 2 * tq;
+            stile[n * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(acci[mt][nt][0]), s_lo[mt]));
+            stile[(n + 1) * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(acci[mt][nt][1]), s_lo[mt]));
+            stile[n * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(acci[mt][nt][2]), s_hi[mt]));
+            stile[(n + 1) * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(acci[mt][nt][3]), s_hi[mt]));
+          }
+        }
+      }
+      consumer_bar();
+      ok = ok && !*(volatile int*)&s_abort;
+      if (ok) {
+        const int4* src = reinterpret_cast<const int4*>(stile);
+        __half* dst = args.C + (size_t)it.row0 * args.N + it.cb * kBN;
+        for (int i = threadIdx.x; i < it.rows * (kBN / 8); i += kConsumerWarps * 32) {
+          const int r = i / (kBN / 8), c = i % (kBN / 8);
+          reinterpret_cast<int4*>(dst + (size_t)r * args.N)[c] = src[r * (kBN / 8) + c];
+        }
+      }
+    }
+    if (threadIdx.x == 0) s_consumed = consumed;
+  }
+
+  __syncthreads();
+  if (s_abort && threadIdx.x == kConsumerWarps * 32) {
+    // let loads still in flight land before the CTA's shared memory is released
+    for (int n = s_consumed; n < s_issued; ++n) mbar_wait_bounded(&full_bar[n % S], (uint32_t)((n / S) & 1));
+  }
+}
+
+// ------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------
+template <int T>
+cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
+  using Cfg = GemmCfg<T>;
+  CUtensorMap tw, tx;
+  if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kBK,
+                            kBN))
+    return cudaErrorInvalidValue;
+  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, T))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<T>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  GemmArgs a;
+  a.cumsum = p.cumsum;
+  a.scale = p.scale;
+  a.C = reinterpret_cast<__half*>(p.C);
+  a.status = p.status;
+  a.E = p.E;
+  a.N = p.N;
+  a.Kd = p.Kd;
+  grouped_gemm_kernel<T><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream) {
+  return T <= 16 ? launch_t<16>(p, stream) : launch_t<32>(p, stream);
+}
+
+}  // namespace moe

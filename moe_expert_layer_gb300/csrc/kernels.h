@@ -14,7 +14,8 @@ cudaError_t launch_route_sort(const int32_t* expert_idx, int R, int E, int32_t* 
 
 // elementwise.cu
 cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16,
-                                float* pts1, cudaStream_t stream);
+                                float* pts1, const int32_t* expanded_row_idx, int topK, uint16_t* a1,
+                                cudaStream_t stream);
 cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int topK, const float* pts1,
                                 const int32_t* sorted_src_route, const int32_t* cumsum, int8_t* q2_i8,
                                 uint16_t* q2_f16, float* pts2, cudaStream_t stream);
@@ -22,23 +23,19 @@ cudaError_t launch_combine_unpermute(const uint16_t* c2, const float* pts2, cons
                                      const float* probs, int M, int K, int topK, uint16_t* out,
                                      cudaStream_t stream);
 
-// gemm.cu: grouped W8A8 GEMM over expert-major rows.
-//   GMM1 (gather = true):  rows gathered from act[token][Kd] with token = sorted_src_route[row] / topK
-//   GMM2 (gather = false): rows read from act[row][Kd]
-//   C[row][n] = sat_f16(float(sum_k act[.,k] * W[e][n][k]) * scale[e][n]),  n < N
+// Grouped W8A8 GEMM over expert-major rows (GMM1 and GMM2):
+//   C[row][n] = sat_f16(float(sum_k act[row][k] * W[e][n][k]) * scale[e][n]),  n < N
 struct GroupedGemmProblem {
-  const uint16_t* act;              // binary16-coded int8 activations
-  int act_rows;                     // rows of act (M for GMM1, R for GMM2)
-  const int32_t* sorted_src_route;  // gather only
-  int topK;
+  const uint16_t* act;              // [R][Kd] binary16-coded int8 activations, expert-major rows
   const int32_t* cumsum;            // [E] inclusive prefix of rows per expert
   const int8_t* w;                  // [E][N][Kd]
   const float* scale;               // [E][N]
   uint16_t* C;                      // [R][N]
   int R, E, N, Kd;
-  bool gather;
   int32_t* status;                  // device status word
 };
-cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream);
+cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream);     // picks an engine
+cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream);  // gemm_hmma.cu
+cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream);  // gemm_tc.cu
 
 }  // namespace moe

@@ -46,7 +46,7 @@ int32_t launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ER
 
 // Layout of the layer workspace.
 struct Layout {
-  size_t status, sorted, expanded, tpe, cumsum, sort_ws, xq16, pts1, c1, q2, pts2, c2, total;
+  size_t status, sorted, expanded, tpe, cumsum, sort_ws, a1, pts1, c1, q2, pts2, c2, total;
   // host-variant staging
   size_t hx, hei, hprobs, hout, host_total;
 };
@@ -66,7 +66,7 @@ Layout layout_of(const moe_dims_t* d) {
   L.tpe = take(E * 4);
   L.cumsum = take(E * 4);
   L.sort_ws = take(moe::route_sort_workspace_bytes((int)R, (int)E));
-  L.xq16 = take(M * K * 2);
+  L.a1 = take(R * K * 2);
   L.pts1 = take(M * 4);
   L.c1 = take(R * 2 * I * 2);
   L.q2 = take(R * I * 2);
@@ -95,7 +95,7 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   int32_t* expanded = at<int32_t>(ws, L.expanded);
   int32_t* tpe = at<int32_t>(ws, L.tpe);
   int32_t* cumsum = at<int32_t>(ws, L.cumsum);
-  uint16_t* xq16 = at<uint16_t>(ws, L.xq16);
+  uint16_t* a1 = at<uint16_t>(ws, L.a1);
   float* pts1 = at<float>(ws, L.pts1);
   uint16_t* c1 = at<uint16_t>(ws, L.c1);
   uint16_t* q2 = at<uint16_t>(ws, L.q2);
@@ -107,13 +107,12 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   if ((e = moe::launch_route_sort(expert_idx, R, E, sorted, expanded, tpe, cumsum, at<void>(ws, L.sort_ws), st)) !=
       cudaSuccess)
     return launch_status(e);
-  if ((e = moe::launch_quant_tokens(x, M, K, nullptr, xq16, pts1, st)) != cudaSuccess) return launch_status(e);
+  // quantise each token once and scatter its codes to its expert-major rows
+  if ((e = moe::launch_quant_tokens(x, M, K, nullptr, nullptr, pts1, expanded, topK, a1, st)) != cudaSuccess)
+    return launch_status(e);
 
   moe::GroupedGemmProblem g1{};
-  g1.act = xq16;
-  g1.act_rows = M;
-  g1.sorted_src_route = sorted;
-  g1.topK = topK;
+  g1.act = a1;
   g1.cumsum = cumsum;
   g1.w = w1;
   g1.scale = s1;
@@ -122,7 +121,6 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   g1.E = E;
   g1.N = 2 * I;
   g1.Kd = K;
-  g1.gather = true;
   g1.status = status;
   if ((e = moe::launch_grouped_gemm(g1, st)) != cudaSuccess) return launch_status(e);
 
@@ -131,9 +129,6 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
 
   moe::GroupedGemmProblem g2{};
   g2.act = q2;
-  g2.act_rows = R;
-  g2.sorted_src_route = nullptr;
-  g2.topK = topK;
   g2.cumsum = cumsum;
   g2.w = w2;
   g2.scale = s2;
@@ -142,7 +137,6 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   g2.E = E;
   g2.N = K;
   g2.Kd = I;
-  g2.gather = false;
   g2.status = status;
   if ((e = moe::launch_grouped_gemm(g2, st)) != cudaSuccess) return launch_status(e);
 
@@ -266,7 +260,19 @@ int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, int8_t* xq_i8, 
   if (!x || !pts1 || (!xq_i8 && !xq_f16)) return MOE_ERR_NULL;
   if (!aligned16(x) || (xq_i8 && !aligned16(xq_i8)) || (xq_f16 && !aligned16(xq_f16))) return MOE_ERR_ALIGN;
   if ((rc = check_device()) != MOE_OK) return rc;
-  return launch_status(moe::launch_quant_tokens(x, d->M, d->K, xq_i8, xq_f16, pts1, static_cast<cudaStream_t>(stream)));
+  return launch_status(moe::launch_quant_tokens(x, d->M, d->K, xq_i8, xq_f16, pts1, nullptr, 0, nullptr,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t* expanded_row_idx, uint16_t* a1_f16,
+                           float* pts1, void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!x || !expanded_row_idx || !a1_f16 || !pts1) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(a1_f16)) return MOE_ERR_ALIGN;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  return launch_status(moe::launch_quant_tokens(x, d->M, d->K, nullptr, nullptr, pts1, expanded_row_idx, d->topK,
+                                                a1_f16, static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_gmm_workspace_size(const moe_dims_t* d) {
@@ -274,20 +280,16 @@ size_t moe_gmm_workspace_size(const moe_dims_t* d) {
   return kAlign;
 }
 
-int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* xq_f16, const int32_t* sorted_src_route, const int32_t* cumsum,
-                 const int8_t* w1, const float* s1, uint16_t* c1, void* workspace, size_t workspace_bytes,
-                 void* stream) {
+int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int8_t* w1, const float* s1,
+                 uint16_t* c1, void* workspace, size_t workspace_bytes, void* stream) {
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
-  if (!xq_f16 || !sorted_src_route || !cumsum || !w1 || !s1 || !c1 || !workspace) return MOE_ERR_NULL;
-  if (!aligned16(xq_f16) || !aligned16(w1) || !aligned16(c1)) return MOE_ERR_ALIGN;
+  if (!a1_f16 || !cumsum || !w1 || !s1 || !c1 || !workspace) return MOE_ERR_NULL;
+  if (!aligned16(a1_f16) || !aligned16(w1) || !aligned16(c1)) return MOE_ERR_ALIGN;
   if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   moe::GroupedGemmProblem g{};
-  g.act = xq_f16;
-  g.act_rows = d->M;
-  g.sorted_src_route = sorted_src_route;
-  g.topK = d->topK;
+  g.act = a1_f16;
   g.cumsum = cumsum;
   g.w = w1;
   g.scale = s1;
@@ -296,7 +298,6 @@ int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* xq_f16, const int32_t* sor
   g.E = d->E;
   g.N = 2 * d->I;
   g.Kd = d->K;
-  g.gather = true;
   g.status = static_cast<int32_t*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
@@ -324,9 +325,6 @@ int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cum
   if ((rc = check_device()) != MOE_OK) return rc;
   moe::GroupedGemmProblem g{};
   g.act = q2_f16;
-  g.act_rows = d->M * d->topK;
-  g.sorted_src_route = nullptr;
-  g.topK = d->topK;
   g.cumsum = cumsum;
   g.w = w2;
   g.scale = s2;
@@ -335,7 +333,6 @@ int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cum
   g.E = d->E;
   g.N = d->K;
   g.Kd = d->I;
-  g.gather = false;
   g.status = static_cast<int32_t*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;

@@ -16,7 +16,12 @@ decode      128   7168   2048  256     8  uniform     1
 mid         512   7168   2048  256     8  biased      2
 skewed     2048   7168   2048  256     8  zipf1.2     3
 prefill    8192   4096   1408   64     6  uniform     4
+decode16      8   7168   2048   16     8  uniform     5
 ========  =====  =====  =====  ===  ====  =======  ====
+
+``decode16`` keeps decode's shapes and rows per expert (about 4) with 16
+experts, so that its weights (0.7 GB) stay above the L2 size while a
+counter capture of one GEMM launch remains small.
 
 x is binary16 N(0,1); w1/w2 are int8 uniform over [-127, 127]; s1/s2 are
 fp32 uniform on [1e-3, 1e-2).  Weight layout: w1[E][2I][K] and w2[E][K][I]
@@ -63,6 +68,7 @@ CONFIGS = {
     "mid": Workload("mid", 512, 7168, 2048, 256, 8, "biased", 2),
     "skewed": Workload("skewed", 2048, 7168, 2048, 256, 8, "zipf", 3),
     "prefill": Workload("prefill", 8192, 4096, 1408, 64, 6, "uniform", 4),
+    "decode16": Workload("decode16", 8, 7168, 2048, 16, 8, "uniform", 5),
 }
 
 

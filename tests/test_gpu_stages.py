@@ -90,7 +90,37 @@ def test_quant_tokens_bit_exact(M, K):
     assert_bits_equal(host(xq16), xq_ref.astype(np.float16), "xq as binary16")
 
 
+# ------------------------------------------------------------------ quant + scatter to expert-major rows
+@pytest.mark.parametrize("cfg", ["tiny", "decode", "prefill"])
+def test_quant_dispatch_bit_exact(cfg):
+    w = synth.CONFIGS[cfg]
+    x = synth.normal_f16(w.seed, 1, (w.M, w.K))
+    ei, _ = synth.routing(w.seed, w.M, w.E, w.topK, w.routing)
+    ei[1, 0] = -1  # an invalid route: its row is not written
+    rs = oracle.route_sort(ei, w.E)
+    xq_ref, pts_ref = oracle.quant_tokens(x)
+    Rv = w.R - rs["invalid"]
+    a1_ref = xq_ref[rs["sorted_src_route"][:Rv] // w.topK].astype(np.float16)
+    d = _dims(w)
+    a1 = torch.full((w.R, w.K), 7.0, dtype=torch.float16, device="cuda")
+    pts = empty(w.M, torch.float32)
+    moe.moe_quant_dispatch(d, dev(x), dev(rs["expanded_row_idx"]), a1, pts)
+    torch.cuda.synchronize()
+    got = host(a1)
+    assert_bits_equal(got[:Rv], a1_ref, "a1")
+    assert np.all(got[Rv:].astype(np.float32) == 7.0)  # rows past the valid ones untouched
+    assert_bits_equal(host(pts), pts_ref, "pts1")
+
+
 # ------------------------------------------------------------------ GEMMs
+def _a1(xq, rs, topK, R):
+    """Expert-major GMM1 operand built from the oracle's per-token codes."""
+    Rv = R - rs["invalid"]
+    a1 = np.zeros((R, xq.shape[1]), np.float16)
+    a1[:Rv] = xq[rs["sorted_src_route"][:Rv] // topK]
+    return a1
+
+
 def _stage_inputs(w):
     inp = synth.make_inputs(w)
     rs = oracle.route_sort(inp["expert_idx"], w.E)
@@ -103,6 +133,7 @@ GEMM_CASES = [
     synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # T=32 tile, ragged rows
     synth.Workload("g_big", 384, 1024, 256, 4, 2, "zipf", 53),              # T=64 tile, hot expert
     synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # many 512-deep chunks
+    synth.Workload("g_tiles", 700, 512, 192, 3, 2, "zipf", 55),             # 128-row tiles + tails, 64-deep tail
 ]
 
 
@@ -114,8 +145,7 @@ def test_gmm1_bit_exact(w):
     d = _dims(w)
     c1 = torch.full((w.R, 2 * w.I), float("nan"), dtype=torch.float16, device="cuda")
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(xq.astype(np.float16)), dev(rs["sorted_src_route"]), dev(rs["cumsum"]),
-                 dev(inp["w1"]), dev(inp["s1"]), c1, ws)
+    moe.moe_gmm1(d, dev(_a1(xq, rs, w.topK, w.R)), dev(rs["cumsum"]), dev(inp["w1"]), dev(inp["s1"]), c1, ws)
     assert moe.moe_workspace_status(ws) == 0
     assert_bits_equal(host(c1)[:Rv], c1_ref, "c1")
 
@@ -160,8 +190,7 @@ def test_gmm_accumulator_exact_beyond_fp32_mantissa():
     d = moe.dims(M, K, I, E, 1)
     c1 = empty((M, 2 * I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(xq.astype(np.float16)), dev(rs["sorted_src_route"]), dev(rs["cumsum"]),
-                 dev(w1), dev(s1), c1, ws)
+    moe.moe_gmm1(d, dev(_a1(xq, rs, 1, M)), dev(rs["cumsum"]), dev(w1), dev(s1), c1, ws)
     got = host(c1).astype(np.float64)
     assert np.array_equal(got, acc_ref.astype(np.float64))
 
@@ -176,8 +205,7 @@ def test_gmm_empty_experts_and_single_rows():
     d = _dims(w)
     c1 = empty((w.R, 2 * w.I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(xq.astype(np.float16)), dev(rs["sorted_src_route"]), dev(rs["cumsum"]),
-                 dev(inp["w1"]), dev(inp["s1"]), c1, ws)
+    moe.moe_gmm1(d, dev(_a1(xq, rs, 1, w.R)), dev(rs["cumsum"]), dev(inp["w1"]), dev(inp["s1"]), c1, ws)
     assert_bits_equal(host(c1), c1_ref, "c1")
 
 
