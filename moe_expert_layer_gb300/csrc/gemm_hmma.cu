@@ -37,21 +37,17 @@ namespace moe {
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;  // 8 MMA warps + 1 TMA producer warp
+constexpr int kGroupWarps = 8;                        // MMA warps per k-half group
+constexpr int kConsumerWarps = 2 * kGroupWarps;       // group h computes k-half h of every stage
+constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;  // + 1 TMA producer warp
 constexpr int kBN = 128;         // channels per work item
 constexpr int kBK = 128;         // reduction depth per pipeline stage (128-byte weight rows)
-constexpr int kChunkStages = 4;  // 4 * 128 = 512-deep exact fp32 chunks
 constexpr int kMaxExperts = 1024;
 
 template <int T>
 struct TileShape;
 template <>
 struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 8; };
-template <>
-struct TileShape<32> { static constexpr int WM = 4, WN = 2, STAGES = 7; };
-template <>
-struct TileShape<64> { static constexpr int WM = 4, WN = 2, STAGES = 6; };
 
 template <int T>
 struct GemmCfg {
@@ -62,14 +58,15 @@ struct GemmCfg {
   static constexpr int NT = T / (8 * WARPS_N);     // n8 tiles per warp
   // independent fp32 partial accumulators per output fragment (k-slices are dealt
   // round-robin), so that at least 8 MMA chains are in flight per warp
-  static constexpr int P = (MT * NT >= 8) ? 1 : 8 / (MT * NT);
+  static constexpr int P = (MT * NT >= 4) ? 1 : 4 / (MT * NT);
   static constexpr int X_HALF_BYTES = T * 128;     // [T][64] binary16, 128-B swizzled rows
   static constexpr int X_BYTES = 2 * X_HALF_BYTES;
   static constexpr int W_BYTES = kBN * kBK;        // [128][128] int8, 128-B swizzled rows
   static constexpr int STAGE_BYTES = X_BYTES + W_BYTES;
   static constexpr int EPI_BYTES = T * kBN * 2;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + 1024;
-  static_assert(WARPS_M * WARPS_N == kConsumerWarps, "warp grid");
+  static constexpr int PART_BYTES = kGroupWarps * MT * NT * 4 * 32 * 4;  // k-half-1 partial sums
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + PART_BYTES + 1024;
+  static_assert(WARPS_M * WARPS_N == kGroupWarps, "warp grid");
   static_assert(X_HALF_BYTES % 1024 == 0, "1024-B alignment of swizzled tiles");
   static_assert(SMEM_BYTES + 9 * 1024 <= 227 * 1024, "shared memory");
 };
@@ -245,10 +242,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     if (lane == 0) s_issued = issued;
   } else {
     // ================= MMA consumer warps =================
-    const int warp_m = warp % Cfg::WARPS_M, warp_n = warp / Cfg::WARPS_M;
+    // Group grp (8 warps) computes k bytes [64*grp, 64*grp+64) of every stage; the
+    // two groups' exact int32 partial sums are added in the epilogue.
+    const int grp = warp / kGroupWarps, wig = warp % kGroupWarps;
+    const int warp_m = wig % Cfg::WARPS_M, warp_n = wig / Cfg::WARPS_M;
     const int g = lane >> 2, tq = lane & 3;
     const int pg = mrow_perm(g);
     __half* stile = reinterpret_cast<__half*>(smem_gen + S * Cfg::STAGE_BYTES);
+    int* spart = reinterpret_cast<int*>(smem_gen + S * Cfg::STAGE_BYTES + Cfg::EPI_BYTES) +
+                 wig * (Cfg::MT * Cfg::NT * 4 * 32) + lane;
     int slot = 0;
     uint32_t phase = 0;
     int consumed = 0;
@@ -286,42 +288,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           record_status(args.status, MOE_ERR_TIMEOUT);
           break;
         }
-        const uint32_t xs = smem_base + slot * Cfg::STAGE_BYTES;
-        const uint32_t ws = xs + Cfg::X_BYTES;
+        const uint32_t xh = smem_base + slot * Cfg::STAGE_BYTES + grp * Cfg::X_HALF_BYTES;
+        const uint32_t ws = smem_base + slot * Cfg::STAGE_BYTES + Cfg::X_BYTES;
+        // B fragments: binary16 k = 64grp + 16tq .. +15 of row n (swizzled chunks 2tq, 2tq+1)
+        uint4 bfrag[Cfg::NT][2];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t xh = xs + h * Cfg::X_HALF_BYTES;
-          // B fragments: binary16 k = 64h + 16tq .. +15 of token row n (swizzled chunks 2tq, 2tq+1)
-          uint4 bfrag[Cfg::NT][2];
+        for (int nt = 0; nt < Cfg::NT; ++nt) {
+          if (nt >= live_nt) break;
+          const int n = warp_n * Cfg::NT * 8 + nt * 8 + g;
+          const uint32_t rb = xh + n * 128;
+          bfrag[nt][0] = lds128(rb + (((2 * tq) ^ (n & 7)) << 4));
+          bfrag[nt][1] = lds128(rb + (((2 * tq + 1) ^ (n & 7)) << 4));
+        }
 #pragma unroll
-          for (int nt = 0; nt < Cfg::NT; ++nt) {
-            if (nt >= live_nt) break;
-            const int n = warp_n * Cfg::NT * 8 + nt * 8 + g;
-            const uint32_t rb = xh + n * 128;
-            bfrag[nt][0] = lds128(rb + (((2 * tq) ^ (n & 7)) << 4));
-            bfrag[nt][1] = lds128(rb + (((2 * tq + 1) ^ (n & 7)) << 4));
-          }
+        for (int mt = 0; mt < Cfg::MT; ++mt) {
+          // A fragments: int8 k = 64grp + 16tq .. +15 of channels perm(g) and 8 + perm(g)
+          const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
+          const uint4 alo = lds128(ws + m * kBK + (((4 * grp + tq) ^ (m & 7)) << 4));
+          const uint4 ahi = lds128(ws + (m + 8) * kBK + (((4 * grp + tq) ^ (m & 7)) << 4));
+          const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
+          const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
 #pragma unroll
-          for (int mt = 0; mt < Cfg::MT; ++mt) {
-            // A fragments: int8 k = 64h + 16tq .. +15 of channels perm(g) and 8 + perm(g)
-            const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
-            const uint4 alo = lds128(ws + m * kBK + (((4 * h + tq) ^ (m & 7)) << 4));
-            const uint4 ahi = lds128(ws + (m + 8) * kBK + (((4 * h + tq) ^ (m & 7)) << 4));
-            const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
-            const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+          for (int sl = 0; sl < 4; ++sl) {
+            uint32_t a0, a2, a1, a3;
+            i8x4_to_f16x4(aw_lo[sl], a0, a2);  // row perm(g):   k 4sl,4sl+1 | 4sl+2,4sl+3
+            i8x4_to_f16x4(aw_hi[sl], a1, a3);  // row 8+perm(g)
 #pragma unroll
-            for (int sl = 0; sl < 4; ++sl) {
-              uint32_t a0, a2, a1, a3;
-              i8x4_to_f16x4(aw_lo[sl], a0, a2);  // row perm(g):   k 4sl,4sl+1 | 4sl+2,4sl+3
-              i8x4_to_f16x4(aw_hi[sl], a1, a3);  // row 8+perm(g)
-#pragma unroll
-              for (int nt = 0; nt < Cfg::NT; ++nt) {
-                if (nt >= live_nt) break;
-                const uint4& bv = bfrag[nt][sl >> 1];
-                const uint32_t b0 = (sl & 1) ? bv.z : bv.x;
-                const uint32_t b1 = (sl & 1) ? bv.w : bv.y;
-                mma_f16_16816(accf[sl % Cfg::P][mt][nt], a0, a1, a2, a3, b0, b1);
-              }
+            for (int nt = 0; nt < Cfg::NT; ++nt) {
+              if (nt >= live_nt) break;
+              const uint4& bv = bfrag[nt][sl >> 1];
+              const uint32_t b0 = (sl & 1) ? bv.z : bv.x;
+              const uint32_t b1 = (sl & 1) ? bv.w : bv.y;
+              mma_f16_16816(accf[sl % Cfg::P][mt][nt], a0, a1, a2, a3, b0, b1);
             }
           }
         }
@@ -332,8 +330,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           slot = 0;
           phase ^= 1u;
         }
-        // drain the exact fp32 chunk into the int32 accumulators
-        if ((kb + 1) % kChunkStages == 0 || kb + 1 == nk) {
+        // drain the exact fp32 chunk (at most 8 stages x 64 = 512 deep) into int32
+        if ((kb + 1) % 8 == 0 || kb + 1 == nk) {
 #pragma unroll
           for (int mt = 0; mt < Cfg::MT; ++mt)
 #pragma unroll
@@ -348,19 +346,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
               }
         }
       }
-      // ---- epilogue: scale, convert, stage [T][128] binary16, coalesced stores
+      // ---- epilogue: add the k-half-1 partials, scale, convert, stage [T][128]
+      // binary16, coalesced stores
       consumer_bar();  // the previous item's stores have read the staging tile
-      if (ok) {
+      if (grp == 1) {
+#pragma unroll
+        for (int mt = 0; mt < Cfg::MT; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < Cfg::NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) spart[((mt * Cfg::NT + nt) * 4 + i) * 32] = acci[mt][nt][i];
+      }
+      consumer_bar();
+      if (grp == 0 && ok) {
 #pragma unroll
         for (int mt = 0; mt < Cfg::MT; ++mt) {
           const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
 #pragma unroll
           for (int nt = 0; nt < Cfg::NT; ++nt) {
             const int n = warp_n * Cfg::NT * 8 + nt * 8 + 2 * tq;
-            stile[n * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(acci[mt][nt][0]), s_lo[mt]));
-            stile[(n + 1) * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(acci[mt][nt][1]), s_lo[mt]));
-            stile[n * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(acci[mt][nt][2]), s_hi[mt]));
-            stile[(n + 1) * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(acci[mt][nt][3]), s_hi[mt]));
+            int v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = acci[mt][nt][i] + spart[((mt * Cfg::NT + nt) * 4 + i) * 32];
+            stile[n * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(v[0]), s_lo[mt]));
+            stile[(n + 1) * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(v[1]), s_lo[mt]));
+            stile[n * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(v[2]), s_hi[mt]));
+            stile[(n + 1) * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(v[3]), s_hi[mt]));
           }
         }
       }
@@ -419,7 +430,8 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream) {
-  return T <= 16 ? launch_t<16>(p, stream) : launch_t<32>(p, stream);
+  (void)T;  // 16-row tiles (the engine serves decode-sized batches)
+  return launch_t<16>(p, stream);
 }
 
 }  // namespace moe
