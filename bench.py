@@ -2,9 +2,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode] [--impl reference]
 
-One step = one pass of the whole layer (route sort, token quant, GMM1 with the
-fused gather, SwiGLU + requant, GMM2, Combine + Unpermute) over one batch of the
-workload's seeded synthetic inputs.  With N > 1 (torchrun, one process per GPU)
+One step = one pass of the whole layer (route sort, token quant with the scatter
+to expert-major rows, GMM1, SwiGLU + requant, GMM2, Combine + Unpermute) over one
+batch of the workload's seeded synthetic inputs.  With N > 1 (torchrun, one process per GPU)
 every rank runs an independent replica of the layer on its own batch: the path
 has no exchange step, so there is no collective on the data path (weak scaling).
 
@@ -185,10 +185,17 @@ def cpu_baseline(w, inp):
 
 
 # ----------------------------------------------------------------------------- ncu traffic record
-def traffic_record(kernel_file):
-    """dram bytes per launch of the dominant kernel from the committed ncu summary,
-    valid only while the kernel source is unchanged since the capture."""
-    p = os.path.join(ROOT, "profiles", "gmm1_decode_ncu.md")
+def engine_source(w):
+    """Source file of the GEMM engine the library picks for this workload."""
+    name = "gemm_hmma.cu" if w.R / w.E <= 12.0 else "gemm_tc.cu"
+    return os.path.join(ROOT, "moe_expert_layer_gb300", "csrc", name)
+
+
+def traffic_record(stage, workload, kernel_file):
+    """dram bytes per launch of the dominant kernel from the committed ncu summary
+    (profiles/<stage>_<workload>_ncu.md), valid only while the kernel source is
+    unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "%s_%s_ncu.md" % (stage, workload))
     if not os.path.exists(p):
         return None
     text = open(p).read()
@@ -328,7 +335,7 @@ def main():
                 "frac": round(ach / peaks["hbm_gbs"], 3),
                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
                 "algorithmic_bytes_per_launch": alg[dom]["bytes"],
-                "traffic": traffic_record(os.path.join(ROOT, "moe_expert_layer_gb300", "csrc", "gemm.cu"))}
+                "traffic": traffic_record(dom, w.name, engine_source(w))}
     layer_ops = alg["gmm1"]["ops"] + alg["gmm2"]["ops"]
 
     # ---- end to end through the host-buffer entry point
