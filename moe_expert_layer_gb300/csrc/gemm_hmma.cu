@@ -58,7 +58,7 @@ struct GemmCfg {
   static constexpr int NT = T / (8 * WARPS_N);     // n8 tiles per warp
   // independent fp32 partial accumulators per output fragment (k-slices are dealt
   // round-robin), so that at least 8 MMA chains are in flight per warp
-  static constexpr int P = (MT * NT >= 4) ? 1 : 4 / (MT * NT);
+  static constexpr int P = (MT * NT >= 8) ? 1 : 8 / (MT * NT);
   static constexpr int X_HALF_BYTES = T * 128;     // [T][64] binary16, 128-B swizzled rows
   static constexpr int X_BYTES = 2 * X_HALF_BYTES;
   static constexpr int W_BYTES = kBN * kBK;        // [128][128] int8, 128-B swizzled rows
@@ -106,7 +106,53 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+
+// One 64-deep k-half of one stage for one warp: A fragments from the int8 weight tile
+// (widened in registers), B fragments from the binary16 row tile, NTL live n8 tiles.
+template <class Cfg, int NTL>
+__device__ __forceinline__ void hmma_half_stage(uint32_t xh, uint32_t ws, int grp, int warp_m, int warp_n, int g,
+                                                int tq, int pg, float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
+  // B fragments: binary16 k = 64grp + 16tq .. +15 of row n (swizzled chunks 2tq, 2tq+1)
+  uint4 bfrag[NTL][2];
+#pragma unroll
+  for (int nt = 0; nt < NTL; ++nt) {
+    const int n = warp_n * Cfg::NT * 8 + nt * 8 + g;
+    const uint32_t rb = xh + n * 128;
+    bfrag[nt][0] = lds128(rb + (((2 * tq) ^ (n & 7)) << 4));
+    bfrag[nt][1] = lds128(rb + (((2 * tq + 1) ^ (n & 7)) << 4));
+  }
+#pragma unroll
+  for (int mt = 0; mt < Cfg::MT; ++mt) {
+    // A fragments: int8 k = 64grp + 16tq .. +15 of channels perm(g) and 8 + perm(g)
+    const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
+    const uint4 alo = lds128(ws + m * kBK + (((4 * grp + tq) ^ (m & 7)) << 4));
+    const uint4 ahi = lds128(ws + (m + 8) * kBK + (((4 * grp + tq) ^ (m & 7)) << 4));
+    const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
+    const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
+#pragma unroll
+    for (int sl = 0; sl < 4; ++sl) {
+      uint32_t a0, a2, a1, a3;
+      i8x4_to_f16x4(aw_lo[sl], a0, a2);  // row perm(g):   k 4sl,4sl+1 | 4sl+2,4sl+3
+      i8x4_to_f16x4(aw_hi[sl], a1, a3);  // row 8+perm(g)
+#pragma unroll
+      for (int nt = 0; nt < NTL; ++nt) {
+        const uint4& bv = bfrag[nt][sl >> 1];
+        const uint32_t b0 = (sl & 1) ? bv.z : bv.x;
+        const uint32_t b1 = (sl & 1) ? bv.w : bv.y;
+        mma_f16_16816(accf[sl % Cfg::P][mt][nt], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
+__device__ __forceinline__ void group0_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kGroupWarps * 32)); }
+
+__device__ __forceinline__ bool wait_part(uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_wait_bounded(bar, parity)) return true;
+  record_status(status, MOE_ERR_TIMEOUT);
+  return false;
+}
 
 // MMA row i of an m16 tile reads weight channel perm(i) of the tile, chosen so
 // that the two rows an 8-lane shared-memory phase reads differ in bit 2: with the
@@ -144,12 +190,14 @@ __device__ __forceinline__ Item decode_item(int j, const int* s_pref, const int*
 template <int T>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                                                                        const __grid_constant__ CUtensorMap tm_x,
+                                                                       const __grid_constant__ CUtensorMap tm_x8,
                                                                        const GemmArgs args) {
   using Cfg = GemmCfg<T>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[S];
   __shared__ __align__(8) uint64_t empty_bar[S];
+  __shared__ __align__(8) uint64_t part_full_bar, part_empty_bar;  // k-half-1 partials hand-off
   __shared__ int s_pref[kMaxExperts + 1];  // first work item of each expert
   __shared__ int s_end[kMaxExperts];       // cumsum
   __shared__ int s_wsum[kConsumerWarps];
@@ -188,10 +236,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   } else if (lane == 0) {
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_x8);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
+    mbar_init(&part_full_bar, kGroupWarps);
+    mbar_init(&part_empty_bar, kGroupWarps);
     s_abort = 0;
     s_issued = 0;
     s_consumed = 0;
@@ -211,7 +262,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     for (int j = blockIdx.x; j < total; j += gridDim.x) {
       const Item it = decode_item<T>(j, s_pref, s_end, E, n_cb);
       const int w_row = it.e * args.N + it.cb * kBN;
-      const uint32_t tx = (uint32_t)Cfg::W_BYTES + (uint32_t)T * 256u;
+      // tiles of at most 8 rows (most decode tiles) load an 8-row token box
+      const bool small = (T > 8) && (it.rows <= 8);
+      const void* tmx = small ? static_cast<const void*>(&tm_x8) : static_cast<const void*>(&tm_x);
+      const uint32_t tx = (uint32_t)Cfg::W_BYTES + (uint32_t)(small ? 8 : T) * 256u;
       for (int kb = 0; kb < nk; ++kb) {
         bool ok = true;
         if (lane == 0) {
@@ -228,8 +282,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         if (lane == 0) {
           mbar_arrive_expect_tx(&full_bar[slot], tx);
           tma_load_2d(ws, &tm_w, kx, w_row, &full_bar[slot]);
-          tma_load_2d(xs, &tm_x, kx, it.row0, &full_bar[slot]);
-          tma_load_2d(xs + Cfg::X_HALF_BYTES, &tm_x, kx + 64, it.row0, &full_bar[slot]);
+          tma_load_2d(xs, tmx, kx, it.row0, &full_bar[slot]);
+          tma_load_2d(xs + Cfg::X_HALF_BYTES, tmx, kx + 64, it.row0, &full_bar[slot]);
         }
         ++issued;
         if (++slot == S) {
@@ -253,7 +307,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                  wig * (Cfg::MT * Cfg::NT * 4 * 32) + lane;
     int slot = 0;
     uint32_t phase = 0;
-    int consumed = 0;
+    int consumed = 0, n_items = 0;
     bool ok = true;
     for (int j = blockIdx.x; j < total && ok; j += gridDim.x) {
       const Item it = decode_item<T>(j, s_pref, s_end, E, n_cb);
@@ -290,39 +344,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
         const uint32_t xh = smem_base + slot * Cfg::STAGE_BYTES + grp * Cfg::X_HALF_BYTES;
         const uint32_t ws = smem_base + slot * Cfg::STAGE_BYTES + Cfg::X_BYTES;
-        // B fragments: binary16 k = 64grp + 16tq .. +15 of row n (swizzled chunks 2tq, 2tq+1)
-        uint4 bfrag[Cfg::NT][2];
-#pragma unroll
-        for (int nt = 0; nt < Cfg::NT; ++nt) {
-          if (nt >= live_nt) break;
-          const int n = warp_n * Cfg::NT * 8 + nt * 8 + g;
-          const uint32_t rb = xh + n * 128;
-          bfrag[nt][0] = lds128(rb + (((2 * tq) ^ (n & 7)) << 4));
-          bfrag[nt][1] = lds128(rb + (((2 * tq + 1) ^ (n & 7)) << 4));
-        }
-#pragma unroll
-        for (int mt = 0; mt < Cfg::MT; ++mt) {
-          // A fragments: int8 k = 64grp + 16tq .. +15 of channels perm(g) and 8 + perm(g)
-          const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
-          const uint4 alo = lds128(ws + m * kBK + (((4 * grp + tq) ^ (m & 7)) << 4));
-          const uint4 ahi = lds128(ws + (m + 8) * kBK + (((4 * grp + tq) ^ (m & 7)) << 4));
-          const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
-          const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
-#pragma unroll
-          for (int sl = 0; sl < 4; ++sl) {
-            uint32_t a0, a2, a1, a3;
-            i8x4_to_f16x4(aw_lo[sl], a0, a2);  // row perm(g):   k 4sl,4sl+1 | 4sl+2,4sl+3
-            i8x4_to_f16x4(aw_hi[sl], a1, a3);  // row 8+perm(g)
-#pragma unroll
-            for (int nt = 0; nt < Cfg::NT; ++nt) {
-              if (nt >= live_nt) break;
-              const uint4& bv = bfrag[nt][sl >> 1];
-              const uint32_t b0 = (sl & 1) ? bv.z : bv.x;
-              const uint32_t b1 = (sl & 1) ? bv.w : bv.y;
-              mma_f16_16816(accf[sl % Cfg::P][mt][nt], a0, a1, a2, a3, b0, b1);
-            }
-          }
-        }
+        // one uniform branch per stage on the number of live n8 tiles
+        if (live_nt >= 2)
+          hmma_half_stage<Cfg, Cfg::NT>(xh, ws, grp, warp_m, warp_n, g, tq, pg, accf);
+        else if (live_nt == 1)
+          hmma_half_stage<Cfg, 1>(xh, ws, grp, warp_m, warp_n, g, tq, pg, accf);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slot]);
         ++consumed;
@@ -346,45 +372,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
               }
         }
       }
-      // ---- epilogue: add the k-half-1 partials, scale, convert, stage [T][128]
-      // binary16, coalesced stores
-      consumer_bar();  // the previous item's stores have read the staging tile
+      // ---- epilogue.  Group 1 hands its int32 partials to group 0 through shared
+      // memory (part_full / part_empty) and moves on to the next item; group 0 adds
+      // them, scales, converts, stages [T][128] binary16 and stores it coalesced.
       if (grp == 1) {
+        bool got = true;
+        if (n_items > 0) got = wait_part(&part_empty_bar, (n_items - 1) & 1, args.status);
+        got = __all_sync(0xffffffffu, got);
+        if (got && ok) {
+#pragma unroll
+          for (int mt = 0; mt < Cfg::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < Cfg::NT; ++nt)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) spart[((mt * Cfg::NT + nt) * 4 + i) * 32] = acci[mt][nt][i];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&part_full_bar);
+        ok = ok && got;
+      } else {
+        bool got = wait_part(&part_full_bar, n_items & 1, args.status);
+        got = __all_sync(0xffffffffu, got);
+        int v[Cfg::MT][Cfg::NT][4];
 #pragma unroll
         for (int mt = 0; mt < Cfg::MT; ++mt)
 #pragma unroll
           for (int nt = 0; nt < Cfg::NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) spart[((mt * Cfg::NT + nt) * 4 + i) * 32] = acci[mt][nt][i];
-      }
-      consumer_bar();
-      if (grp == 0 && ok) {
+            for (int i = 0; i < 4; ++i)
+              v[mt][nt][i] = acci[mt][nt][i] + (got ? spart[((mt * Cfg::NT + nt) * 4 + i) * 32] : 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&part_empty_bar);
+        ok = ok && got;
+        group0_bar();  // group 0's stores of the previous item have read the staging tile
+        if (ok) {
 #pragma unroll
-        for (int mt = 0; mt < Cfg::MT; ++mt) {
-          const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
+          for (int mt = 0; mt < Cfg::MT; ++mt) {
+            const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
 #pragma unroll
-          for (int nt = 0; nt < Cfg::NT; ++nt) {
-            const int n = warp_n * Cfg::NT * 8 + nt * 8 + 2 * tq;
-            int v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = acci[mt][nt][i] + spart[((mt * Cfg::NT + nt) * 4 + i) * 32];
-            stile[n * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(v[0]), s_lo[mt]));
-            stile[(n + 1) * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(v[1]), s_lo[mt]));
-            stile[n * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(v[2]), s_hi[mt]));
-            stile[(n + 1) * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(v[3]), s_hi[mt]));
+            for (int nt = 0; nt < Cfg::NT; ++nt) {
+              const int n = warp_n * Cfg::NT * 8 + nt * 8 + 2 * tq;
+              stile[n * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(v[mt][nt][0]), s_lo[mt]));
+              stile[(n + 1) * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(v[mt][nt][1]), s_lo[mt]));
+              stile[n * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(v[mt][nt][2]), s_hi[mt]));
+              stile[(n + 1) * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(v[mt][nt][3]), s_hi[mt]));
+            }
+          }
+        }
+        group0_bar();
+        ok = ok && !*(volatile int*)&s_abort;
+        if (ok) {
+          const int4* src = reinterpret_cast<const int4*>(stile);
+          __half* dst = args.C + (size_t)it.row0 * args.N + it.cb * kBN;
+          for (int i = threadIdx.x; i < it.rows * (kBN / 8); i += kGroupWarps * 32) {
+            const int r = i / (kBN / 8), c = i % (kBN / 8);
+            reinterpret_cast<int4*>(dst + (size_t)r * args.N)[c] = src[r * (kBN / 8) + c];
           }
         }
       }
-      consumer_bar();
-      ok = ok && !*(volatile int*)&s_abort;
-      if (ok) {
-        const int4* src = reinterpret_cast<const int4*>(stile);
-        __half* dst = args.C + (size_t)it.row0 * args.N + it.cb * kBN;
-        for (int i = threadIdx.x; i < it.rows * (kBN / 8); i += kConsumerWarps * 32) {
-          const int r = i / (kBN / 8), c = i % (kBN / 8);
-          reinterpret_cast<int4*>(dst + (size_t)r * args.N)[c] = src[r * (kBN / 8) + c];
-        }
-      }
+      ++n_items;
     }
     if (threadIdx.x == 0) s_consumed = consumed;
   }
@@ -406,7 +452,9 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kBK,
                             kBN))
     return cudaErrorInvalidValue;
-  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, T))
+  CUtensorMap tx8;
+  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, T) ||
+      !encode_tensor_map_2d(&tx8, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, 8))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -423,7 +471,7 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.E = p.E;
   a.N = p.N;
   a.Kd = p.Kd;
-  grouped_gemm_kernel<T><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, a);
+  grouped_gemm_kernel<T><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
   return cudaGetLastError();
 }
 
