@@ -79,12 +79,6 @@ struct GemmArgs {
   int E, N, Kd;
 };
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
 // 4 int8 (one 32-bit word) -> two half2 {b0,b1}, {b2,b3}, exactly.
 // Byte v+128 placed in the mantissa of 0x6400 (=1024) gives 1024+v+128;
 // subtracting 1152 leaves v.
@@ -97,9 +91,10 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
 }
 
+// Not volatile: the compiler may reorder MMAs against independent loads and ALU work.
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -110,23 +105,26 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 // One 64-deep k-half of one stage for one warp: A fragments from the int8 weight tile
 // (widened in registers), B fragments from the binary16 row tile, NTL live n8 tiles.
 template <class Cfg, int NTL>
-__device__ __forceinline__ void hmma_half_stage(uint32_t xh, uint32_t ws, int grp, int warp_m, int warp_n, int g,
-                                                int tq, int pg, float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
-  // B fragments: binary16 k = 64grp + 16tq .. +15 of row n (swizzled chunks 2tq, 2tq+1)
+__device__ __forceinline__ void hmma_half_stage(const uint8_t* xh, const uint8_t* ws, int half, int warp_m, int warp_n,
+                                                int g, int tq, int pg, float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
+  // Plain shared-memory reads (ordered after the stage's barrier wait by its memory
+  // clobber) let the compiler issue every load of the stage before the first MMA.
+  auto lds = [](const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); };
+  // B fragments: binary16 k = 64half + 16tq .. +15 of row n (swizzled chunks 2tq, 2tq+1)
   uint4 bfrag[NTL][2];
 #pragma unroll
   for (int nt = 0; nt < NTL; ++nt) {
     const int n = warp_n * Cfg::NT * 8 + nt * 8 + g;
-    const uint32_t rb = xh + n * 128;
-    bfrag[nt][0] = lds128(rb + (((2 * tq) ^ (n & 7)) << 4));
-    bfrag[nt][1] = lds128(rb + (((2 * tq + 1) ^ (n & 7)) << 4));
+    const uint8_t* rb = xh + n * 128;
+    bfrag[nt][0] = lds(rb + (((2 * tq) ^ (n & 7)) << 4));
+    bfrag[nt][1] = lds(rb + (((2 * tq + 1) ^ (n & 7)) << 4));
   }
 #pragma unroll
   for (int mt = 0; mt < Cfg::MT; ++mt) {
-    // A fragments: int8 k = 64grp + 16tq .. +15 of channels perm(g) and 8 + perm(g)
+    // A fragments: int8 k = 64half + 16tq .. +15 of channels perm(g) and 8 + perm(g)
     const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
-    const uint4 alo = lds128(ws + m * kBK + (((4 * grp + tq) ^ (m & 7)) << 4));
-    const uint4 ahi = lds128(ws + (m + 8) * kBK + (((4 * grp + tq) ^ (m & 7)) << 4));
+    const uint4 alo = lds(ws + m * kBK + (((4 * half + tq) ^ (m & 7)) << 4));
+    const uint4 ahi = lds(ws + (m + 8) * kBK + (((4 * half + tq) ^ (m & 7)) << 4));
     const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
     const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
 #pragma unroll
@@ -143,6 +141,23 @@ __device__ __forceinline__ void hmma_half_stage(uint32_t xh, uint32_t ws, int gr
       }
     }
   }
+}
+
+// Exact fp32 chunk sums -> int32 accumulators; the fp32 partials restart at 0.
+template <class Cfg>
+__device__ __forceinline__ void drain_chunk(float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4], int (&acci)[Cfg::MT][Cfg::NT][4]) {
+#pragma unroll
+  for (int mt = 0; mt < Cfg::MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < Cfg::NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int q = 0; q < Cfg::P; ++q) {
+          acci[mt][nt][i] += __float2int_rn(accf[q][mt][nt][i]);
+          accf[q][mt][nt][i] = 0.0f;
+        }
+      }
 }
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
@@ -239,7 +254,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     prefetch_tmap(&tm_x8);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kConsumerWarps);
+      mbar_init(&empty_bar[s], kGroupWarps);  // one group consumes each stage
     }
     mbar_init(&part_full_bar, kGroupWarps);
     mbar_init(&part_empty_bar, kGroupWarps);
@@ -296,8 +311,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     if (lane == 0) s_issued = issued;
   } else {
     // ================= MMA consumer warps =================
-    // Group grp (8 warps) computes k bytes [64*grp, 64*grp+64) of every stage; the
-    // two groups' exact int32 partial sums are added in the epilogue.
+    // Group grp (8 warps) computes the stages kb with kb % 2 == grp (both 64-deep
+    // halves); the two groups' exact int32 partial sums are added in the epilogue.
     const int grp = warp / kGroupWarps, wig = warp % kGroupWarps;
     const int warp_m = wig % Cfg::WARPS_M, warp_n = wig / Cfg::WARPS_M;
     const int g = lane >> 2, tq = lane & 3;
@@ -335,43 +350,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       // n8 tiles of this warp that hold real rows (the rest are skipped)
       const int live_nt = min(Cfg::NT, max(0, (it.rows - warp_n * Cfg::NT * 8 + 7) / 8));
 
+      int own = 0;  // stages of this item computed by this group
       for (int kb = 0; kb < nk; ++kb) {
-        ok = !*(volatile int*)&s_abort && mbar_wait_bounded(&full_bar[slot], phase);
-        if (!ok) {
-          s_abort = 1;
-          record_status(args.status, MOE_ERR_TIMEOUT);
-          break;
+        if ((kb & 1) == grp) {
+          ok = !*(volatile int*)&s_abort && mbar_wait_bounded(&full_bar[slot], phase);
+          if (!ok) {
+            s_abort = 1;
+            record_status(args.status, MOE_ERR_TIMEOUT);
+            break;
+          }
+          const uint8_t* xs = smem_gen + slot * Cfg::STAGE_BYTES;
+          const uint8_t* ws = xs + Cfg::X_BYTES;
+          // one uniform branch per stage on the number of live n8 tiles
+          if (live_nt >= 2) {
+            hmma_half_stage<Cfg, Cfg::NT>(xs, ws, 0, warp_m, warp_n, g, tq, pg, accf);
+            hmma_half_stage<Cfg, Cfg::NT>(xs + Cfg::X_HALF_BYTES, ws, 1, warp_m, warp_n, g, tq, pg, accf);
+          } else if (live_nt == 1) {
+            hmma_half_stage<Cfg, 1>(xs, ws, 0, warp_m, warp_n, g, tq, pg, accf);
+            hmma_half_stage<Cfg, 1>(xs + Cfg::X_HALF_BYTES, ws, 1, warp_m, warp_n, g, tq, pg, accf);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty_bar[slot]);
+          ++consumed;
+          // drain the exact fp32 chunk (4 own stages x 128 = 512 deep) into int32
+          if (++own % 4 == 0) drain_chunk<Cfg>(accf, acci);
         }
-        const uint32_t xh = smem_base + slot * Cfg::STAGE_BYTES + grp * Cfg::X_HALF_BYTES;
-        const uint32_t ws = smem_base + slot * Cfg::STAGE_BYTES + Cfg::X_BYTES;
-        // one uniform branch per stage on the number of live n8 tiles
-        if (live_nt >= 2)
-          hmma_half_stage<Cfg, Cfg::NT>(xh, ws, grp, warp_m, warp_n, g, tq, pg, accf);
-        else if (live_nt == 1)
-          hmma_half_stage<Cfg, 1>(xh, ws, grp, warp_m, warp_n, g, tq, pg, accf);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
-        ++consumed;
         if (++slot == S) {
           slot = 0;
           phase ^= 1u;
         }
-        // drain the exact fp32 chunk (at most 8 stages x 64 = 512 deep) into int32
-        if ((kb + 1) % 8 == 0 || kb + 1 == nk) {
-#pragma unroll
-          for (int mt = 0; mt < Cfg::MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < Cfg::NT; ++nt)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-#pragma unroll
-                for (int q = 0; q < Cfg::P; ++q) {
-                  acci[mt][nt][i] += __float2int_rn(accf[q][mt][nt][i]);
-                  accf[q][mt][nt][i] = 0.0f;
-                }
-              }
-        }
       }
+      if (own % 4 != 0) drain_chunk<Cfg>(accf, acci);
       // ---- epilogue.  Group 1 hands its int32 partials to group 0 through shared
       // memory (part_full / part_empty) and moves on to the next item; group 0 adds
       // them, scales, converts, stages [T][128] binary16 and stores it coalesced.
