@@ -37,8 +37,9 @@ namespace moe {
 
 namespace {
 
-constexpr int kGroupWarps = 8;                        // MMA warps per k-half group
-constexpr int kConsumerWarps = 2 * kGroupWarps;       // group h computes k-half h of every stage
+constexpr int kGroupWarps = 8;                        // MMA warps per group
+constexpr int kGroups = 2;                            // group g computes the stages in slots s % kGroups == g
+constexpr int kConsumerWarps = kGroups * kGroupWarps;
 constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;  // + 1 TMA producer warp
 constexpr int kBN = 128;         // channels per work item
 constexpr int kBK = 128;         // reduction depth per pipeline stage (128-byte weight rows)
@@ -64,9 +65,13 @@ struct GemmCfg {
   static constexpr int W_BYTES = kBN * kBK;        // [128][128] int8, 128-B swizzled rows
   static constexpr int STAGE_BYTES = X_BYTES + W_BYTES;
   static constexpr int EPI_BYTES = T * kBN * 2;
-  static constexpr int PART_BYTES = kGroupWarps * MT * NT * 4 * 32 * 4;  // k-half-1 partial sums
+  static constexpr int PART_BYTES = (kGroups - 1) * kGroupWarps * MT * NT * 4 * 32 * 4;  // groups 1.. partials
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + PART_BYTES + 1024;
   static_assert(WARPS_M * WARPS_N == kGroupWarps, "warp grid");
+  // stage n is computed by group n % kGroups: with STAGES a multiple of kGroups every
+  // ring slot always belongs to the same group, which then waits on every phase of its
+  // slots in order (a group never tests the parity of a phase it skipped)
+  static_assert(STAGES % kGroups == 0, "ring slots per group");
   static_assert(X_HALF_BYTES % 1024 == 0, "1024-B alignment of swizzled tiles");
   static_assert(SMEM_BYTES + 9 * 1024 <= 227 * 1024, "shared memory");
 };
@@ -216,7 +221,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   __shared__ int s_pref[kMaxExperts + 1];  // first work item of each expert
   __shared__ int s_end[kMaxExperts];       // cumsum
   __shared__ int s_wsum[kConsumerWarps];
-  __shared__ int s_abort, s_issued, s_consumed;
+  __shared__ int s_abort, s_issued;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E, n_cb = args.N / kBN;
@@ -256,11 +261,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kGroupWarps);  // one group consumes each stage
     }
-    mbar_init(&part_full_bar, kGroupWarps);
+    mbar_init(&part_full_bar, (kGroups - 1) * kGroupWarps);
     mbar_init(&part_empty_bar, kGroupWarps);
     s_abort = 0;
     s_issued = 0;
-    s_consumed = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -311,15 +315,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     if (lane == 0) s_issued = issued;
   } else {
     // ================= MMA consumer warps =================
-    // Group grp (8 warps) computes the stages kb with kb % 2 == grp (both 64-deep
-    // halves); the two groups' exact int32 partial sums are added in the epilogue.
+    // Group grp (8 warps) computes the stages held in ring slots s with
+    // s % kGroups == grp (both 64-deep halves); the groups' exact int32 partial sums
+    // are added in the epilogue.
     const int grp = warp / kGroupWarps, wig = warp % kGroupWarps;
     const int warp_m = wig % Cfg::WARPS_M, warp_n = wig / Cfg::WARPS_M;
     const int g = lane >> 2, tq = lane & 3;
     const int pg = mrow_perm(g);
     __half* stile = reinterpret_cast<__half*>(smem_gen + S * Cfg::STAGE_BYTES);
-    int* spart = reinterpret_cast<int*>(smem_gen + S * Cfg::STAGE_BYTES + Cfg::EPI_BYTES) +
-                 wig * (Cfg::MT * Cfg::NT * 4 * 32) + lane;
+    constexpr int kPartWarp = Cfg::MT * Cfg::NT * 4 * 32;  // ints per warp
+    int* spart_base = reinterpret_cast<int*>(smem_gen + S * Cfg::STAGE_BYTES + Cfg::EPI_BYTES) + wig * kPartWarp + lane;
+    int* spart = spart_base + (grp > 0 ? (grp - 1) : 0) * kGroupWarps * kPartWarp;
     int slot = 0;
     uint32_t phase = 0;
     int consumed = 0, n_items = 0;
@@ -352,7 +358,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
       int own = 0;  // stages of this item computed by this group
       for (int kb = 0; kb < nk; ++kb) {
-        if ((kb & 1) == grp) {
+        if (slot % kGroups == grp) {
           ok = !*(volatile int*)&s_abort && mbar_wait_bounded(&full_bar[slot], phase);
           if (!ok) {
             s_abort = 1;
@@ -384,7 +390,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       // ---- epilogue.  Group 1 hands its int32 partials to group 0 through shared
       // memory (part_full / part_empty) and moves on to the next item; group 0 adds
       // them, scales, converts, stages [T][128] binary16 and stores it coalesced.
-      if (grp == 1) {
+      if (grp > 0) {
         bool got = true;
         if (n_items > 0) got = wait_part(&part_empty_bar, (n_items - 1) & 1, args.status);
         got = __all_sync(0xffffffffu, got);
@@ -408,8 +414,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 #pragma unroll
           for (int nt = 0; nt < Cfg::NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              v[mt][nt][i] = acci[mt][nt][i] + (got ? spart[((mt * Cfg::NT + nt) * 4 + i) * 32] : 0);
+            for (int i = 0; i < 4; ++i) {
+              int sum = acci[mt][nt][i];
+#pragma unroll
+              for (int q = 1; q < kGroups; ++q)
+                sum += got ? spart_base[(q - 1) * kGroupWarps * kPartWarp + ((mt * Cfg::NT + nt) * 4 + i) * 32] : 0;
+              v[mt][nt][i] = sum;
+            }
         __syncwarp();
         if (lane == 0) mbar_arrive(&part_empty_bar);
         ok = ok && got;
@@ -441,13 +452,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       }
       ++n_items;
     }
-    if (threadIdx.x == 0) s_consumed = consumed;
+    (void)consumed;
   }
 
   __syncthreads();
   if (s_abort && threadIdx.x == kConsumerWarps * 32) {
-    // let loads still in flight land before the CTA's shared memory is released
-    for (int n = s_consumed; n < s_issued; ++n) mbar_wait_bounded(&full_bar[n % S], (uint32_t)((n / S) & 1));
+    // let loads still in flight land before the CTA's shared memory is released: the
+    // last S issued stages are the latest phase of each slot
+    const int issued = s_issued;
+    for (int n = max(0, issued - S); n < issued; ++n) mbar_wait_bounded(&full_bar[n % S], (uint32_t)((n / S) & 1));
   }
 }
 

@@ -134,6 +134,7 @@ GEMM_CASES = [
     synth.Workload("g_big", 384, 1024, 256, 4, 2, "zipf", 53),              # T=64 tile, hot expert
     synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # many 512-deep chunks
     synth.Workload("g_tiles", 700, 512, 192, 3, 2, "zipf", 55),             # 128-row tiles + tails, 64-deep tail
+    synth.Workload("g_odd", 48, 384, 192, 8, 2, "uniform", 56),             # warp-MMA engine, 3 stages per item
 ]
 
 
