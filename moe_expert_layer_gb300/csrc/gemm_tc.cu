@@ -364,13 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
   } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kNumConvWarps) {
     // ======================= converters =======================
     // Group g widens the stages n with n % 2 == g, a full 128-byte weight row per
-    // thread.  The tensor-memory store of a stage drains while the warp waits for
-    // and widens its next stage; only then is the stage handed to the MMA issuer.
+    // thread, stores it into the stage's tensor-memory A buffer and hands it to the
+    // MMA issuer.
     const int grp = (warp - kConvWarp0) >> 2;
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;         // weight channel row of this thread
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    int n = 0, pending_ab = -1;
+    int n = 0;
     bool ok = true;
     for (int j = blockIdx.x; j < total && ok; j += gridDim.x) {
       for (int kb = 0; kb < nk; ++kb, ++n) {
@@ -394,24 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
         // the weight stage is in registers: hand it back to the producer
         __syncwarp();
         if (lane == 0) mbar_arrive(&wempty_bar[slot]);
-        if (pending_ab >= 0) {
-          // the previous stage's store has drained by now: publish it
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&afull_bar[pending_ab]);
-        }
         const uint32_t ta = tmem + lane_off + kACol0 + ab * 64;
         tmem_st32(ta, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
         tmem_st32(ta + 32, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]));
-        pending_ab = ab;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull_bar[ab]);
       }
-    }
-    if (pending_ab >= 0 && ok) {
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&afull_bar[pending_ab]);
     }
   } else if (warp >= kDrainWarp0) {
     // ======================= drain + epilogue =======================
