@@ -240,6 +240,19 @@ int32_t moe_combine_unpermute(const moe_dims_t* d, const uint16_t* c2, const flo
                               const int32_t* expanded_row_idx, const float* probs, uint16_t* out,
                               void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Exercises the bounded device-side wait every pipeline kernel uses (failure
+ * detection): a one-warp kernel waits on a barrier phase that nothing completes,
+ * gives up after limit_us microseconds (1 .. 2,000,000) and writes MOE_ERR_TIMEOUT
+ * to *status (device memory, cleared first).  The kernel returns normally; the
+ * context stays usable.  Asynchronous on `stream`.
+ */
+int32_t moe_selftest_wait_timeout(int32_t* status, uint32_t limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ EXPORTS = [
     "moe_layer_host_workspace_size", "moe_layer_fwd_host", "moe_workspace_status",
     "moe_workspace_clear_status", "moe_route_sort_workspace_size", "moe_route_sort",
     "moe_quant_tokens", "moe_quant_dispatch", "moe_gmm_workspace_size", "moe_gmm1", "moe_swiglu_quant", "moe_gmm2",
-    "moe_combine_unpermute", "moe_route_sort_noalloc",
+    "moe_combine_unpermute", "moe_route_sort_noalloc", "moe_selftest_wait_timeout",
 ]
 
 
@@ -76,6 +76,7 @@ def load_library(path=None):
         "moe_gmm2": ([D] + [vp] * 6 + [sz, vp], i32),
         "moe_combine_unpermute": ([D] + [vp] * 6, i32),
         "moe_route_sort_noalloc": ([D] + [vp] * 6, i32),
+        "moe_selftest_wait_timeout": ([vp, ctypes.c_uint32, vp], i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -190,6 +191,12 @@ def moe_combine_unpermute(d, c2, pts2, expanded_row_idx, probs, out, stream=None
     _check("moe_combine_unpermute", load_library().moe_combine_unpermute(
         ctypes.byref(d), _p(c2), _p(pts2), _p(expanded_row_idx), _p(probs), _p(out),
         _stream(stream)))
+
+
+def moe_selftest_wait_timeout(status, limit_us, stream=None):
+    """Runs the bounded-wait self-test; status (int32 device tensor) receives the code."""
+    _check("moe_selftest_wait_timeout", load_library().moe_selftest_wait_timeout(
+        _p(status), limit_us, _stream(stream)))
 
 
 # Largest route count (M * topK) moe_route_sort_noalloc accepts (its fixed scratch).
