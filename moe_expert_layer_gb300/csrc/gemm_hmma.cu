@@ -42,13 +42,15 @@ constexpr int kGroups = 2;                            // group g computes the st
 constexpr int kConsumerWarps = kGroups * kGroupWarps;
 constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;  // + 1 TMA producer warp
 constexpr int kBN = 128;         // channels per work item
-constexpr int kBK = 128;         // reduction depth per pipeline stage (128-byte weight rows)
+constexpr int kBK = 256;         // reduction depth per pipeline stage
+constexpr int kSubK = 128;       // weight sub-tile depth (one 128-byte swizzled TMA box)
+constexpr int kQuarters = kBK / 64;  // 64-deep k quarters per stage
 constexpr int kMaxExperts = 1024;
 
 template <int T>
 struct TileShape;
 template <>
-struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 8; };
+struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 4; };
 
 template <int T>
 struct GemmCfg {
@@ -60,9 +62,10 @@ struct GemmCfg {
   // independent fp32 partial accumulators per output fragment (k-slices are dealt
   // round-robin), so that at least 8 MMA chains are in flight per warp
   static constexpr int P = (MT * NT >= 8) ? 1 : 8 / (MT * NT);
-  static constexpr int X_HALF_BYTES = T * 128;     // [T][64] binary16, 128-B swizzled rows
-  static constexpr int X_BYTES = 2 * X_HALF_BYTES;
-  static constexpr int W_BYTES = kBN * kBK;        // [128][128] int8, 128-B swizzled rows
+  static constexpr int X_HALF_BYTES = T * 128;     // one k quarter: [T][64] binary16, 128-B swizzled rows
+  static constexpr int X_BYTES = kQuarters * X_HALF_BYTES;
+  static constexpr int W_SUB_BYTES = kBN * kSubK;  // [128][128] int8, 128-B swizzled rows
+  static constexpr int W_BYTES = (kBK / kSubK) * W_SUB_BYTES;
   static constexpr int STAGE_BYTES = X_BYTES + W_BYTES;
   static constexpr int EPI_BYTES = T * kBN * 2;
   static constexpr int PART_BYTES = (kGroups - 1) * kGroupWarps * MT * NT * 4 * 32 * 4;  // groups 1.. partials
@@ -128,8 +131,8 @@ __device__ __forceinline__ void hmma_half_stage(const uint8_t* xh, const uint8_t
   for (int mt = 0; mt < Cfg::MT; ++mt) {
     // A fragments: int8 k = 64half + 16tq .. +15 of channels perm(g) and 8 + perm(g)
     const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
-    const uint4 alo = lds(ws + m * kBK + (((4 * half + tq) ^ (m & 7)) << 4));
-    const uint4 ahi = lds(ws + (m + 8) * kBK + (((4 * half + tq) ^ (m & 7)) << 4));
+    const uint4 alo = lds(ws + m * kSubK + (((4 * half + tq) ^ (m & 7)) << 4));
+    const uint4 ahi = lds(ws + (m + 8) * kSubK + (((4 * half + tq) ^ (m & 7)) << 4));
     const uint32_t aw_lo[4] = {alo.x, alo.y, alo.z, alo.w};
     const uint32_t aw_hi[4] = {ahi.x, ahi.y, ahi.z, ahi.w};
 #pragma unroll
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E, n_cb = args.N / kBN;
-  const int nk = (args.Kd + kBK - 1) / kBK;  // a 64-deep tail reads TMA zero fill
+  const int nk = (args.Kd + kBK - 1) / kBK;  // a ragged tail reads TMA zero fill
 
   // ---- work list: s_pref[e] = sum over e' < e of ceil(cnt_e' / T) * n_cb
   if (threadIdx.x < kConsumerWarps * 32) {
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       // tiles of at most 8 rows (most decode tiles) load an 8-row token box
       const bool small = (T > 8) && (it.rows <= 8);
       const void* tmx = small ? static_cast<const void*>(&tm_x8) : static_cast<const void*>(&tm_x);
-      const uint32_t tx = (uint32_t)Cfg::W_BYTES + (uint32_t)(small ? 8 : T) * 256u;
+      const uint32_t tx = (uint32_t)Cfg::W_BYTES + (uint32_t)(small ? 8 : T) * 128u * kQuarters;
       for (int kb = 0; kb < nk; ++kb) {
         bool ok = true;
         if (lane == 0) {
@@ -301,8 +304,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         if (lane == 0) {
           mbar_arrive_expect_tx(&full_bar[slot], tx);
           tma_load_2d(ws, &tm_w, kx, w_row, &full_bar[slot]);
-          tma_load_2d(xs, tmx, kx, it.row0, &full_bar[slot]);
-          tma_load_2d(xs + Cfg::X_HALF_BYTES, tmx, kx + 64, it.row0, &full_bar[slot]);
+          tma_load_2d(ws + Cfg::W_SUB_BYTES, &tm_w, kx + kSubK, w_row, &full_bar[slot]);
+#pragma unroll
+          for (int q = 0; q < kQuarters; ++q)
+            tma_load_2d(xs + q * Cfg::X_HALF_BYTES, tmx, kx + 64 * q, it.row0, &full_bar[slot]);
         }
         ++issued;
         if (++slot == S) {
@@ -369,24 +374,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           const uint8_t* ws = xs + Cfg::X_BYTES;
           // one uniform branch per stage on the number of live n8 tiles
           if (live_nt >= 2) {
-            hmma_half_stage<Cfg, Cfg::NT>(xs, ws, 0, warp_m, warp_n, g, tq, pg, accf);
-            hmma_half_stage<Cfg, Cfg::NT>(xs + Cfg::X_HALF_BYTES, ws, 1, warp_m, warp_n, g, tq, pg, accf);
+#pragma unroll
+            for (int q = 0; q < kQuarters; ++q)
+              hmma_half_stage<Cfg, Cfg::NT>(xs + q * Cfg::X_HALF_BYTES, ws + (q >> 1) * Cfg::W_SUB_BYTES, q & 1,
+                                            warp_m, warp_n, g, tq, pg, accf);
           } else if (live_nt == 1) {
-            hmma_half_stage<Cfg, 1>(xs, ws, 0, warp_m, warp_n, g, tq, pg, accf);
-            hmma_half_stage<Cfg, 1>(xs + Cfg::X_HALF_BYTES, ws, 1, warp_m, warp_n, g, tq, pg, accf);
+#pragma unroll
+            for (int q = 0; q < kQuarters; ++q)
+              hmma_half_stage<Cfg, 1>(xs + q * Cfg::X_HALF_BYTES, ws + (q >> 1) * Cfg::W_SUB_BYTES, q & 1, warp_m,
+                                      warp_n, g, tq, pg, accf);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty_bar[slot]);
           ++consumed;
-          // drain the exact fp32 chunk (4 own stages x 128 = 512 deep) into int32
-          if (++own % 4 == 0) drain_chunk<Cfg>(accf, acci);
+          // drain the exact fp32 chunk (2 own stages x 256 = 512 deep) into int32
+          if (++own % 2 == 0) drain_chunk<Cfg>(accf, acci);
         }
         if (++slot == S) {
           slot = 0;
           phase ^= 1u;
         }
       }
-      if (own % 4 != 0) drain_chunk<Cfg>(accf, acci);
+      if (own % 2 != 0) drain_chunk<Cfg>(accf, acci);
       // ---- epilogue.  Group 1 hands its int32 partials to group 0 through shared
       // memory (part_full / part_empty) and moves on to the next item; group 0 adds
       // them, scales, converts, stages [T][128] binary16 and stores it coalesced.
@@ -471,7 +480,7 @@ template <int T>
 cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   using Cfg = GemmCfg<T>;
   CUtensorMap tw, tx;
-  if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kBK,
+  if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kSubK,
                             kBN))
     return cudaErrorInvalidValue;
   CUtensorMap tx8;
