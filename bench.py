@@ -187,7 +187,7 @@ def cpu_baseline(w, inp):
 # ----------------------------------------------------------------------------- ncu traffic record
 def engine_source(w):
     """Source file of the GEMM engine the library picks for this workload."""
-    name = "gemm_hmma.cu" if w.R / w.E <= 12.0 else "gemm_tc.cu"
+    name = "gemm_hmma.cu" if w.R / w.E <= 24.0 else "gemm_tc.cu"
     return os.path.join(ROOT, "moe_expert_layer_gb300", "csrc", name)
 
 

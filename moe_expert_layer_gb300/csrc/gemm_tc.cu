@@ -499,15 +499,17 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
 }
 
 // Engine choice.  A tcgen05.mma of M=128, K=16 costs about the same for any N up to
-// 128 (measured ~83 cycles on GB300), i.e. it consumes 2 KB of weights per issue
+// 128 (measured ~88 cycles on GB300), i.e. it consumes 2 KB of weights per issue
 // slot: with few rows per expert that caps weight streaming at about the HBM rate.
 // Warp-level HMMA (m16n8k16) consumes weights several times faster at N=8, so
-// batches with at most ~12 rows per expert on average (decode) run on it with
-// 16-row tiles, larger ones on tcgen05 with 128-row tiles.  The tile follows the mean rows per expert (the host never
-// reads device counts).
+// batches with at most 24 rows per expert on average run on it with 16-row tiles,
+// larger ones on tcgen05 with 128-row tiles.  Measured at K=7168, I=2048, E=256:
+// 16 rows per expert, GMM1 1.64 ms on the warp-MMA engine against 2.92 ms on
+// tcgen05; 64 rows per expert, 4.97 ms against 3.73 ms.  The tile follows the mean
+// rows per expert (the host never reads device counts).
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream) {
   const double mean_rows = (double)p.R / (double)p.E;
-  if (mean_rows <= 12.0) return launch_grouped_gemm_hmma(p, 16, stream);
+  if (mean_rows <= 24.0) return launch_grouped_gemm_hmma(p, 16, stream);
   return launch_grouped_gemm_tc(p, stream);
 }
 

@@ -130,7 +130,8 @@ def _stage_inputs(w):
 
 GEMM_CASES = [
     synth.Workload("g_small", 40, 256, 128, 8, 2, "uniform", 51),           # T=16 tile
-    synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # T=32 tile, ragged rows
+    synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # warp-MMA engine, ragged rows
+    synth.Workload("g_mid_tc", 320, 512, 192, 16, 2, "biased", 57),         # tcgen05 engine, ragged rows
     synth.Workload("g_big", 384, 1024, 256, 4, 2, "zipf", 53),              # T=64 tile, hot expert
     synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # many 512-deep chunks
     synth.Workload("g_tiles", 700, 512, 192, 3, 2, "zipf", 55),             # 128-row tiles + tails, 64-deep tail
