@@ -1,5 +1,6 @@
 // Grouped W8A8 GEMM of the expert layer on the 5th-generation tensor cores
-// (tcgen05).  PTO-ISA MegaMoE operator page, sections "3. GMM1" and "5. GMM2".
+// (tcgen05), run by CTA pairs.  PTO-ISA MegaMoE operator page, sections "3. GMM1"
+// and "5. GMM2".
 //
 // For expert e with rows [cumsum[e]-cnt_e, cumsum[e]) of the expert-major row
 // space and every output channel n < N:
@@ -8,36 +9,57 @@
 //
 // Exact integers on the fp16 tensor path.  GB300 executes int8 tensor MMAs
 // and dp4a far below its binary16 rate, so the int8 operands are multiplied as
-// binary16 (every int8 value, and every product |p| <= 127^2, is exact) with
+// binary16 (every int8 value, and every product |p| <= 128^2, is exact) with
 // fp32 accumulation in tensor memory.  An fp32 sum of integers is exact while
-// every partial sum stays below 2^24, so the reduction runs in chunks of 512
-// (512 * 127^2 < 2^23); after each chunk the epilogue warps read the fp32
-// accumulator, convert it to int32 and add it to a per-thread int32 sum.  The
-// result is the exact integer dot product for any K.
+// every partial sum stays within 2^24 in magnitude, so the reduction runs in
+// chunks of 1024 (1024 * 128 * 128 = 2^24); after each chunk the drain warps read
+// the fp32 accumulator, convert it to int32 and add it to per-thread int32 sums.
+// The result is the exact integer dot product for any K.
 //
-// Operands.  The MMA is "swapped": weights are operand A (M = 128 output
-// channels per work item) and token rows are operand B (N = T rows).
-//   - Weights stay int8 in HBM (they are the dominant traffic).  A TMA box of
-//     128 channels x 128 k lands in shared memory (128-byte swizzle); converter
-//     warps read one channel row per thread, widen 4 int8 to 4 binary16 with a
-//     byte permute into the 1024+v encoding and one subtract, and store the row
-//     into a tensor-memory A buffer (tcgen05.st, 32x32b).
+// CTA pairs.  One tcgen05.mma of M = 256 costs ~92 cycles for any N <= 128 and
+// 128 cycles at N = 256 (measured on GB300); at N = 256 changing the operand
+// addresses between MMAs is free and a tcgen05.commit costs ~60 cycles of tensor
+// time.  So two CTAs of a cluster issue MMAs of M = 256, N = 256 (cta_group::2),
+// one commit per 128-deep stage: each CTA contributes 128 weight channels
+// (operand A, in its own tensor memory) and half of the N token rows (operand B,
+// in its own shared memory), and receives the 128 x N block of its channels in its
+// tensor memory.  A work item is (expert, 256-channel block, 256-row tile); N is
+// 64, 128 or 256 by the rows the tile holds.
+//   - Weights stay int8 in HBM (they are the dominant traffic at small batches).
+//     A TMA box of 128 channels x 128 k lands in shared memory (128-byte swizzle);
+//     converter warps read one channel row per thread, widen 4 int8 to 4 binary16
+//     with a byte permute into the 1024+v encoding and one subtract, and store the
+//     row into the stage's tensor-memory A buffer (tcgen05.st, 32x32b).
 //   - Activations are binary16-coded int8 in expert-major rows (written so by the
-//     quant-scatter and SwiGLU kernels), loaded by TMA as two [T][64] tiles per
+//     quant-scatter and SwiGLU kernels), loaded by TMA as two [128][64] tiles per
 //     stage in the canonical K-major 128-byte-swizzled layout the MMA reads
 //     through a shared-memory descriptor.
+//   - Tensor memory: the accumulator (256 columns) and four A buffers (64 columns
+//     each).  The token ring and the A buffers have the same four slots, so one
+//     commit per stage frees both.
+//   - The MMA issuer cannot run far ahead of the tensor pipe (a stage completes
+//     ~500 cycles after its last MMA is issued), so its per-stage work is kept to
+//     one barrier wait: the stage's readiness (both CTAs' token halves and A
+//     buffers) is gathered on one barrier in CTA 0.
 //
-// Roles (one persistent CTA per SM, work items strided over the CTAs):
+// Roles (one persistent pair per two SMs, work items strided over the pairs):
 //   warp 0      TMA producer of the weight ring (freed by the converters as soon
 //               as they hold the stage in registers)
-//   warp 2      TMA producer of the row-tile ring (freed when the stage's MMAs finish)
-//   warp 1      tensor-memory allocation; one elected thread issues tcgen05.mma
-//   warps 4-11  converters: group 0 widens the even stages, group 1 the odd
-//               ones (warp w owns TMEM lanes 32*(w%4) .. +31)
-//   warps 12-15 drain + epilogue: one thread per output channel
-// Every wait on an mbarrier is bounded; a wait that gives up sets the status
-// word to MOE_ERR_TIMEOUT and the CTA winds down (in-flight copies and MMAs
-// are waited for, tensor memory is freed) before returning.
+//   warp 1      tensor-memory allocation (both CTAs); in CTA 0 of the pair one
+//               thread issues the pair's tcgen05.mma and commits
+//   warp 2      TMA producer of the token ring
+//   warp 3      relay: tells CTA 0's stage barrier when this CTA's token stage has landed
+//   warps 4-7   converters (warp w owns TMEM lanes 32*(w%4) .. +31)
+//   warps 8-23  drain + epilogue: warp w reads TMEM lanes 32*(w%4).. and the 64
+//               accumulator columns 64*((w-8)/4) ..; each thread keeps 64 int32
+//               sums, so the warpgroups rebalance registers (setmaxnreg) from the
+//               single-lane roles and the converters to the drains.
+// CTA 1 signals readiness of its A buffers, token stages and drained accumulator
+// to barriers in CTA 0 (remote mbarrier arrives); the MMA commits arrive on the
+// barriers of both CTAs (multicast).  Every wait on an mbarrier is bounded; a wait
+// that gives up sets the status word to MOE_ERR_TIMEOUT and the CTA winds down
+// (in-flight copies and MMAs are waited for, the pair synchronises, tensor memory
+// is freed) before returning.
 #include "common.cuh"
 #include "kernels.h"
 #include "tensor_map.h"
@@ -46,33 +68,35 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 640;
-constexpr int kBN = 128;          // output channels per work item (MMA M)
-constexpr int kBK = 128;          // reduction depth per stage
-constexpr int kChunkStages = 4;   // 512-deep exact chunks
-constexpr int kNumABuf = 4;       // tensor-memory A buffers (64 columns each)
-constexpr int kTmemCols = 512;
-constexpr int kAccCol0 = 0;       // accumulator buffers: columns [0,128) and [128,256)
-constexpr int kAccStride = 128;
-constexpr int kACol0 = 256;       // A buffers: columns 256 + 64*b
+constexpr int kThreads = 768;
+constexpr int kLaunchRegs = 80;     // registers per thread at launch (65536 / 768, rounded to 8)
+constexpr int kRegsSingle = 40;     // warpgroup 0: producers, MMA issuer, relay
+constexpr int kRegsConv = 56;       // warpgroup 1: converters
+constexpr int kRegsDrain = 96;      // warpgroups 2-5: drains
+static_assert(128 * kRegsSingle + 128 * kRegsConv + 512 * kRegsDrain <= kThreads * kLaunchRegs,
+              "register split exceeds the registers the CTA is launched with");
+constexpr int kBM = 128;            // weight channels per CTA
+constexpr int kPairCh = 256;        // weight channels per pair (MMA M)
+constexpr int kBK = 128;            // reduction depth per stage
+constexpr int kTileRows = 256;      // token rows per work item (MMA N <= 256)
+constexpr int kHalfRows = kTileRows / 2;  // token rows per CTA (TMA box height)
+constexpr int kChunkStages = 8;     // 1024-deep exact chunks
+constexpr int kTmemCols = 512;      // accumulator [0, 256), A buffers 256 + 64*slot
+constexpr int kACol0 = 256;
 constexpr int kMaxExperts = 1024;
-constexpr int kWProducerWarp = 0, kMmaWarp = 1, kXProducerWarp = 2, kConvWarp0 = 4, kNumConvWarps = 8,
-              kDrainWarp0 = 12, kNumDrainWarps = 8;
-
-template <int T>
-struct Cfg {
-  static constexpr int W_STAGES = 4;   // weight ring, freed after conversion
-  static constexpr int X_STAGES = 4;   // token ring, freed by the MMA
-  static constexpr int X_HALF_BYTES = T * 128;  // [T][64] binary16, 128-B swizzled rows
-  static constexpr int X_BYTES = 2 * X_HALF_BYTES;
-  static constexpr int W_BYTES = kBN * kBK;      // [128][128] int8, 128-B swizzled rows
-  static constexpr int SMEM_BYTES = W_STAGES * W_BYTES + X_STAGES * X_BYTES + 1024;
-  // kind::f16 instruction descriptor: D f32, A/B f16, both K-major, N = T, M = 128
-  static constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(T >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-  static_assert(T == 128, "row tile: N = 128 (the MMA costs the same for any N <= 128)");
-  static_assert(X_HALF_BYTES % 1024 == 0, "1024-B alignment of swizzled tiles");
-  static_assert(SMEM_BYTES + 10 * 1024 <= 227 * 1024, "shared memory");
-};
+constexpr int kStages = 4;          // token ring = A buffers, freed by one commit per stage
+constexpr int kWStages = 4;         // weight ring, freed after conversion
+constexpr int kWBytes = kBM * kBK;  // [128][128] int8, 128-B swizzled rows
+constexpr int kXHalfBytes = kHalfRows * 128;  // [128 rows][64] binary16, 128-B swizzled rows
+constexpr int kXBytes = 2 * kXHalfBytes;
+static_assert(kXHalfBytes % 1024 == 0, "1024-B alignment of swizzled tiles");
+constexpr int kSmemBytes = kWStages * kWBytes + kStages * kXBytes + 1024;
+constexpr int kWProducerWarp = 0, kMmaWarp = 1, kXProducerWarp = 2, kRelayWarp = 3, kConvWarp0 = 4,
+              kNumConvWarps = 4, kDrainWarp0 = 8, kNumDrainWarps = 16;
+static_assert(kThreads == 32 * (kDrainWarp0 + kNumDrainWarps), "warp roles");
+static_assert(kSmemBytes + 10 * 1024 <= 227 * 1024, "shared memory");
+// kind::f16 instruction descriptor: D f32, A/B f16, both K-major, M = 256; N is set per item
+constexpr uint32_t kIdescBase = (1u << 4) | ((uint32_t)(256 >> 4) << 24);
 
 struct Args {
   const int32_t* cumsum;
@@ -82,7 +106,36 @@ struct Args {
   int E, N, Kd;
 };
 
-// ------------------------------------------------------------------ tcgen05 helpers
+// ------------------------------------------------------------------ cluster / tcgen05 helpers
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrive on a barrier given by its shared::cluster address (either CTA of the pair).
+// Default semantics: an arrive with cluster-scope release costs ~320 cycles on
+// GB300, this one ~6; the data it publishes is tensor memory (ordered by
+// tcgen05.wait + tcgen05.fence) or TMA-written shared memory whose barrier the
+// signalling thread has already seen complete.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs)); }
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs)); }
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -98,18 +151,27 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ void mma_f16_tmemA(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
+// D[256 x N] (+)= A[256 x 16] * B[N x 16]^T over the pair: A rows 0-127 from this
+// CTA's tensor memory, 128-255 from the peer's; B rows split N/2 + N/2 likewise.
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.u32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+// Arrive on `bar` in both CTAs of the pair once the MMAs issued so far complete.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
 
@@ -154,13 +216,12 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
 }
 
 struct Item {
-  int e, cb, row0, rows;
+  int e, cb, row0, rows, n_mma;
 };
 
-// Work item j -> (expert, channel block, first row, rows).  Items run expert-major,
-// then channel block, then row tile: CTAs working at the same time share weight
-// blocks (and token rows) through L2.
-template <int T>
+// Work item j -> (expert, channel block, first row, rows, MMA N).  Items run
+// expert-major, then channel block, then row tile: pairs working at the same time
+// share weight blocks through L2.
 __device__ __forceinline__ Item decode_item(int j, const int* s_pref, const int* s_end, int E) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
@@ -169,19 +230,21 @@ __device__ __forceinline__ Item decode_item(int j, const int* s_pref, const int*
   }
   const int start = lo ? s_end[lo - 1] : 0;
   const int cnt = s_end[lo] - start;
-  const int n_rt = (cnt + T - 1) / T;
+  const int n_rt = (cnt + kTileRows - 1) / kTileRows;
   const int local = j - s_pref[lo];
   const int cb = local / n_rt, rt = local - cb * n_rt;
   Item it;
   it.e = lo;
   it.cb = cb;
-  it.row0 = start + rt * T;
-  it.rows = min(T, cnt - rt * T);
+  it.row0 = start + rt * kTileRows;
+  it.rows = min(kTileRows, cnt - rt * kTileRows);
+  it.n_mma = it.rows <= 64 ? 64 : (it.rows <= 128 ? 128 : 256);
   return it;
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;  // fast path: one probe of a completed phase
   if (*abort_flag) return false;
   if (mbar_wait_bounded(bar, parity)) return true;
   *abort_flag = 1;
@@ -189,24 +252,23 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-template <int T>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
-                                                                      const __grid_constant__ CUtensorMap tm_x,
-                                                                      const Args args) {
-  using C = Cfg<T>;
-  constexpr int SW = C::W_STAGES, SX = C::X_STAGES;
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                             const Args args) {
+  constexpr int S = kStages, SW = kWStages;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t wfull_bar[SW], wempty_bar[SW], xfull_bar[SX], xempty_bar[SX];
-  __shared__ __align__(8) uint64_t afull_bar[kNumABuf], aempty_bar[kNumABuf];
-  __shared__ __align__(8) uint64_t accfull_bar[2], accempty_bar[2], final_bar;
+  __shared__ __align__(8) uint64_t wfull_bar[SW], wempty_bar[SW], xfull_bar[S], ready_bar[S], sdone_bar[S];
+  __shared__ __align__(8) uint64_t accfull_bar, accempty_bar, final_bar;
   __shared__ int s_pref[kMaxExperts + 1];
   __shared__ int s_end[kMaxExperts];
-  __shared__ int s_wsum[16];
+  __shared__ int s_wsum[kThreads / 32];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_w_issued, s_x_issued;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int E = args.E, n_cb = args.N / kBN;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int E = args.E, n_cb = (args.N + kPairCh - 1) / kPairCh;
   const int nk = (args.Kd + kBK - 1) / kBK;  // a 64-deep tail reads TMA zero fill
   volatile int* abort_flag = &s_abort;
 
@@ -218,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
     for (int e = e0; e < e1; ++e) {
       const int hi = __ldg(args.cumsum + e), lo = e ? __ldg(args.cumsum + e - 1) : 0;
       s_end[e] = hi;
-      local += (hi - lo + T - 1) / T * n_cb;
+      local += (hi - lo + kTileRows - 1) / kTileRows * n_cb;
     }
     int incl = local;
 #pragma unroll
@@ -233,30 +295,26 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
       s_x_issued = 0;
     }
     if (warp == kMmaWarp) {
-      // all 512 tensor-memory columns (one CTA per SM)
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+      // all 512 tensor-memory columns of both SMs (one pair per two SMs)
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                    "n"(kTmemCols)
                    : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
       if (lane == 0) {
         prefetch_tmap(&tm_w);
         prefetch_tmap(&tm_x);
         for (int s = 0; s < SW; ++s) {
           mbar_init(&wfull_bar[s], 1);
-          mbar_init(&wempty_bar[s], kNumConvWarps / 2);
+          mbar_init(&wempty_bar[s], kNumConvWarps);
         }
-        for (int s = 0; s < SX; ++s) {
+        for (int s = 0; s < S; ++s) {
           mbar_init(&xfull_bar[s], 1);
-          mbar_init(&xempty_bar[s], 1);
+          mbar_init(&sdone_bar[s], 1);
+          // CTA 0: both relays + both CTAs' converter warps
+          mbar_init(&ready_bar[s], 2 + 2 * kNumConvWarps);
         }
-        for (int b = 0; b < kNumABuf; ++b) {
-          mbar_init(&afull_bar[b], kNumConvWarps / 2);
-          mbar_init(&aempty_bar[b], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-          mbar_init(&accfull_bar[b], 1);
-          mbar_init(&accempty_bar[b], kNumDrainWarps);
-        }
+        mbar_init(&accfull_bar, 1);
+        mbar_init(&accempty_bar, 2 * kNumDrainWarps);
         mbar_init(&final_bar, 1);
         fence_barrier_init();
       }
@@ -268,217 +326,250 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_tc_kernel(const __gr
     for (int e = e0; e < e1; ++e) {
       s_pref[e] = run;
       const int lo = e ? s_end[e - 1] : 0;
-      run += (s_end[e] - lo + T - 1) / T * n_cb;
+      run += (s_end[e] - lo + kTileRows - 1) / kTileRows * n_cb;
     }
     if (e0 < E && e1 == E) s_pref[E] = run;
   }
   __syncthreads();
+  cluster_sync_all();  // the peer's barriers and tensor memory are ready
   tc_fence_after();
   const int total = s_pref[E];
   const uint32_t tmem = s_tmem;
 
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
-  const uint32_t w_ring = smem_base;                     // SW x [128][128] int8
-  const uint32_t x_ring = smem_base + SW * C::W_BYTES;   // SX x 2 x [T][64] binary16
+  const uint32_t w_ring = smem_base;                  // SW x [128][128] int8
+  const uint32_t x_ring = smem_base + SW * kWBytes;   // S x 2 x [128][64] binary16
 
-  if (warp == kWProducerWarp) {
-    // ======================= weight producer (one lane) =======================
-    if (lane == 0) {
-      int n = 0;
-      for (int j = blockIdx.x; j < total; j += gridDim.x) {
-        const Item it = decode_item<T>(j, s_pref, s_end, E);
-        const int w_row = it.e * args.N + it.cb * kBN;
-        for (int kb = 0; kb < nk; ++kb, ++n) {
-          const int slot = n % SW;
-          if (!wait_or_abort(&wempty_bar[slot], ((n / SW) & 1) ^ 1, abort_flag, args.status)) goto w_done;
-          mbar_arrive_expect_tx(&wfull_bar[slot], (uint32_t)C::W_BYTES);
-          tma_load_2d(smem_gen + slot * C::W_BYTES, &tm_w, kb * kBK, w_row, &wfull_bar[slot]);
+  if (warp < kConvWarp0) {
+    regs_dec<kRegsSingle>();
+    if (warp == kWProducerWarp) {
+      // ======================= weight producer (one lane) =======================
+      if (lane == 0) {
+        int n = 0;
+        for (int j = pair; j < total; j += npairs) {
+          const Item it = decode_item(j, s_pref, s_end, E);
+          const int w_row = it.e * args.N + it.cb * kPairCh + (int)rank * kBM;
+          for (int kb = 0; kb < nk; ++kb, ++n) {
+            const int slot = n % SW;
+            if (!wait_or_abort(&wempty_bar[slot], ((n / SW) & 1) ^ 1, abort_flag, args.status)) goto w_done;
+            mbar_arrive_expect_tx(&wfull_bar[slot], (uint32_t)kWBytes);
+            tma_load_2d(smem_gen + slot * kWBytes, &tm_w, kb * kBK, w_row, &wfull_bar[slot]);
+          }
         }
+      w_done:
+        s_w_issued = n;
       }
-    w_done:
-      s_w_issued = n;
-    }
-  } else if (warp == kXProducerWarp) {
-    // ======================= token producer =======================
-    int n = 0;
-    for (int j = blockIdx.x; j < total; j += gridDim.x) {
-      const Item it = decode_item<T>(j, s_pref, s_end, E);
-      const uint32_t tx = (uint32_t)T * 256u;
-      for (int kb = 0; kb < nk; ++kb, ++n) {
-        const int slot = n % SX;
+    } else if (warp == kXProducerWarp) {
+      // ======================= token producer (one lane) =======================
+      if (lane == 0) {
+        int n = 0;
+        for (int j = pair; j < total; j += npairs) {
+          const Item it = decode_item(j, s_pref, s_end, E);
+          const int y = it.row0 + (int)rank * (it.n_mma >> 1);
+          for (int kb = 0; kb < nk; ++kb, ++n) {
+            const int slot = n % S;
+            if (!wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status)) goto x_done;
+            uint8_t* xs_g = smem_gen + SW * kWBytes + slot * kXBytes;
+            mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)kXBytes);
+            tma_load_2d(xs_g, &tm_x, kb * kBK, y, &xfull_bar[slot]);
+            tma_load_2d(xs_g + kXHalfBytes, &tm_x, kb * kBK + 64, y, &xfull_bar[slot]);
+          }
+        }
+      x_done:
+        s_x_issued = n;
+      }
+    } else if (warp == kRelayWarp) {
+      // ======================= relay: token stage landed -> CTA 0's stage barrier =======================
+      if (lane == 0) {
+        const uint32_t ready_remote0 = cluster_addr(&ready_bar[0], 0);
+        int n = 0;
         bool ok = true;
-        if (lane == 0) ok = wait_or_abort(&xempty_bar[slot], ((n / SX) & 1) ^ 1, abort_flag, args.status);
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) goto x_done;
-        const uint32_t xs = x_ring + slot * C::X_BYTES;
-        uint8_t* xs_g = smem_gen + (xs - smem_base);
-        const int kx = kb * kBK;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&xfull_bar[slot], tx);
-          tma_load_2d(xs_g, &tm_x, kx, it.row0, &xfull_bar[slot]);
-          tma_load_2d(xs_g + C::X_HALF_BYTES, &tm_x, kx + 64, it.row0, &xfull_bar[slot]);
-        }
-        __syncwarp();
-      }
-    }
-  x_done:
-    if (lane == 0) s_x_issued = n;
-  } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer (one thread) =======================
-    if (lane == 0) {
-      int n = 0, c = 0;
-      bool ok = true;
-      for (int j = blockIdx.x; j < total && ok; j += gridDim.x) {
-        for (int kb = 0; kb < nk && ok; ++kb, ++n) {
-          const int slot = n % SX, ab = n % kNumABuf, acc = c & 1;
-          if (kb % kChunkStages == 0) {
-            // a new exact chunk: the drain must have read this accumulator buffer
-            ok = wait_or_abort(&accempty_bar[acc], ((c >> 1) & 1) ^ 1, abort_flag, args.status);
+        for (int j = pair; j < total && ok; j += npairs) {
+          for (int kb = 0; kb < nk; ++kb, ++n) {
+            const int slot = n % S;
+            ok = wait_or_abort(&xfull_bar[slot], (n / S) & 1, abort_flag, args.status);
             if (!ok) break;
-          }
-          ok = wait_or_abort(&xfull_bar[slot], (n / SX) & 1, abort_flag, args.status) &&
-               wait_or_abort(&afull_bar[ab], (n / kNumABuf) & 1, abort_flag, args.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t xs = x_ring + slot * C::X_BYTES;
-          const uint32_t d_tmem = tmem + kAccCol0 + acc * kAccStride;
-          const uint32_t a_tmem = tmem + kACol0 + ab * 64;
-#pragma unroll
-          for (int s = 0; s < 8; ++s) {
-            const uint64_t bdesc = sw128_desc(xs + (s >> 2) * C::X_HALF_BYTES + (s & 3) * 32);
-            mma_f16_tmemA(d_tmem, a_tmem + s * 8, bdesc, C::IDESC, (kb % kChunkStages != 0 || s != 0) ? 1u : 0u);
-          }
-          mma_commit(&xempty_bar[slot]);  // token stage free once these MMAs complete
-          mma_commit(&aempty_bar[ab]);    // tensor-memory A buffer free
-          if (kb % kChunkStages == kChunkStages - 1 || kb == nk - 1) {
-            mma_commit(&accfull_bar[acc]);  // chunk accumulated: hand it to the drain
-            ++c;
+            mbar_arrive_remote(ready_remote0 + slot * (uint32_t)sizeof(uint64_t));
           }
         }
       }
-      // every MMA issued by this thread has completed once final_bar fires
-      mma_commit(&final_bar);
-      mbar_wait_bounded(&final_bar, 0);
+    } else {
+      // ======================= MMA issuer (CTA 0, one thread) =======================
+      if (rank == 0 && lane == 0) {
+        int n = 0, c = 0;
+        bool ok = true;
+        for (int j = pair; j < total && ok; j += npairs) {
+          const Item it = decode_item(j, s_pref, s_end, E);
+          const uint32_t idesc = kIdescBase | ((uint32_t)(it.n_mma >> 3) << 17);
+          for (int kb = 0; kb < nk && ok; ++kb, ++n) {
+            const int slot = n % S;
+            const uint32_t ph = (n / S) & 1;
+            if (kb % kChunkStages == 0) {
+              // a new exact chunk: both CTAs' drains must have read the accumulator
+              ok = wait_or_abort(&accempty_bar, (c & 1) ^ 1, abort_flag, args.status);
+              if (!ok) break;
+            }
+            ok = wait_or_abort(&ready_bar[slot], ph, abort_flag, args.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t xs = x_ring + slot * kXBytes;
+            const uint32_t a_tmem = tmem + kACol0 + slot * 64;
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+              // 16-k step s: A columns 8s.., token tile s/4
+              const uint64_t bdesc = sw128_desc(xs + (s >> 2) * kXHalfBytes + (s & 3) * 32);
+              mma_pair(tmem, a_tmem + s * 8, bdesc, idesc, (kb % kChunkStages != 0 || s != 0) ? 1u : 0u);
+            }
+            mma_commit_pair(&sdone_bar[slot]);  // token slot and A buffer free once these MMAs complete
+            if (kb % kChunkStages == kChunkStages - 1 || kb == nk - 1) {
+              mma_commit_pair(&accfull_bar);    // chunk accumulated: hand it to the drains
+              ++c;
+            }
+          }
+        }
+        // every MMA issued by this thread has completed once final_bar fires
+        mma_commit_local(&final_bar);
+        mbar_wait_bounded(&final_bar, 0);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp >= kConvWarp0 && warp < kConvWarp0 + kNumConvWarps) {
+  } else if (warp < kDrainWarp0) {
     // ======================= converters =======================
-    // Group g widens the stages n with n % 2 == g, a full 128-byte weight row per
-    // thread, stores it into the stage's tensor-memory A buffer and hands it to the
-    // MMA issuer.
-    const int grp = (warp - kConvWarp0) >> 2;
+    // A full 128-byte weight row per thread, widened and stored into the stage's
+    // tensor-memory A buffer in two 64-k halves, then handed to the MMA issuer.
+    regs_dec<kRegsConv>();
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;         // weight channel row of this thread
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t ready_remote0 = cluster_addr(&ready_bar[0], 0);
     int n = 0;
     bool ok = true;
-    for (int j = blockIdx.x; j < total && ok; j += gridDim.x) {
+    for (int j = pair; j < total && ok; j += npairs) {
       for (int kb = 0; kb < nk; ++kb, ++n) {
-        if ((n & 1) != grp) continue;
-        const int slot = n % SW, ab = n % kNumABuf;
-        ok = wait_or_abort(&wfull_bar[slot], (n / SW) & 1, abort_flag, args.status) &&
-             wait_or_abort(&aempty_bar[ab], ((n / kNumABuf) & 1) ^ 1, abort_flag, args.status);
+        const int slot = n % S, wslot = n % SW;
+        ok = wait_or_abort(&wfull_bar[wslot], (n / SW) & 1, abort_flag, args.status) &&
+             wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t wrow = w_ring + slot * C::W_BYTES + r * kBK;
-        uint32_t v[64];
+        const uint32_t wrow = w_ring + wslot * kWBytes + r * kBK;
+        const uint32_t ta = tmem + lane_off + kACol0 + slot * 64;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 w4 = lds128(wrow + ((q ^ (r & 7)) << 4));
-          i8x4_to_f16x4(w4.x, v[8 * q + 0], v[8 * q + 1]);
-          i8x4_to_f16x4(w4.y, v[8 * q + 2], v[8 * q + 3]);
-          i8x4_to_f16x4(w4.z, v[8 * q + 4], v[8 * q + 5]);
-          i8x4_to_f16x4(w4.w, v[8 * q + 6], v[8 * q + 7]);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w4 = lds128(wrow + (((4 * h + q) ^ (r & 7)) << 4));
+            i8x4_to_f16x4(w4.x, v[8 * q + 0], v[8 * q + 1]);
+            i8x4_to_f16x4(w4.y, v[8 * q + 2], v[8 * q + 3]);
+            i8x4_to_f16x4(w4.z, v[8 * q + 4], v[8 * q + 5]);
+            i8x4_to_f16x4(w4.w, v[8 * q + 6], v[8 * q + 7]);
+          }
+          if (h == 1) {
+            // the weight stage is in registers: hand it back to the producer
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty_bar[wslot]);
+          }
+          tmem_st32(ta + 32 * h, v);
         }
-        // the weight stage is in registers: hand it back to the producer
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty_bar[slot]);
-        const uint32_t ta = tmem + lane_off + kACol0 + ab * 64;
-        tmem_st32(ta, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
-        tmem_st32(ta + 32, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull_bar[ab]);
+        if (lane == 0) mbar_arrive_remote(ready_remote0 + slot * (uint32_t)sizeof(uint64_t));
       }
     }
-  } else if (warp >= kDrainWarp0) {
+  } else {
     // ======================= drain + epilogue =======================
-    // warp w drains TMEM lanes 32*(w%4).. (output channels) and the 64 accumulator
-    // columns (row-tile rows) of half (w-12)/4
+    // warp w drains TMEM lanes 32*(w%4).. (output channels) and accumulator columns
+    // 64*cg .. +63 (token rows of the item), cg = (w-8)/4
+    regs_inc<kRegsDrain>();
     const int quarter = warp & 3;
-    const int chalf = (warp - kDrainWarp0) >> 2;
-    const int r = quarter * 32 + lane;  // output channel within the item
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + chalf * 64;
+    const int cg = (warp - kDrainWarp0) >> 2;
+    const int r = quarter * 32 + lane;  // output channel within this CTA's 128
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + cg * 64;
+    const uint32_t accempty_remote = cluster_addr(&accempty_bar, 0);
     const int nch = (nk + kChunkStages - 1) / kChunkStages;
     int c = 0;
     bool ok = true;
-    for (int j = blockIdx.x; j < total && ok; j += gridDim.x) {
-      const Item it = decode_item<T>(j, s_pref, s_end, E);
-      const float sc = __ldg(args.scale + (size_t)it.e * args.N + it.cb * kBN + r);
+    for (int j = pair; j < total && ok; j += npairs) {
+      const Item it = decode_item(j, s_pref, s_end, E);
+      const bool active = cg * 64 < it.n_mma;
       int acci[64];
 #pragma unroll
       for (int t = 0; t < 64; ++t) acci[t] = 0;
       for (int ch = 0; ch < nch; ++ch, ++c) {
-        const int acc = c & 1;
-        ok = wait_or_abort(&accfull_bar[acc], (c >> 1) & 1, abort_flag, args.status);
+        ok = wait_or_abort(&accfull_bar, c & 1, abort_flag, args.status);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
+        if (active) {
 #pragma unroll
-        for (int t0 = 0; t0 < 64; t0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(lane_base + kAccCol0 + acc * kAccStride + t0, v);
-          tmem_wait_ld();
+          for (int t0 = 0; t0 < 64; t0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(lane_base + t0, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acci[t0 + i] += __float2int_rn(__uint_as_float(v[i]));
+            for (int i = 0; i < 16; ++i) acci[t0 + i] += __float2int_rn(__uint_as_float(v[i]));
+          }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&accempty_bar[acc]);
+        if (lane == 0) mbar_arrive_remote(accempty_remote);
       }
       if (!ok) break;
-      // epilogue: channel r of rows row0 + 64*chalf + t (a warp writes 64 contiguous bytes per row)
-      const int t_lo = chalf * 64;
-      __half* dst = args.C + (size_t)(it.row0 + t_lo) * args.N + it.cb * kBN + r;
+      if (!active) continue;
+      // epilogue: channel r of rows row0 + 64*cg + t (a warp writes 64 contiguous bytes per row)
+      const int ch = it.cb * kPairCh + (int)rank * kBM + r;
+      if (ch < args.N) {
+        const float sc = __ldg(args.scale + (size_t)it.e * args.N + ch);
+        const int t_lo = cg * 64;
+        __half* dst = args.C + (size_t)(it.row0 + t_lo) * args.N + ch;
 #pragma unroll
-      for (int t = 0; t < 64; ++t)
-        if (t_lo + t < it.rows) dst[(size_t)t * args.N] = f2h_sat(__fmul_rn(__int2float_rn(acci[t]), sc));
+        for (int t = 0; t < 64; ++t)
+          if (t_lo + t < it.rows) dst[(size_t)t * args.N] = f2h_sat(__fmul_rn(__int2float_rn(acci[t]), sc));
+      }
     }
   }
 
   __syncthreads();
   if (threadIdx.x == 0) {
-    // copies still in flight (only after an abort) land before shared memory is released
+    // this CTA's copies still in flight (only after an abort) land before shared memory is released
     const int wi = s_w_issued, xi = s_x_issued;
     for (int n = max(0, wi - SW); n < wi; ++n) mbar_wait_bounded(&wfull_bar[n % SW], (n / SW) & 1);
-    for (int n = max(0, xi - SX); n < xi; ++n) mbar_wait_bounded(&xfull_bar[n % SX], (n / SX) & 1);
+    for (int n = max(0, xi - S); n < xi; ++n) mbar_wait_bounded(&xfull_bar[n % S], (n / S) & 1);
   }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the pair's MMAs or remote arrivals may touch it
   if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
   }
 }
 
-// ------------------------------------------------------------------------------
-// host side
-// ------------------------------------------------------------------------------
-template <int T>
-cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
-  using Cf = Cfg<T>;
+}  // namespace
+
+cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream) {
   CUtensorMap tw, tx;
   if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kBK,
-                            kBN))
+                            kBM))
     return cudaErrorInvalidValue;
-  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, T))
+  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64,
+                            kHalfRows))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<T>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM_BYTES);
+  static bool checked = false;
+  if (!checked) {
+    // The warpgroups' register split (setmaxnreg) adds up to exactly the registers
+    // the CTA is launched with; a build that launches with another count would
+    // leave the drains' increase waiting forever, so it is refused here.
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_pair_kernel);
     if (err != cudaSuccess) return err;
-    attr_set = true;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
+    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    checked = true;
   }
   Args a;
   a.cumsum = p.cumsum;
@@ -488,25 +579,20 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.E = p.E;
   a.N = p.N;
   a.Kd = p.Kd;
-  grouped_gemm_tc_kernel<T><<<sm_count(), kThreads, Cf::SMEM_BYTES, stream>>>(tw, tx, a);
+  const int grid = sm_count() & ~1;  // whole pairs, one CTA per SM
+  grouped_gemm_pair_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tw, tx, a);
   return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream) {
-  return launch_t<128>(p, stream);
-}
-
-// Engine choice.  A tcgen05.mma of M=128, K=16 costs about the same for any N up to
-// 128 (measured ~88 cycles on GB300), i.e. it consumes 2 KB of weights per issue
-// slot: with few rows per expert that caps weight streaming at about the HBM rate.
-// Warp-level HMMA (m16n8k16) consumes weights several times faster at N=8, so
-// batches with at most 24 rows per expert on average run on it with 16-row tiles,
-// larger ones on tcgen05 with 128-row tiles.  Measured at K=7168, I=2048, E=256:
-// 16 rows per expert, GMM1 1.64 ms on the warp-MMA engine against 2.92 ms on
-// tcgen05; 64 rows per expert, 4.97 ms against 3.73 ms.  The tile follows the mean
-// rows per expert (the host never reads device counts).
+// Engine choice.  A tcgen05.mma costs ~90 cycles for any N up to 128 (measured on
+// GB300) and consumes 2 KB of int8 weights per SM in that time: with few rows per
+// expert that caps weight streaming at about the HBM rate.  Warp-level HMMA
+// (m16n8k16) consumes weights several times faster at N=8, so batches with at
+// most 24 rows per expert on average run on it with 16-row tiles, larger ones on
+// the tcgen05 pairs.  Measured at K=7168, I=2048, E=256: 16 rows per expert, GMM1
+// 1.64 ms on the warp-MMA engine against 2.92 ms on single-CTA tcgen05; 64 rows
+// per expert, 4.97 ms against 3.73 ms.  The tile follows the mean rows per expert
+// (the host never reads device counts).
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream) {
   const double mean_rows = (double)p.R / (double)p.E;
   if (mean_rows <= 24.0) return launch_grouped_gemm_hmma(p, 16, stream);

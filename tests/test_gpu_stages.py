@@ -129,12 +129,12 @@ def _stage_inputs(w):
 
 
 GEMM_CASES = [
-    synth.Workload("g_small", 40, 256, 128, 8, 2, "uniform", 51),           # T=16 tile
+    synth.Workload("g_small", 40, 256, 128, 8, 2, "uniform", 51),           # warp-MMA engine
     synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # warp-MMA engine, ragged rows
-    synth.Workload("g_mid_tc", 320, 512, 192, 16, 2, "biased", 57),         # tcgen05 engine, ragged rows
-    synth.Workload("g_big", 384, 1024, 256, 4, 2, "zipf", 53),              # T=64 tile, hot expert
-    synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # many 512-deep chunks
-    synth.Workload("g_tiles", 700, 512, 192, 3, 2, "zipf", 55),             # 128-row tiles + tails, 64-deep tail
+    synth.Workload("g_mid_tc", 320, 512, 192, 16, 2, "biased", 57),         # tcgen05 pairs, N=64/128 tiles, 128-channel tail
+    synth.Workload("g_big", 384, 1024, 256, 4, 2, "zipf", 53),              # tcgen05 pairs, N=256 tiles, hot expert
+    synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # tcgen05 pairs, three 1024-deep chunks
+    synth.Workload("g_tiles", 700, 512, 192, 3, 2, "zipf", 55),             # 256-row tiles + tails, 64-deep tail
     synth.Workload("g_odd", 48, 384, 192, 8, 2, "uniform", 56),             # warp-MMA engine, 3 stages per item
 ]
 
@@ -168,13 +168,16 @@ def test_gmm2_bit_exact(w):
     assert_bits_equal(host(c2)[:Rv], c2_ref, "c2")
 
 
-def test_gmm_accumulator_exact_beyond_fp32_mantissa():
+@pytest.mark.parametrize("M,wv", [(8, 127), (40, 127), (40, -128)])
+def test_gmm_accumulator_exact_beyond_fp32_mantissa(M, wv):
     """Partial sums far above 2^24 that cancel to a small integer.  The reduction
-    runs +127*127 terms, then small terms, then -127*127 terms: a single fp32
+    runs +127*wv terms, then small terms, then -127*wv terms: a single fp32
     accumulator would reach ~5.6e7 (ulp 4) while adding the small terms and lose
     them; the exact chunked accumulation must return them bit for bit (scale 1,
-    |acc| < 2048, so binary16 holds the integer exactly)."""
-    M, K, I, E = 8, 7168, 64, 1
+    |acc| < 2048, so binary16 holds the integer exactly).  M=8 runs on the
+    warp-MMA engine, M=40 on the tcgen05 pairs, whose 1024-deep chunks reach
+    1024*127*128 < 2^24 with wv = -128."""
+    K, I, E = 7168, 64, 1
     mid = 168
     h = (K - mid) // 2
     rng = np.random.default_rng(5)
@@ -182,7 +185,7 @@ def test_gmm_accumulator_exact_beyond_fp32_mantissa():
     xq[:, :h], xq[:, h + mid:] = 127, -127
     xq[:, h:h + mid] = rng.integers(-2, 3, (M, mid))
     w1 = np.empty((E, 2 * I, K), np.int8)
-    w1[0, :, :h], w1[0, :, h + mid:] = 127, 127
+    w1[0, :, :h], w1[0, :, h + mid:] = wv, wv
     w1[0, :, h:h + mid] = rng.integers(-3, 4, (2 * I, mid))
     s1 = np.ones((E, 2 * I), np.float32)
     ei = np.zeros((M, 1), np.int32)
