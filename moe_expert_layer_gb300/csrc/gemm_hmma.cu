@@ -85,6 +85,7 @@ struct GemmArgs {
   __half* C;
   int32_t* status;
   int E, N, Kd;
+  int split_rows;  // this engine serves the experts with at most split_rows rows
 };
 
 // 4 int8 (one 32-bit word) -> two half2 {b0,b1}, {b2,b3}, exactly.
@@ -186,6 +187,15 @@ struct Item {
   int e, cb, row0, rows;
 };
 
+// Work items of an expert with `cnt` rows on this engine: its row tiles x channel
+// blocks, or none when the expert has more than split_rows rows (the tcgen05 pairs
+// take it).  Experts without items leave the prefix flat, and the binary search in
+// decode_item (last expert whose first item is <= j) skips them.
+template <int T>
+__device__ __forceinline__ int own_items(int cnt, int split_rows, int n_cb) {
+  return cnt <= split_rows ? (cnt + T - 1) / T * n_cb : 0;
+}
+
 // Work item j -> (expert, channel block, first row, rows).  Items are ordered
 // expert-major, then channel block, then row tile, so CTAs that run at the
 // same time share weight blocks through L2.
@@ -238,7 +248,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     for (int e = e0; e < e1; ++e) {
       const int hi = __ldg(args.cumsum + e), lo = e ? __ldg(args.cumsum + e - 1) : 0;
       s_end[e] = hi;
-      local += (hi - lo + T - 1) / T * n_cb;
+      local += own_items<T>(hi - lo, args.split_rows, n_cb);
     }
     int incl = local;
 #pragma unroll
@@ -253,7 +263,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     for (int e = e0; e < e1; ++e) {
       s_pref[e] = run;
       const int lo = e ? s_end[e - 1] : 0;
-      run += (s_end[e] - lo + T - 1) / T * n_cb;
+      run += own_items<T>(s_end[e] - lo, args.split_rows, n_cb);
     }
     if (e0 < E && e1 == E) s_pref[E] = run;
   } else if (lane == 0) {
@@ -502,6 +512,7 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.E = p.E;
   a.N = p.N;
   a.Kd = p.Kd;
+  a.split_rows = p.split_rows;
   grouped_gemm_kernel<T><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
   return cudaGetLastError();
 }

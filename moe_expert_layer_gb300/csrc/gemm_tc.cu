@@ -66,6 +66,11 @@
 
 namespace moe {
 
+#ifdef MOE_GEMM_PROFILE
+static unsigned long long* g_gemm_prof = nullptr;
+extern "C" void moe_gemm_profile_set(void* p) { g_gemm_prof = static_cast<unsigned long long*>(p); }
+#endif
+
 namespace {
 
 constexpr int kThreads = 768;
@@ -104,7 +109,32 @@ struct Args {
   __half* C;
   int32_t* status;
   int E, N, Kd;
+  int split_rows;  // this engine serves the experts with more than split_rows rows
+#ifdef MOE_GEMM_PROFILE
+  unsigned long long* prof;
+#endif
 };
+
+// Role timing, compiled in only with -DMOE_GEMM_PROFILE: each role sums clock64()
+// intervals (time in a wait, time doing its work) into registers and adds them to
+// a 32-slot device buffer at the end.  Slot bases: weight producer 0, token producer
+// 2, relay 4, MMA issuer 8, converters 16, drains 24, issuer's total 31.
+#ifdef MOE_GEMM_PROFILE
+#define PROF_REGS unsigned long long _pf[6] = {0, 0, 0, 0, 0, 0}
+#define PROF_WAIT(i, expr) ([&]() { const long long _t0 = clock64(); const bool _r = (expr); \
+                                    _pf[i] += clock64() - _t0; return _r; }())
+#define PROF_T0(v) const long long v = clock64()
+#define PROF_ADD(i, t0) (_pf[i] += clock64() - (t0))
+#define PROF_FLUSH(base) for (int _i = 0; _i < 6; ++_i) if (_pf[_i]) atomicAdd(args.prof + (base) + _i, _pf[_i])
+#define PROF_TOTAL(t0) atomicAdd(args.prof + 31, (unsigned long long)(clock64() - (t0)))
+#else
+#define PROF_REGS
+#define PROF_WAIT(i, expr) (expr)
+#define PROF_T0(v)
+#define PROF_ADD(i, t0)
+#define PROF_FLUSH(base)
+#define PROF_TOTAL(t0)
+#endif
 
 // ------------------------------------------------------------------ cluster / tcgen05 helpers
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -219,6 +249,14 @@ struct Item {
   int e, cb, row0, rows, n_mma;
 };
 
+// Work items of an expert with `cnt` rows on the pairs: its row tiles x channel
+// blocks, or none when it has at most split_rows rows (the warp-MMA engine takes
+// it).  Experts without items leave the prefix flat, and the binary search in
+// decode_item (last expert whose first item is <= j) skips them.
+__device__ __forceinline__ int own_items(int cnt, int split_rows, int n_cb) {
+  return cnt > split_rows ? (cnt + kTileRows - 1) / kTileRows * n_cb : 0;
+}
+
 // Work item j -> (expert, channel block, first row, rows, MMA N).  Items run
 // expert-major, then channel block, then row tile: pairs working at the same time
 // share weight blocks through L2.
@@ -242,11 +280,37 @@ __device__ __forceinline__ Item decode_item(int j, const int* s_pref, const int*
   return it;
 }
 
+// try_wait that lets the warp sleep in hardware until the phase completes (up to
+// `hint_ns`), instead of re-issuing probes that take issue slots from the MMA warp.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false after about two seconds of %globaltimer.
+__device__ __forceinline__ bool mbar_wait_sleep_bounded(uint64_t* bar, uint32_t parity) {
+  constexpr uint32_t kHintNs = 100000;
+  if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait_sleep(bar, parity, kHintNs)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                               int32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;  // fast path: one probe of a completed phase
   if (*abort_flag) return false;
-  if (mbar_wait_bounded(bar, parity)) return true;
+  if (mbar_wait_sleep_bounded(bar, parity)) return true;
   *abort_flag = 1;
   record_status(status, MOE_ERR_TIMEOUT);
   return false;
@@ -270,6 +334,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int E = args.E, n_cb = (args.N + kPairCh - 1) / kPairCh;
   const int nk = (args.Kd + kBK - 1) / kBK;  // a 64-deep tail reads TMA zero fill
+  PROF_T0(t_start);
+  PROF_REGS;
   volatile int* abort_flag = &s_abort;
 
   // ---- work list (s_pref[e] = first work item of expert e), barriers, tensor memory
@@ -280,7 +346,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int e = e0; e < e1; ++e) {
       const int hi = __ldg(args.cumsum + e), lo = e ? __ldg(args.cumsum + e - 1) : 0;
       s_end[e] = hi;
-      local += (hi - lo + kTileRows - 1) / kTileRows * n_cb;
+      local += own_items(hi - lo, args.split_rows, n_cb);
     }
     int incl = local;
 #pragma unroll
@@ -326,13 +392,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int e = e0; e < e1; ++e) {
       s_pref[e] = run;
       const int lo = e ? s_end[e - 1] : 0;
-      run += (s_end[e] - lo + kTileRows - 1) / kTileRows * n_cb;
+      run += own_items(s_end[e] - lo, args.split_rows, n_cb);
     }
     if (e0 < E && e1 == E) s_pref[E] = run;
   }
   __syncthreads();
   cluster_sync_all();  // the peer's barriers and tensor memory are ready
   tc_fence_after();
+  PROF_ADD(5, t_start);
   const int total = s_pref[E];
   const uint32_t tmem = s_tmem;
 
@@ -352,13 +419,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int w_row = it.e * args.N + it.cb * kPairCh + (int)rank * kBM;
           for (int kb = 0; kb < nk; ++kb, ++n) {
             const int slot = n % SW;
-            if (!wait_or_abort(&wempty_bar[slot], ((n / SW) & 1) ^ 1, abort_flag, args.status)) goto w_done;
+            if (!PROF_WAIT(0, wait_or_abort(&wempty_bar[slot], ((n / SW) & 1) ^ 1, abort_flag, args.status)))
+              goto w_done;
             mbar_arrive_expect_tx(&wfull_bar[slot], (uint32_t)kWBytes);
             tma_load_2d(smem_gen + slot * kWBytes, &tm_w, kb * kBK, w_row, &wfull_bar[slot]);
           }
         }
       w_done:
         s_w_issued = n;
+        PROF_FLUSH(0);
       }
     } else if (warp == kXProducerWarp) {
       // ======================= token producer (one lane) =======================
@@ -369,7 +438,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int y = it.row0 + (int)rank * (it.n_mma >> 1);
           for (int kb = 0; kb < nk; ++kb, ++n) {
             const int slot = n % S;
-            if (!wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status)) goto x_done;
+            if (!PROF_WAIT(0, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status)))
+              goto x_done;
             uint8_t* xs_g = smem_gen + SW * kWBytes + slot * kXBytes;
             mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)kXBytes);
             tma_load_2d(xs_g, &tm_x, kb * kBK, y, &xfull_bar[slot]);
@@ -378,6 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       x_done:
         s_x_issued = n;
+        PROF_FLUSH(2);
       }
     } else if (warp == kRelayWarp) {
       // ======================= relay: token stage landed -> CTA 0's stage barrier =======================
@@ -388,11 +459,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = pair; j < total && ok; j += npairs) {
           for (int kb = 0; kb < nk; ++kb, ++n) {
             const int slot = n % S;
-            ok = wait_or_abort(&xfull_bar[slot], (n / S) & 1, abort_flag, args.status);
+            ok = PROF_WAIT(0, wait_or_abort(&xfull_bar[slot], (n / S) & 1, abort_flag, args.status));
             if (!ok) break;
             mbar_arrive_remote(ready_remote0 + slot * (uint32_t)sizeof(uint64_t));
           }
         }
+        PROF_FLUSH(4);
       }
     } else {
       // ======================= MMA issuer (CTA 0, one thread) =======================
@@ -403,15 +475,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const Item it = decode_item(j, s_pref, s_end, E);
           const uint32_t idesc = kIdescBase | ((uint32_t)(it.n_mma >> 3) << 17);
           for (int kb = 0; kb < nk && ok; ++kb, ++n) {
+            PROF_T0(t_body);
             const int slot = n % S;
             const uint32_t ph = (n / S) & 1;
             if (kb % kChunkStages == 0) {
               // a new exact chunk: both CTAs' drains must have read the accumulator
-              ok = wait_or_abort(&accempty_bar, (c & 1) ^ 1, abort_flag, args.status);
+              ok = PROF_WAIT(0, wait_or_abort(&accempty_bar, (c & 1) ^ 1, abort_flag, args.status));
               if (!ok) break;
             }
-            ok = wait_or_abort(&ready_bar[slot], ph, abort_flag, args.status);
+            ok = PROF_WAIT(1, wait_or_abort(&ready_bar[slot], ph, abort_flag, args.status));
             if (!ok) break;
+            PROF_T0(t_issue);
             tc_fence_after();
             const uint32_t xs = x_ring + slot * kXBytes;
             const uint32_t a_tmem = tmem + kACol0 + slot * 64;
@@ -421,16 +495,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const uint64_t bdesc = sw128_desc(xs + (s >> 2) * kXHalfBytes + (s & 3) * 32);
               mma_pair(tmem, a_tmem + s * 8, bdesc, idesc, (kb % kChunkStages != 0 || s != 0) ? 1u : 0u);
             }
+            PROF_ADD(2, t_issue);
+            PROF_T0(t_commit);
             mma_commit_pair(&sdone_bar[slot]);  // token slot and A buffer free once these MMAs complete
+            PROF_ADD(3, t_commit);
             if (kb % kChunkStages == kChunkStages - 1 || kb == nk - 1) {
               mma_commit_pair(&accfull_bar);    // chunk accumulated: hand it to the drains
               ++c;
             }
+            PROF_ADD(4, t_body);
           }
         }
         // every MMA issued by this thread has completed once final_bar fires
         mma_commit_local(&final_bar);
         mbar_wait_bounded(&final_bar, 0);
+        PROF_FLUSH(8);
+        PROF_TOTAL(t_start);
       }
       __syncwarp();
     }
@@ -448,10 +528,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int j = pair; j < total && ok; j += npairs) {
       for (int kb = 0; kb < nk; ++kb, ++n) {
         const int slot = n % S, wslot = n % SW;
-        ok = wait_or_abort(&wfull_bar[wslot], (n / SW) & 1, abort_flag, args.status) &&
-             wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status);
+        ok = PROF_WAIT(0, wait_or_abort(&wfull_bar[wslot], (n / SW) & 1, abort_flag, args.status)) &&
+             PROF_WAIT(1, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        PROF_T0(t_conv);
         tc_fence_after();
         const uint32_t wrow = w_ring + wslot * kWBytes + r * kBK;
         const uint32_t ta = tmem + lane_off + kACol0 + slot * 64;
@@ -477,8 +558,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(ready_remote0 + slot * (uint32_t)sizeof(uint64_t));
+        PROF_ADD(2, t_conv);
       }
     }
+    if (lane == 0) PROF_FLUSH(16);
   } else {
     // ======================= drain + epilogue =======================
     // warp w drains TMEM lanes 32*(w%4).. (output channels) and accumulator columns
@@ -499,9 +582,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < 64; ++t) acci[t] = 0;
       for (int ch = 0; ch < nch; ++ch, ++c) {
-        ok = wait_or_abort(&accfull_bar, c & 1, abort_flag, args.status);
+        ok = PROF_WAIT(0, wait_or_abort(&accfull_bar, c & 1, abort_flag, args.status));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
+        PROF_T0(t_drain);
         tc_fence_after();
         if (active) {
 #pragma unroll
@@ -516,9 +600,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(accempty_remote);
+        PROF_ADD(1, t_drain);
       }
       if (!ok) break;
       if (!active) continue;
+      PROF_T0(t_epi);
       // epilogue: channel r of rows row0 + 64*cg + t (a warp writes 64 contiguous bytes per row)
       const int ch = it.cb * kPairCh + (int)rank * kBM + r;
       if (ch < args.N) {
@@ -529,7 +615,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 64; ++t)
           if (t_lo + t < it.rows) dst[(size_t)t * args.N] = f2h_sat(__fmul_rn(__int2float_rn(acci[t]), sc));
       }
+      PROF_ADD(2, t_epi);
     }
+    if (lane == 0) PROF_FLUSH(24);
   }
 
   __syncthreads();
@@ -579,6 +667,11 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
   a.E = p.E;
   a.N = p.N;
   a.Kd = p.Kd;
+  a.split_rows = p.split_rows;
+#ifdef MOE_GEMM_PROFILE
+  a.prof = g_gemm_prof;
+  if (!a.prof) return cudaErrorInvalidValue;
+#endif
   const int grid = sm_count() & ~1;  // whole pairs, one CTA per SM
   grouped_gemm_pair_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tw, tx, a);
   return cudaGetLastError();
@@ -586,17 +679,27 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
 
 // Engine choice.  A tcgen05.mma costs ~90 cycles for any N up to 128 (measured on
 // GB300) and consumes 2 KB of int8 weights per SM in that time: with few rows per
-// expert that caps weight streaming at about the HBM rate.  Warp-level HMMA
-// (m16n8k16) consumes weights several times faster at N=8, so batches with at
-// most 24 rows per expert on average run on it with 16-row tiles, larger ones on
-// the tcgen05 pairs.  Measured at K=7168, I=2048, E=256: 16 rows per expert, GMM1
-// 1.64 ms on the warp-MMA engine against 2.92 ms on single-CTA tcgen05; 64 rows
-// per expert, 4.97 ms against 3.73 ms.  The tile follows the mean rows per expert
-// (the host never reads device counts).
+// expert that caps weight streaming at about the HBM rate before any overhead.
+// Warp-level HMMA (m16n8k16) consumes weights several times faster at N=8.  So
+// batches with at most 24 rows per expert on average run entirely on the warp-MMA
+// engine with 16-row tiles (GMM1 at K=7168, I=2048, E=256, 16 rows per expert:
+// 1.64 ms against 2.92 ms on single-CTA tcgen05).  Larger batches split by expert
+// on the device: experts with at most kSplitRows rows go to the warp-MMA engine,
+// the others to the tcgen05 pairs; both kernels derive their share from cumsum, so
+// the host never reads device counts (a kernel with no share exits at once).
+constexpr int kSplitRows = 16;
+
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream) {
+  GroupedGemmProblem q = p;
   const double mean_rows = (double)p.R / (double)p.E;
-  if (mean_rows <= 24.0) return launch_grouped_gemm_hmma(p, 16, stream);
-  return launch_grouped_gemm_tc(p, stream);
+  if (mean_rows <= 24.0) {
+    q.split_rows = 0x7fffffff;
+    return launch_grouped_gemm_hmma(q, 16, stream);
+  }
+  q.split_rows = kSplitRows;
+  cudaError_t err = launch_grouped_gemm_hmma(q, 16, stream);
+  if (err != cudaSuccess) return err;
+  return launch_grouped_gemm_tc(q, stream);
 }
 
 }  // namespace moe

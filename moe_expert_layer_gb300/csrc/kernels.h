@@ -33,6 +33,8 @@ struct GroupedGemmProblem {
   uint16_t* C;                      // [R][N]
   int R, E, N, Kd;
   int32_t* status;                  // device status word
+  int split_rows;                   // experts with <= split_rows rows run on the warp-MMA engine,
+                                    // the others on the tcgen05 pairs (set by launch_grouped_gemm)
 };
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream);     // picks an engine
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream);  // gemm_hmma.cu

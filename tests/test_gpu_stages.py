@@ -136,6 +136,7 @@ GEMM_CASES = [
     synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # tcgen05 pairs, three 1024-deep chunks
     synth.Workload("g_tiles", 700, 512, 192, 3, 2, "zipf", 55),             # 256-row tiles + tails, 64-deep tail
     synth.Workload("g_odd", 48, 384, 192, 8, 2, "uniform", 56),             # warp-MMA engine, 3 stages per item
+    synth.Workload("g_hybrid", 400, 512, 192, 32, 2, "zipf", 58),           # both engines: small experts on warp MMA
 ]
 
 
