@@ -245,6 +245,21 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
 }
 
+// Exact int32 of an integer-valued fp32 v with |v| <= 2^24, on the FMA and integer
+// pipes: v = 4096*hi + lo with hi = rint(v / 4096) and |lo| <= 2048, each part
+// read off the mantissa after adding 1.5 * 2^23 (all steps exact in fp32).  The
+// drains convert two of every three values this way and the rest with cvt.rni
+// (whose ~16 conversions per cycle per SM alone would set the drain time).
+__device__ __forceinline__ int f2i_exact(float v) {
+  const float kMagic = 12582912.0f;  // 1.5 * 2^23
+  const float h = __fmaf_rn(v, 1.0f / 4096.0f, kMagic);
+  const float hi = __fsub_rn(h, kMagic);
+  const float lo = __fmaf_rn(-hi, 4096.0f, v);
+  const float l = __fadd_rn(lo, kMagic);
+  return (int)(((uint32_t)__float_as_int(h) << 12) + (uint32_t)__float_as_int(l) -
+               ((0x4B400000u << 12) + 0x4B400000u));
+}
+
 struct Item {
   int e, cb, row0, rows, n_mma;
 };
@@ -594,7 +609,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld16(lane_base + t0, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acci[t0 + i] += __float2int_rn(__uint_as_float(v[i]));
+            for (int i = 0; i < 16; ++i) {
+              const float f = __uint_as_float(v[i]);
+              acci[t0 + i] += (i % 3 == 0) ? __float2int_rn(f) : f2i_exact(f);
+            }
           }
         }
         tc_fence_before();
