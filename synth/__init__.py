@@ -69,6 +69,7 @@ CONFIGS = {
     "skewed": Workload("skewed", 2048, 7168, 2048, 256, 8, "zipf", 3),
     "prefill": Workload("prefill", 8192, 4096, 1408, 64, 6, "uniform", 4),
     "decode16": Workload("decode16", 8, 7168, 2048, 16, 8, "uniform", 5),
+    "mid16": Workload("mid16", 512, 7168, 2048, 16, 8, "biased", 6),
 }
 
 
