@@ -51,6 +51,8 @@ template <int T>
 struct TileShape;
 template <>
 struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 4; };
+template <>
+struct TileShape<32> { static constexpr int WM = 8, WN = 1, STAGES = 4; };
 
 template <int T>
 struct GemmCfg {
@@ -149,6 +151,33 @@ __device__ __forceinline__ void hmma_half_stage(const uint8_t* xh, const uint8_t
         mma_f16_16816(accf[sl % Cfg::P][mt][nt], a0, a1, a2, a3, b0, b1);
       }
     }
+  }
+}
+
+// A whole stage (all 64-deep k quarters) with NTL live n8 tiles.
+template <class Cfg, int NTL>
+__device__ __forceinline__ void hmma_stage(const uint8_t* xs, const uint8_t* ws, int warp_m, int warp_n, int g, int tq,
+                                           int pg, float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
+#pragma unroll
+  for (int q = 0; q < kQuarters; ++q)
+    hmma_half_stage<Cfg, NTL>(xs + q * Cfg::X_HALF_BYTES, ws + (q >> 1) * Cfg::W_SUB_BYTES, q & 1, warp_m, warp_n, g,
+                              tq, pg, accf);
+}
+
+// Dispatch on the live n8 tiles of the item (rows beyond the item's rows are
+// skipped, so the MMA work follows the real row count).
+template <class Cfg>
+__device__ __forceinline__ void hmma_stage_live(int live_nt, const uint8_t* xs, const uint8_t* ws, int warp_m,
+                                                int warp_n, int g, int tq, int pg,
+                                                float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
+  if (Cfg::NT >= 4 && live_nt >= 4) {
+    hmma_stage<Cfg, (Cfg::NT >= 4 ? 4 : 1)>(xs, ws, warp_m, warp_n, g, tq, pg, accf);
+  } else if (Cfg::NT >= 3 && live_nt == 3) {
+    hmma_stage<Cfg, (Cfg::NT >= 3 ? 3 : 1)>(xs, ws, warp_m, warp_n, g, tq, pg, accf);
+  } else if (live_nt >= 2) {
+    hmma_stage<Cfg, 2>(xs, ws, warp_m, warp_n, g, tq, pg, accf);
+  } else if (live_nt == 1) {
+    hmma_stage<Cfg, 1>(xs, ws, warp_m, warp_n, g, tq, pg, accf);
   }
 }
 
@@ -383,17 +412,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           const uint8_t* xs = smem_gen + slot * Cfg::STAGE_BYTES;
           const uint8_t* ws = xs + Cfg::X_BYTES;
           // one uniform branch per stage on the number of live n8 tiles
-          if (live_nt >= 2) {
-#pragma unroll
-            for (int q = 0; q < kQuarters; ++q)
-              hmma_half_stage<Cfg, Cfg::NT>(xs + q * Cfg::X_HALF_BYTES, ws + (q >> 1) * Cfg::W_SUB_BYTES, q & 1,
-                                            warp_m, warp_n, g, tq, pg, accf);
-          } else if (live_nt == 1) {
-#pragma unroll
-            for (int q = 0; q < kQuarters; ++q)
-              hmma_half_stage<Cfg, 1>(xs + q * Cfg::X_HALF_BYTES, ws + (q >> 1) * Cfg::W_SUB_BYTES, q & 1, warp_m,
-                                      warp_n, g, tq, pg, accf);
-          }
+          hmma_stage_live<Cfg>(live_nt, xs, ws, warp_m, warp_n, g, tq, pg, accf);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty_bar[slot]);
           ++consumed;
@@ -520,7 +539,7 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream) {
-  (void)T;  // 16-row tiles (the engine serves decode-sized batches)
+  if (T == 32) return launch_t<32>(p, stream);
   return launch_t<16>(p, stream);
 }
 

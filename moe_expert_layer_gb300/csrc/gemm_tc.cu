@@ -700,8 +700,8 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
 // expert that caps weight streaming at about the HBM rate before any overhead.
 // Warp-level HMMA (m16n8k16) consumes weights several times faster at N=8.  So
 // batches with at most 24 rows per expert on average run entirely on the warp-MMA
-// engine with 16-row tiles (GMM1 at K=7168, I=2048, E=256, 16 rows per expert:
-// 1.64 ms against 2.92 ms on single-CTA tcgen05).  Larger batches split by expert
+// engine (GMM1 at K=7168, I=2048, E=256, 16 rows per expert: 1.64 ms with 16-row
+// tiles against 2.92 ms on single-CTA tcgen05).  Larger batches split by expert
 // on the device: experts with at most kSplitRows rows go to the warp-MMA engine,
 // the others to the tcgen05 pairs; both kernels derive their share from cumsum, so
 // the host never reads device counts (a kernel with no share exits at once).
@@ -711,8 +711,10 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream
   GroupedGemmProblem q = p;
   const double mean_rows = (double)p.R / (double)p.E;
   if (mean_rows <= 24.0) {
+    // 16-row tiles up to 8 rows per expert on average (decode); 32-row tiles above,
+    // so that an expert of up to 32 rows streams its weights through one work item
     q.split_rows = 0x7fffffff;
-    return launch_grouped_gemm_hmma(q, 16, stream);
+    return launch_grouped_gemm_hmma(q, mean_rows <= 8.0 ? 16 : 32, stream);
   }
   q.split_rows = kSplitRows;
   cudaError_t err = launch_grouped_gemm_hmma(q, 16, stream);

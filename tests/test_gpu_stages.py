@@ -129,8 +129,9 @@ def _stage_inputs(w):
 
 
 GEMM_CASES = [
-    synth.Workload("g_small", 40, 256, 128, 8, 2, "uniform", 51),           # warp-MMA engine
-    synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # warp-MMA engine, ragged rows
+    synth.Workload("g_dec", 60, 512, 128, 16, 2, "uniform", 59),            # warp-MMA engine, 16-row tiles
+    synth.Workload("g_small", 40, 256, 128, 8, 2, "uniform", 51),           # warp-MMA engine, 32-row tiles
+    synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # warp-MMA engine, 32-row tiles, ragged
     synth.Workload("g_mid_tc", 320, 512, 192, 16, 2, "biased", 57),         # tcgen05 pairs, N=64/128 tiles, 128-channel tail
     synth.Workload("g_big", 384, 1024, 256, 4, 2, "zipf", 53),              # tcgen05 pairs, N=256 tiles, hot expert
     synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # tcgen05 pairs, three 1024-deep chunks
