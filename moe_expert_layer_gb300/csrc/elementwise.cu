@@ -22,6 +22,21 @@ union Vec8h {
 
 constexpr int kRowThreads = 256;
 
+// Integer-valued conversions without the conversion pipe (~16 per cycle per SM),
+// all exact for the ranges used here:
+//   rint_small(v):  round-half-even of |v| < 2^22, read off the mantissa of v + 1.5*2^23
+//   codes_to_half2: two integers in [-127, 127] -> their binary16 pair, by placing
+//                   q+128 in the mantissa of 1024 and subtracting 1152 (sub.f16x2)
+__device__ __forceinline__ int rint_small(float v) {
+  return __float_as_int(__fadd_rn(v, 12582912.0f)) - 0x4B400000;
+}
+__device__ __forceinline__ uint32_t codes_to_half2(int q0, int q1) {
+  const uint32_t w = (uint32_t)(0x6400 + q0 + 128) | ((uint32_t)(0x6400 + q1 + 128) << 16);
+  uint32_t r;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0x64806480u));
+  return r;
+}
+
 // --------------------------------------------------------------------------
 // per-token dynamic quant: pts1 = amax / 127, q = round_half_away(x / pts1)
 // --------------------------------------------------------------------------
@@ -43,7 +58,7 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int idx = threadIdx.x + i * kRowThreads;
+    const int idx = threadIdx.x + i * (int)blockDim.x;
     if (idx < nvec) {
       v[i].v = __ldg(row + idx);
 #pragma unroll
@@ -55,12 +70,12 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
   if (threadIdx.x == 0) pts1[t] = scale;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int idx = threadIdx.x + i * kRowThreads;
+    const int idx = threadIdx.x + i * (int)blockDim.x;
     if (idx < nvec) {
       int q[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        q[j] = (amax > 0.0f) ? clamp127((int)roundf(__fdiv_rn(__half2float(v[i].h[j]), scale))) : 0;
+        q[j] = (amax > 0.0f) ? clamp127(rint_small(roundf(__fdiv_rn(__half2float(v[i].h[j]), scale)))) : 0;
       if (xq_i8) {
         uint2 packed;
         packed.x = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
@@ -70,14 +85,16 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
         reinterpret_cast<uint2*>(xq_i8 + (size_t)t * K)[idx] = packed;
       }
       if (xq_f16 || expanded_row_idx) {
-        Vec8h o;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) o.h[j] = __int2half_rn(q[j]);
-        if (xq_f16) reinterpret_cast<int4*>(xq_f16 + (size_t)t * K)[idx] = o.v;
+        int4 o;
+        o.x = (int)codes_to_half2(q[0], q[1]);
+        o.y = (int)codes_to_half2(q[2], q[3]);
+        o.z = (int)codes_to_half2(q[4], q[5]);
+        o.w = (int)codes_to_half2(q[6], q[7]);
+        if (xq_f16) reinterpret_cast<int4*>(xq_f16 + (size_t)t * K)[idx] = o;
         if (expanded_row_idx) {
           for (int s = 0; s < topK; ++s) {
             const int d = __ldg(expanded_row_idx + (size_t)t * topK + s);
-            if (d >= 0) reinterpret_cast<int4*>(a1 + (size_t)d * K)[idx] = o.v;
+            if (d >= 0) reinterpret_cast<int4*>(a1 + (size_t)d * K)[idx] = o;
           }
         }
       }
@@ -104,7 +121,7 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int idx = threadIdx.x + i * kRowThreads;
+    const int idx = threadIdx.x + i * (int)blockDim.x;
     if (idx < nvec) {
       Vec8h g, u;
       g.v = __ldg(gate + idx);
@@ -113,7 +130,10 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
       for (int j = 0; j < 8; ++j) {
         const float hg = __fmul_rn(__half2float(g.h[j]), p1);
         const float hu = __fmul_rn(__half2float(u.h[j]), p1);
-        const float silu = __fdiv_rn(hg, __fadd_rn(1.0f, expf(-hg)));
+        // exp and the division on the MUFU fast paths (ex2 / rcp, a few ulp): SwiGLU
+        // is instruction-bound, and the requantised codes tolerate it (the pages'
+        // exp is a different library's in any case)
+        const float silu = __fdividef(hg, __fadd_rn(1.0f, __expf(-hg)));
         y[i][j] = __fmul_rn(silu, hu);
         amax = fmaxf(amax, fabsf(y[i][j]));
       }
@@ -125,11 +145,11 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
   if (threadIdx.x == 0) pts2[d] = nz ? __fdiv_rn(amax, 127.0f) : 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
-    const int idx = threadIdx.x + i * kRowThreads;
+    const int idx = threadIdx.x + i * (int)blockDim.x;
     if (idx < nvec) {
       int q[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) q[j] = nz ? clamp127(__float2int_rn(__fmul_rn(y[i][j], inv))) : 0;
+      for (int j = 0; j < 8; ++j) q[j] = nz ? clamp127(rint_small(__fmul_rn(y[i][j], inv))) : 0;
       if (q2_i8) {
         uint2 packed;
         packed.x = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
@@ -139,10 +159,12 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
         reinterpret_cast<uint2*>(q2_i8 + (size_t)d * I)[idx] = packed;
       }
       if (q2_f16) {
-        Vec8h o;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) o.h[j] = __int2half_rn(q[j]);
-        reinterpret_cast<int4*>(q2_f16 + (size_t)d * I)[idx] = o.v;
+        int4 o;
+        o.x = (int)codes_to_half2(q[0], q[1]);
+        o.y = (int)codes_to_half2(q[2], q[3]);
+        o.z = (int)codes_to_half2(q[4], q[5]);
+        o.w = (int)codes_to_half2(q[6], q[7]);
+        reinterpret_cast<int4*>(q2_f16 + (size_t)d * I)[idx] = o;
       }
     }
   }
@@ -183,23 +205,31 @@ __global__ void __launch_bounds__(kCombineThreads) combine_unpermute_kernel(
   reinterpret_cast<int4*>(out + (size_t)t * K)[vec] = o.v;
 }
 
+// Threads for a row of nvec 16-byte vectors handled vpt per thread: whole warps,
+// no more than the row needs (a 1408-wide SwiGLU row runs on 192 threads, not 256).
+int row_threads(int nvec, int vpt) {
+  const int t = (nvec + vpt - 1) / vpt;
+  return (t + 31) / 32 * 32;
+}
+
 }  // namespace
 
 cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16, float* pts1,
                                 const int32_t* expanded_row_idx, int topK, uint16_t* a1, cudaStream_t stream) {
   const int nvec = K / 8;
   const int vpt = (nvec + kRowThreads - 1) / kRowThreads;
+  const int threads = row_threads(nvec, vpt);
   const __half* xh = reinterpret_cast<const __half*>(x);
   __half* qf = reinterpret_cast<__half*>(xq_f16);
   __half* ah = reinterpret_cast<__half*>(a1);
   if (vpt <= 1)
-    quant_tokens_kernel<1><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
+    quant_tokens_kernel<1><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
   else if (vpt <= 2)
-    quant_tokens_kernel<2><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
+    quant_tokens_kernel<2><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
   else if (vpt <= 4)
-    quant_tokens_kernel<4><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
+    quant_tokens_kernel<4><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
   else if (vpt <= 8)
-    quant_tokens_kernel<8><<<M, kRowThreads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
+    quant_tokens_kernel<8><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -210,16 +240,17 @@ cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int top
                                 uint16_t* q2_f16, float* pts2, cudaStream_t stream) {
   const int nvec = I / 8;
   const int vpt = (nvec + kRowThreads - 1) / kRowThreads;
+  const int threads = row_threads(nvec, vpt);
   const __half* ch = reinterpret_cast<const __half*>(c1);
   __half* qf = reinterpret_cast<__half*>(q2_f16);
   if (vpt <= 1)
-    swiglu_quant_kernel<1><<<R, kRowThreads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
+    swiglu_quant_kernel<1><<<R, threads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
                                                           qf, pts2);
   else if (vpt <= 2)
-    swiglu_quant_kernel<2><<<R, kRowThreads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
+    swiglu_quant_kernel<2><<<R, threads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
                                                           qf, pts2);
   else if (vpt <= 4)
-    swiglu_quant_kernel<4><<<R, kRowThreads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
+    swiglu_quant_kernel<4><<<R, threads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
                                                           qf, pts2);
   else
     return cudaErrorInvalidValue;

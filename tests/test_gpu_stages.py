@@ -217,10 +217,13 @@ def test_gmm_empty_experts_and_single_rows():
 
 
 # ------------------------------------------------------------------ SwiGLU
-@pytest.mark.parametrize("R,I", [(64, 256), (300, 2048), (77, 1408), (5, 8192)])
-def test_swiglu_quant(R, I):
+@pytest.mark.parametrize("R,I,spread", [(64, 256, 1500), (300, 2048, 1500), (77, 1408, 1500), (5, 8192, 1500),
+                                         (2000, 1408, 100), (300, 2048, 30)])
+def test_swiglu_quant(R, I, spread):
+    """spread 1500 puts the SwiGLU inputs h at |h| ~ 45 (as the workloads do);
+    100 and 30 at |h| ~ 3 and ~1, where exp(-h) and the division shape every value."""
     rng = np.random.default_rng(R + I)
-    c1 = (rng.standard_normal((R, 2 * I)) * 1500).astype(np.float16)
+    c1 = (rng.standard_normal((R, 2 * I)) * spread).astype(np.float16)
     c1[1] = 0
     topK = 1
     M = R
