@@ -290,19 +290,22 @@ def main():
     q2, pts2 = torch.empty((R, w.I), dtype=f16, device="cuda"), torch.empty(R, dtype=f32, device="cuda")
     c2 = torch.empty((R, w.K), dtype=f16, device="cuda")
     gws = torch.empty(moe.moe_gmm_workspace_size(d), dtype=torch.uint8, device="cuda")
+    bounds = torch.zeros((2, w.E, moe.BOUND_SEGMENTS), dtype=i32, device="cuda")  # activation bounds of a1, q2
     names = ["route_sort", "quant", "gmm1", "swiglu", "gmm2", "combine"]
 
     def stages(evs):
+        with torch.cuda.stream(stream):
+            bounds.zero_()  # the layer clears them with its status word
         evs[0].record(stream)
         moe.moe_route_sort(d, dev["expert_idx"], sorted_, expanded, tpe, cs, sws, stream)
         evs[1].record(stream)
-        moe.moe_quant_dispatch(d, dev["x"], expanded, a1, pts1, stream)
+        moe.moe_quant_dispatch(d, dev["x"], dev["expert_idx"], expanded, a1, pts1, bounds[0], stream)
         evs[2].record(stream)
-        moe.moe_gmm1(d, a1, cs, dev["w1"], dev["s1"], c1, gws, stream)
+        moe.moe_gmm1(d, a1, cs, bounds[0], dev["w1"], dev["s1"], c1, gws, stream)
         evs[3].record(stream)
-        moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, None, q2, pts2, stream)
+        moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, dev["expert_idx"], None, q2, pts2, bounds[1], stream)
         evs[4].record(stream)
-        moe.moe_gmm2(d, q2, cs, dev["w2"], dev["s2"], c2, gws, stream)
+        moe.moe_gmm2(d, q2, cs, bounds[1], dev["w2"], dev["s2"], c2, gws, stream)
         evs[5].record(stream)
         moe.moe_combine_unpermute(d, c2, pts2, expanded, dev["probs"], out, stream)
         evs[6].record(stream)

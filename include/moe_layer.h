@@ -186,15 +186,36 @@ int32_t moe_route_sort_noalloc(const moe_dims_t* d, const int32_t* expert_idx, i
                                void* stream);
 
 /*
+ * Activation bounds.  The grouped GEMMs accumulate exact integers in fp32 in
+ * chunks whose every partial sum stays within 2^24.  Without further knowledge
+ * a chunk is 1024 deep (1024 * 128 * 128 = 2^24).  A bounds array
+ *   int32_t bounds[E][MOE_BOUND_SEGMENTS]
+ * holds, for expert e and the s-th MOE_BOUND_SEGMENT-deep segment of the
+ * reduction dimension (k in [1024 s, 1024 s + 1024)), an upper bound of
+ *   sum over k in the segment of |a[row][k]|      for every row of expert e,
+ * so a chunk of consecutive segments S is exact when 128 * sum_{s in S} bound[e][s]
+ * <= 2^24 (|w| <= 128); the GEMMs then use the longest such uniform chunk per
+ * expert.  moe_quant_dispatch and moe_swiglu_quant produce exact maxima when
+ * given a zero-filled array (atomic max); a bound that is too small makes the
+ * GEMM results inexact.  Passing NULL everywhere keeps the 1024-deep chunks.
+ */
+#define MOE_BOUND_SEGMENT 1024
+#define MOE_BOUND_SEGMENTS 16
+
+/*
  * FrontReorder phase 2c with the quant-scatter (page section "1. FrontReorder"):
  * quantise every token once (as moe_quant_tokens) and write its codes, as
  * binary16 integers, to each of its expanded rows:
  *   a1_f16[expanded_row_idx[t*topK + j]][k] = q[t][k]   for every valid route j
  * giving the expert-major GMM1 operand (rows of invalid routes are not written).
- *   expanded_row_idx [R] from moe_route_sort; a1_f16 [R][K]; pts1 [M]
+ *   expert_idx [M][topK] (read only when a1_bounds is given); expanded_row_idx [R]
+ *   from moe_route_sort; a1_f16 [R][K]; pts1 [M];
+ *   a1_bounds: NULL, or a zero-filled int32 [E][MOE_BOUND_SEGMENTS] that receives
+ *   the per-expert segment maxima of sum |code| (see "Activation bounds").
  */
-int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t* expanded_row_idx,
-                           uint16_t* a1_f16, float* pts1, void* stream);
+int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx,
+                           const int32_t* expanded_row_idx, uint16_t* a1_f16, float* pts1, int32_t* a1_bounds,
+                           void* stream);
 
 /* Workspace bytes of moe_gmm1 / moe_gmm2 (status word). */
 size_t moe_gmm_workspace_size(const moe_dims_t* d);
@@ -205,30 +226,36 @@ size_t moe_gmm_workspace_size(const moe_dims_t* d);
  *   acc[n]   = sum_k a1[d][k] * w1[e][n][k]                (exact integer)
  *   c1[d][n] = binary16(float(acc[n]) * s1[e][n])          n < 2I
  *   a1_f16 [R][K] expert-major binary16-coded int8 codes (moe_quant_dispatch);
+ *   a1_bounds: NULL or the activation bounds of a1_f16 (see "Activation bounds");
  *   c1 [R][2I] (rows >= cumsum[E-1] untouched)
  */
-int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int8_t* w1,
-                 const float* s1, uint16_t* c1, void* workspace, size_t workspace_bytes, void* stream);
+int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int32_t* a1_bounds,
+                 const int8_t* w1, const float* s1, uint16_t* c1, void* workspace, size_t workspace_bytes,
+                 void* stream);
 
 /*
  * SwiGLU + dynamic requant (page section "4. SwiGLU"), per valid expanded row d
  * with token t = sorted_src_route[d] / topK:
  *   h = float(c1[d]) * pts1[t];  y_j = silu(h_j) * h_{j+I},  silu(v) = v / (1 + exp(-v))
  *   pts2[d] = max_j |y_j| / 127;  q_j = round-half-even(y_j * (127 / max|y|)), clamped
- *   q2_i8 [R][I] int8 (may be NULL); q2_f16 [R][I] binary16-coded (may be NULL); pts2 [R]
+ *   q2_i8 [R][I] int8 (may be NULL); q2_f16 [R][I] binary16-coded (may be NULL); pts2 [R];
+ *   q2_bounds: NULL, or a zero-filled int32 [E][MOE_BOUND_SEGMENTS] that receives the
+ *   per-expert segment maxima of sum |q| (see "Activation bounds"); expert_idx
+ *   [M][topK] is read only then (the expert of row d is expert_idx[sorted_src_route[d]])
  */
 int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* pts1,
-                         const int32_t* sorted_src_route, const int32_t* cumsum, int8_t* q2_i8,
-                         uint16_t* q2_f16, float* pts2, void* stream);
+                         const int32_t* sorted_src_route, const int32_t* cumsum, const int32_t* expert_idx,
+                         int8_t* q2_i8, uint16_t* q2_f16, float* pts2, int32_t* q2_bounds, void* stream);
 
 /*
  * GMM2 (page section "5. GMM2"): for each valid expanded row d of expert e,
  *   c2[d][k] = binary16(float(sum_i q2[d,i] * w2[e][k][i]) * s2[e][k])
- *   q2_f16 [R][I] binary16-coded int8 codes; c2 [R][K]
+ *   q2_f16 [R][I] binary16-coded int8 codes; q2_bounds: NULL or their activation
+ *   bounds (see "Activation bounds"); c2 [R][K]
  */
-int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cumsum,
-                 const int8_t* w2, const float* s2, uint16_t* c2, void* workspace,
-                 size_t workspace_bytes, void* stream);
+int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cumsum, const int32_t* q2_bounds,
+                 const int8_t* w2, const float* s2, uint16_t* c2, void* workspace, size_t workspace_bytes,
+                 void* stream);
 
 /*
  * Combine + Unpermute (page sections "6. Combine" and "7. Unpermute"), fused:

@@ -70,10 +70,10 @@ def load_library(path=None):
         "moe_route_sort": ([D] + [vp] * 6 + [sz, vp], i32),
         "moe_quant_tokens": ([D] + [vp] * 5, i32),
         "moe_gmm_workspace_size": ([D], sz),
-        "moe_quant_dispatch": ([D] + [vp] * 5, i32),
-        "moe_gmm1": ([D] + [vp] * 6 + [sz, vp], i32),
-        "moe_swiglu_quant": ([D] + [vp] * 8, i32),
-        "moe_gmm2": ([D] + [vp] * 6 + [sz, vp], i32),
+        "moe_quant_dispatch": ([D] + [vp] * 7, i32),
+        "moe_gmm1": ([D] + [vp] * 7 + [sz, vp], i32),
+        "moe_swiglu_quant": ([D] + [vp] * 10, i32),
+        "moe_gmm2": ([D] + [vp] * 7 + [sz, vp], i32),
         "moe_combine_unpermute": ([D] + [vp] * 6, i32),
         "moe_route_sort_noalloc": ([D] + [vp] * 6, i32),
         "moe_selftest_wait_timeout": ([vp, ctypes.c_uint32, vp], i32),
@@ -164,26 +164,28 @@ def moe_quant_tokens(d, x, xq_i8, xq_f16, pts1, stream=None):
         ctypes.byref(d), _p(x), _p(xq_i8), _p(xq_f16), _p(pts1), _stream(stream)))
 
 
-def moe_quant_dispatch(d, x, expanded_row_idx, a1_f16, pts1, stream=None):
+def moe_quant_dispatch(d, x, expert_idx, expanded_row_idx, a1_f16, pts1, a1_bounds, stream=None):
     _check("moe_quant_dispatch", load_library().moe_quant_dispatch(
-        ctypes.byref(d), _p(x), _p(expanded_row_idx), _p(a1_f16), _p(pts1), _stream(stream)))
+        ctypes.byref(d), _p(x), _p(expert_idx), _p(expanded_row_idx), _p(a1_f16), _p(pts1), _p(a1_bounds),
+        _stream(stream)))
 
 
-def moe_gmm1(d, a1_f16, cumsum, w1, s1, c1, workspace, stream=None):
+def moe_gmm1(d, a1_f16, cumsum, a1_bounds, w1, s1, c1, workspace, stream=None):
     _check("moe_gmm1", load_library().moe_gmm1(
-        ctypes.byref(d), _p(a1_f16), _p(cumsum), _p(w1), _p(s1), _p(c1), _p(workspace),
+        ctypes.byref(d), _p(a1_f16), _p(cumsum), _p(a1_bounds), _p(w1), _p(s1), _p(c1), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def moe_swiglu_quant(d, c1, pts1, sorted_src_route, cumsum, q2_i8, q2_f16, pts2, stream=None):
+def moe_swiglu_quant(d, c1, pts1, sorted_src_route, cumsum, expert_idx, q2_i8, q2_f16, pts2, q2_bounds,
+                     stream=None):
     _check("moe_swiglu_quant", load_library().moe_swiglu_quant(
-        ctypes.byref(d), _p(c1), _p(pts1), _p(sorted_src_route), _p(cumsum), _p(q2_i8), _p(q2_f16),
-        _p(pts2), _stream(stream)))
+        ctypes.byref(d), _p(c1), _p(pts1), _p(sorted_src_route), _p(cumsum), _p(expert_idx), _p(q2_i8),
+        _p(q2_f16), _p(pts2), _p(q2_bounds), _stream(stream)))
 
 
-def moe_gmm2(d, q2_f16, cumsum, w2, s2, c2, workspace, stream=None):
+def moe_gmm2(d, q2_f16, cumsum, q2_bounds, w2, s2, c2, workspace, stream=None):
     _check("moe_gmm2", load_library().moe_gmm2(
-        ctypes.byref(d), _p(q2_f16), _p(cumsum), _p(w2), _p(s2), _p(c2), _p(workspace),
+        ctypes.byref(d), _p(q2_f16), _p(cumsum), _p(q2_bounds), _p(w2), _p(s2), _p(c2), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -201,6 +203,11 @@ def moe_selftest_wait_timeout(status, limit_us, stream=None):
 
 # Largest route count (M * topK) moe_route_sort_noalloc accepts (its fixed scratch).
 ROUTE_SORT_NOALLOC_MAX_ROUTES = 524288
+
+# Activation bounds arrays: int32 [E][BOUND_SEGMENTS], one entry per BOUND_SEGMENT-deep
+# segment of the reduction dimension (include/moe_layer.h, "Activation bounds").
+BOUND_SEGMENT = 1024
+BOUND_SEGMENTS = 16
 
 
 def moe_route_sort_noalloc(d, expert_idx, sorted_src_route, expanded_row_idx, tokens_per_expert,

@@ -30,6 +30,15 @@ constexpr int kRowThreads = 256;
 __device__ __forceinline__ int rint_small(float v) {
   return __float_as_int(__fadd_rn(v, 12582912.0f)) - 0x4B400000;
 }
+// Adds a vector's sum of |code| to its 1024-deep segment's shared total.  The
+// active lanes of a warp hold consecutive vectors starting at a multiple of 32,
+// which never straddle a segment (128 vectors), so one atomic per warp suffices.
+__device__ __forceinline__ void add_segment_l1(int* s_l1, int idx, int l1) {
+  const unsigned mask = __activemask();
+  const int sum = __reduce_add_sync(mask, l1);
+  if ((int)(threadIdx.x & 31) == __ffs(mask) - 1) atomicAdd(&s_l1[(idx * 8) / kBoundSegment], sum);
+}
+
 __device__ __forceinline__ uint32_t codes_to_half2(int q0, int q1) {
   const uint32_t w = (uint32_t)(0x6400 + q0 + 128) | ((uint32_t)(0x6400 + q1 + 128) << 16);
   uint32_t r;
@@ -43,14 +52,20 @@ __device__ __forceinline__ uint32_t codes_to_half2(int q0, int q1) {
 // With `expanded_row_idx` set, the codes of token t are also written (as binary16)
 // to row expanded_row_idx[t*topK + j] of `a1` for every valid route j: the
 // expert-major GMM1 operand (FrontReorder's quant-scatter into offsetA).
+// With `bounds` set, the token's sum of |code| over each 1024-deep segment of k is
+// folded (atomic max) into bounds[e][segment] of every expert e it is routed to.
 template <int VPT>
 __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half* __restrict__ x, int K,
                                                                    int8_t* __restrict__ xq_i8,
                                                                    __half* __restrict__ xq_f16,
                                                                    float* __restrict__ pts1,
                                                                    const int32_t* __restrict__ expanded_row_idx,
-                                                                   int topK, __half* __restrict__ a1) {
+                                                                   int topK, __half* __restrict__ a1,
+                                                                   const int32_t* __restrict__ expert_idx, int E,
+                                                                   int32_t* __restrict__ bounds) {
   __shared__ float red[kRowThreads / 32];
+  __shared__ int s_l1[kBoundSegments];
+  if (threadIdx.x < kBoundSegments) s_l1[threadIdx.x] = 0;  // visible after the row-max barriers
   const int t = blockIdx.x;
   const int nvec = K >> 3;
   const int4* row = reinterpret_cast<const int4*>(x + (size_t)t * K);
@@ -76,6 +91,12 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         q[j] = (amax > 0.0f) ? clamp127(rint_small(roundf(__fdiv_rn(__half2float(v[i].h[j]), scale)))) : 0;
+      if (bounds) {
+        int l1 = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) l1 += abs(q[j]);
+        add_segment_l1(s_l1, idx, l1);
+      }
       if (xq_i8) {
         uint2 packed;
         packed.x = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
@@ -100,20 +121,36 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
       }
     }
   }
+  if (bounds) {
+    __syncthreads();
+    const int nseg = (K + kBoundSegment - 1) / kBoundSegment;
+    if (threadIdx.x < nseg) {
+      for (int s = 0; s < topK; ++s) {
+        const int e = __ldg(expert_idx + (size_t)t * topK + s);
+        if (e >= 0 && e < E) atomicMax(bounds + (size_t)e * kBoundSegments + threadIdx.x, s_l1[threadIdx.x]);
+      }
+    }
+  }
 }
 
 // --------------------------------------------------------------------------
 // SwiGLU + requant over expanded rows d < cumsum[E-1]
 // --------------------------------------------------------------------------
+// With `bounds` set, the row's sum of |code| over each 1024-deep segment of I is
+// folded (atomic max) into bounds[e][segment] of the row's expert e.
 template <int VPT>
 __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
     const __half* __restrict__ c1, int I, int E, int topK, const float* __restrict__ pts1,
     const int32_t* __restrict__ sorted_src_route, const int32_t* __restrict__ cumsum,
-    int8_t* __restrict__ q2_i8, __half* __restrict__ q2_f16, float* __restrict__ pts2) {
+    int8_t* __restrict__ q2_i8, __half* __restrict__ q2_f16, float* __restrict__ pts2,
+    const int32_t* __restrict__ expert_idx, int32_t* __restrict__ bounds) {
   __shared__ float red[kRowThreads / 32];
+  __shared__ int s_l1[kBoundSegments];
   const int d = blockIdx.x;
   if (d >= __ldg(cumsum + E - 1)) return;
-  const float p1 = __ldg(pts1 + __ldg(sorted_src_route + d) / topK);
+  if (threadIdx.x < kBoundSegments) s_l1[threadIdx.x] = 0;  // visible after the row-max barriers
+  const int src = __ldg(sorted_src_route + d);
+  const float p1 = __ldg(pts1 + src / topK);
   const int nvec = I >> 3;
   const int4* gate = reinterpret_cast<const int4*>(c1 + (size_t)d * 2 * I);
   const int4* up = gate + nvec;
@@ -150,6 +187,12 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
       int q[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) q[j] = nz ? clamp127(rint_small(__fmul_rn(y[i][j], inv))) : 0;
+      if (bounds) {
+        int l1 = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) l1 += abs(q[j]);
+        add_segment_l1(s_l1, idx, l1);
+      }
       if (q2_i8) {
         uint2 packed;
         packed.x = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
@@ -167,6 +210,13 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
         reinterpret_cast<int4*>(q2_f16 + (size_t)d * I)[idx] = o;
       }
     }
+  }
+  if (bounds) {
+    __syncthreads();
+    const int nseg = (I + kBoundSegment - 1) / kBoundSegment;
+    const int e = __ldg(expert_idx + src);
+    if (threadIdx.x < nseg && e >= 0 && e < E)
+      atomicMax(bounds + (size_t)e * kBoundSegments + threadIdx.x, s_l1[threadIdx.x]);
   }
 }
 
@@ -215,7 +265,8 @@ int row_threads(int nvec, int vpt) {
 }  // namespace
 
 cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16, float* pts1,
-                                const int32_t* expanded_row_idx, int topK, uint16_t* a1, cudaStream_t stream) {
+                                const int32_t* expanded_row_idx, int topK, uint16_t* a1, const int32_t* expert_idx,
+                                int E, int32_t* bounds, cudaStream_t stream) {
   const int nvec = K / 8;
   const int vpt = (nvec + kRowThreads - 1) / kRowThreads;
   const int threads = row_threads(nvec, vpt);
@@ -223,13 +274,17 @@ cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, 
   __half* qf = reinterpret_cast<__half*>(xq_f16);
   __half* ah = reinterpret_cast<__half*>(a1);
   if (vpt <= 1)
-    quant_tokens_kernel<1><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
+    quant_tokens_kernel<1><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,
+                                                        expert_idx, E, bounds);
   else if (vpt <= 2)
-    quant_tokens_kernel<2><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
+    quant_tokens_kernel<2><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,
+                                                        expert_idx, E, bounds);
   else if (vpt <= 4)
-    quant_tokens_kernel<4><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
+    quant_tokens_kernel<4><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,
+                                                        expert_idx, E, bounds);
   else if (vpt <= 8)
-    quant_tokens_kernel<8><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah);
+    quant_tokens_kernel<8><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,
+                                                        expert_idx, E, bounds);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -237,7 +292,8 @@ cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, 
 
 cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int topK, const float* pts1,
                                 const int32_t* sorted_src_route, const int32_t* cumsum, int8_t* q2_i8,
-                                uint16_t* q2_f16, float* pts2, cudaStream_t stream) {
+                                uint16_t* q2_f16, float* pts2, const int32_t* expert_idx, int32_t* bounds,
+                                cudaStream_t stream) {
   const int nvec = I / 8;
   const int vpt = (nvec + kRowThreads - 1) / kRowThreads;
   const int threads = row_threads(nvec, vpt);
@@ -245,13 +301,13 @@ cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int top
   __half* qf = reinterpret_cast<__half*>(q2_f16);
   if (vpt <= 1)
     swiglu_quant_kernel<1><<<R, threads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
-                                                          qf, pts2);
+                                                          qf, pts2, expert_idx, bounds);
   else if (vpt <= 2)
     swiglu_quant_kernel<2><<<R, threads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
-                                                          qf, pts2);
+                                                          qf, pts2, expert_idx, bounds);
   else if (vpt <= 4)
     swiglu_quant_kernel<4><<<R, threads, 0, stream>>>(ch, I, E, topK, pts1, sorted_src_route, cumsum, q2_i8,
-                                                          qf, pts2);
+                                                          qf, pts2, expert_idx, bounds);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

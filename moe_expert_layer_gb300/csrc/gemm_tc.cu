@@ -85,7 +85,6 @@ constexpr int kPairCh = 256;        // weight channels per pair (MMA M)
 constexpr int kBK = 128;            // reduction depth per stage
 constexpr int kTileRows = 256;      // token rows per work item (MMA N <= 256)
 constexpr int kHalfRows = kTileRows / 2;  // token rows per CTA (TMA box height)
-constexpr int kChunkStages = 8;     // 1024-deep exact chunks
 constexpr int kTmemCols = 512;      // accumulator [0, 256), A buffers 256 + 64*slot
 constexpr int kACol0 = 256;
 constexpr int kMaxExperts = 1024;
@@ -110,6 +109,7 @@ struct Args {
   int32_t* status;
   int E, N, Kd;
   int split_rows;  // this engine serves the experts with more than split_rows rows
+  const int32_t* bounds;  // [E][kBoundSegments] activation bounds, or null (1024-deep chunks)
 #ifdef MOE_GEMM_PROFILE
   unsigned long long* prof;
 #endif
@@ -264,6 +264,27 @@ struct Item {
   int e, cb, row0, rows, n_mma;
 };
 
+// Stages per exact chunk for expert e.  Without bounds 8 (1024 deep: every partial
+// sum within 1024 * 128 * 128 = 2^24).  With bounds, the longest run of L whole
+// 1024-deep segments such that every aligned run's bound sum B satisfies
+// 128 * B <= 2^24, which keeps every partial sum of every row of the expert exact.
+__device__ __forceinline__ int chunk_stages(const int32_t* bounds, int e, int nk) {
+  constexpr int kStagesPerSegment = kBoundSegment / kBK;
+  if (!bounds) return kStagesPerSegment;
+  const int32_t* b = bounds + (size_t)e * kBoundSegments;
+  const int nseg = (nk + kStagesPerSegment - 1) / kStagesPerSegment;
+  for (int L = nseg; L > 1; --L) {
+    bool ok = true;
+    for (int s0 = 0; s0 < nseg && ok; s0 += L) {
+      long long sum = 0;
+      for (int s = s0; s < min(nseg, s0 + L); ++s) sum += __ldg(b + s);
+      ok = sum * 128 <= (1ll << 24);
+    }
+    if (ok) return L * kStagesPerSegment;
+  }
+  return kStagesPerSegment;
+}
+
 // Work items of an expert with `cnt` rows on the pairs: its row tiles x channel
 // blocks, or none when it has at most split_rows rows (the warp-MMA engine takes
 // it).  Experts without items leave the prefix flat, and the binary search in
@@ -340,6 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t accfull_bar, accempty_bar, final_bar;
   __shared__ int s_pref[kMaxExperts + 1];
   __shared__ int s_end[kMaxExperts];
+  __shared__ short s_chunk[kMaxExperts];  // stages per exact chunk of each expert
   __shared__ int s_wsum[kThreads / 32];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_w_issued, s_x_issued;
@@ -361,6 +383,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int e = e0; e < e1; ++e) {
       const int hi = __ldg(args.cumsum + e), lo = e ? __ldg(args.cumsum + e - 1) : 0;
       s_end[e] = hi;
+      s_chunk[e] = (short)chunk_stages(args.bounds, e, nk);
       local += own_items(hi - lo, args.split_rows, n_cb);
     }
     int incl = local;
@@ -489,11 +512,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = pair; j < total && ok; j += npairs) {
           const Item it = decode_item(j, s_pref, s_end, E);
           const uint32_t idesc = kIdescBase | ((uint32_t)(it.n_mma >> 3) << 17);
+          const int cs = s_chunk[it.e];
+          int kc = 0;  // stage index within the current exact chunk
           for (int kb = 0; kb < nk && ok; ++kb, ++n) {
             PROF_T0(t_body);
             const int slot = n % S;
             const uint32_t ph = (n / S) & 1;
-            if (kb % kChunkStages == 0) {
+            if (kc == 0) {
               // a new exact chunk: both CTAs' drains must have read the accumulator
               ok = PROF_WAIT(0, wait_or_abort(&accempty_bar, (c & 1) ^ 1, abort_flag, args.status));
               if (!ok) break;
@@ -508,15 +533,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int s = 0; s < 8; ++s) {
               // 16-k step s: A columns 8s.., token tile s/4
               const uint64_t bdesc = sw128_desc(xs + (s >> 2) * kXHalfBytes + (s & 3) * 32);
-              mma_pair(tmem, a_tmem + s * 8, bdesc, idesc, (kb % kChunkStages != 0 || s != 0) ? 1u : 0u);
+              mma_pair(tmem, a_tmem + s * 8, bdesc, idesc, (kc != 0 || s != 0) ? 1u : 0u);
             }
             PROF_ADD(2, t_issue);
             PROF_T0(t_commit);
             mma_commit_pair(&sdone_bar[slot]);  // token slot and A buffer free once these MMAs complete
             PROF_ADD(3, t_commit);
-            if (kb % kChunkStages == kChunkStages - 1 || kb == nk - 1) {
+            if (++kc == cs || kb == nk - 1) {
               mma_commit_pair(&accfull_bar);    // chunk accumulated: hand it to the drains
               ++c;
+              kc = 0;
             }
             PROF_ADD(4, t_body);
           }
@@ -587,12 +613,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;  // output channel within this CTA's 128
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + cg * 64;
     const uint32_t accempty_remote = cluster_addr(&accempty_bar, 0);
-    const int nch = (nk + kChunkStages - 1) / kChunkStages;
     int c = 0;
     bool ok = true;
     for (int j = pair; j < total && ok; j += npairs) {
       const Item it = decode_item(j, s_pref, s_end, E);
       const bool active = cg * 64 < it.n_mma;
+      const int cs = s_chunk[it.e];
+      const int nch = (nk + cs - 1) / cs;
       int acci[64];
 #pragma unroll
       for (int t = 0; t < 64; ++t) acci[t] = 0;
@@ -686,6 +713,7 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
   a.N = p.N;
   a.Kd = p.Kd;
   a.split_rows = p.split_rows;
+  a.bounds = p.bounds;
 #ifdef MOE_GEMM_PROFILE
   a.prof = g_gemm_prof;
   if (!a.prof) return cudaErrorInvalidValue;

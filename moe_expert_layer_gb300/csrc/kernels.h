@@ -13,12 +13,16 @@ cudaError_t launch_route_sort(const int32_t* expert_idx, int R, int E, int32_t* 
                               void* workspace, cudaStream_t stream);
 
 // elementwise.cu
+// Activation bounds (include/moe_layer.h): per expert, per 1024-deep segment
+constexpr int kBoundSegment = 1024;
+constexpr int kBoundSegments = 16;
 cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16,
                                 float* pts1, const int32_t* expanded_row_idx, int topK, uint16_t* a1,
-                                cudaStream_t stream);
+                                const int32_t* expert_idx, int E, int32_t* bounds, cudaStream_t stream);
 cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int topK, const float* pts1,
                                 const int32_t* sorted_src_route, const int32_t* cumsum, int8_t* q2_i8,
-                                uint16_t* q2_f16, float* pts2, cudaStream_t stream);
+                                uint16_t* q2_f16, float* pts2, const int32_t* expert_idx, int32_t* bounds,
+                                cudaStream_t stream);
 cudaError_t launch_combine_unpermute(const uint16_t* c2, const float* pts2, const int32_t* expanded_row_idx,
                                      const float* probs, int M, int K, int topK, uint16_t* out,
                                      cudaStream_t stream);
@@ -35,6 +39,7 @@ struct GroupedGemmProblem {
   int32_t* status;                  // device status word
   int split_rows;                   // experts with <= split_rows rows run on the warp-MMA engine,
                                     // the others on the tcgen05 pairs (set by launch_grouped_gemm)
+  const int32_t* bounds;            // [E][kBoundSegments] activation bounds, or null
 };
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream);     // picks an engine
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream);  // gemm_hmma.cu

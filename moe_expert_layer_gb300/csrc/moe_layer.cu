@@ -46,7 +46,7 @@ int32_t launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ER
 
 // Layout of the layer workspace.
 struct Layout {
-  size_t status, sorted, expanded, tpe, cumsum, sort_ws, a1, pts1, c1, q2, pts2, c2, total;
+  size_t status, bounds1, bounds2, sorted, expanded, tpe, cumsum, sort_ws, a1, pts1, c1, q2, pts2, c2, total;
   // host-variant staging
   size_t hx, hei, hprobs, hout, host_total;
 };
@@ -60,7 +60,11 @@ Layout layout_of(const moe_dims_t* d) {
     off = align_up(off + bytes);
     return at;
   };
-  L.status = take(sizeof(int32_t));
+  // status word and both bounds arrays are contiguous: one memset clears them
+  L.status = 0;
+  L.bounds1 = 16;
+  L.bounds2 = L.bounds1 + E * moe::kBoundSegments * 4;
+  take(L.bounds2 + E * moe::kBoundSegments * 4);
   L.sorted = take(R * 4);
   L.expanded = take(R * 4);
   L.tpe = take(E * 4);
@@ -102,13 +106,17 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   float* pts2 = at<float>(ws, L.pts2);
   uint16_t* c2 = at<uint16_t>(ws, L.c2);
 
+  int32_t* bounds1 = at<int32_t>(ws, L.bounds1);
+  int32_t* bounds2 = at<int32_t>(ws, L.bounds2);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(status, 0, sizeof(int32_t), st)) != cudaSuccess) return launch_status(e);
+  if ((e = cudaMemsetAsync(status, 0, L.bounds2 + (size_t)E * moe::kBoundSegments * 4, st)) != cudaSuccess)
+    return launch_status(e);
   if ((e = moe::launch_route_sort(expert_idx, R, E, sorted, expanded, tpe, cumsum, at<void>(ws, L.sort_ws), st)) !=
       cudaSuccess)
     return launch_status(e);
   // quantise each token once and scatter its codes to its expert-major rows
-  if ((e = moe::launch_quant_tokens(x, M, K, nullptr, nullptr, pts1, expanded, topK, a1, st)) != cudaSuccess)
+  if ((e = moe::launch_quant_tokens(x, M, K, nullptr, nullptr, pts1, expanded, topK, a1, expert_idx, E, bounds1,
+                                    st)) != cudaSuccess)
     return launch_status(e);
 
   moe::GroupedGemmProblem g1{};
@@ -122,9 +130,11 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   g1.N = 2 * I;
   g1.Kd = K;
   g1.status = status;
+  g1.bounds = bounds1;
   if ((e = moe::launch_grouped_gemm(g1, st)) != cudaSuccess) return launch_status(e);
 
-  if ((e = moe::launch_swiglu_quant(c1, R, I, E, topK, pts1, sorted, cumsum, nullptr, q2, pts2, st)) != cudaSuccess)
+  if ((e = moe::launch_swiglu_quant(c1, R, I, E, topK, pts1, sorted, cumsum, nullptr, q2, pts2, expert_idx, bounds2,
+                                    st)) != cudaSuccess)
     return launch_status(e);
 
   moe::GroupedGemmProblem g2{};
@@ -138,6 +148,7 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   g2.N = K;
   g2.Kd = I;
   g2.status = status;
+  g2.bounds = bounds2;
   if ((e = moe::launch_grouped_gemm(g2, st)) != cudaSuccess) return launch_status(e);
 
   e = moe::launch_combine_unpermute(c2, pts2, expanded, probs, M, K, topK, out, st);
@@ -260,19 +271,21 @@ int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, int8_t* xq_i8, 
   if (!x || !pts1 || (!xq_i8 && !xq_f16)) return MOE_ERR_NULL;
   if (!aligned16(x) || (xq_i8 && !aligned16(xq_i8)) || (xq_f16 && !aligned16(xq_f16))) return MOE_ERR_ALIGN;
   if ((rc = check_device()) != MOE_OK) return rc;
-  return launch_status(moe::launch_quant_tokens(x, d->M, d->K, xq_i8, xq_f16, pts1, nullptr, 0, nullptr,
-                                                static_cast<cudaStream_t>(stream)));
+  return launch_status(moe::launch_quant_tokens(x, d->M, d->K, xq_i8, xq_f16, pts1, nullptr, 0, nullptr, nullptr,
+                                                d->E, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
-int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t* expanded_row_idx, uint16_t* a1_f16,
-                           float* pts1, void* stream) {
+int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx,
+                           const int32_t* expanded_row_idx, uint16_t* a1_f16, float* pts1, int32_t* a1_bounds,
+                           void* stream) {
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
-  if (!x || !expanded_row_idx || !a1_f16 || !pts1) return MOE_ERR_NULL;
+  if (!x || !expanded_row_idx || !a1_f16 || !pts1 || (a1_bounds && !expert_idx)) return MOE_ERR_NULL;
   if (!aligned16(x) || !aligned16(a1_f16)) return MOE_ERR_ALIGN;
   if ((rc = check_device()) != MOE_OK) return rc;
   return launch_status(moe::launch_quant_tokens(x, d->M, d->K, nullptr, nullptr, pts1, expanded_row_idx, d->topK,
-                                                a1_f16, static_cast<cudaStream_t>(stream)));
+                                                a1_f16, expert_idx, d->E, a1_bounds,
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_gmm_workspace_size(const moe_dims_t* d) {
@@ -280,8 +293,9 @@ size_t moe_gmm_workspace_size(const moe_dims_t* d) {
   return kAlign;
 }
 
-int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int8_t* w1, const float* s1,
-                 uint16_t* c1, void* workspace, size_t workspace_bytes, void* stream) {
+int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int32_t* a1_bounds,
+                 const int8_t* w1, const float* s1, uint16_t* c1, void* workspace, size_t workspace_bytes,
+                 void* stream) {
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!a1_f16 || !cumsum || !w1 || !s1 || !c1 || !workspace) return MOE_ERR_NULL;
@@ -299,24 +313,29 @@ int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cum
   g.N = 2 * d->I;
   g.Kd = d->K;
   g.status = static_cast<int32_t*>(workspace);
+  g.bounds = a1_bounds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
   return launch_status(moe::launch_grouped_gemm(g, st));
 }
 
 int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* pts1, const int32_t* sorted_src_route,
-                         const int32_t* cumsum, int8_t* q2_i8, uint16_t* q2_f16, float* pts2, void* stream) {
+                         const int32_t* cumsum, const int32_t* expert_idx, int8_t* q2_i8, uint16_t* q2_f16,
+                         float* pts2, int32_t* q2_bounds, void* stream) {
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
-  if (!c1 || !pts1 || !sorted_src_route || !cumsum || !pts2 || (!q2_i8 && !q2_f16)) return MOE_ERR_NULL;
+  if (!c1 || !pts1 || !sorted_src_route || !cumsum || !pts2 || (!q2_i8 && !q2_f16) || (q2_bounds && !expert_idx))
+    return MOE_ERR_NULL;
   if (!aligned16(c1) || (q2_i8 && !aligned16(q2_i8)) || (q2_f16 && !aligned16(q2_f16))) return MOE_ERR_ALIGN;
   if ((rc = check_device()) != MOE_OK) return rc;
   return launch_status(moe::launch_swiglu_quant(c1, d->M * d->topK, d->I, d->E, d->topK, pts1, sorted_src_route,
-                                                cumsum, q2_i8, q2_f16, pts2, static_cast<cudaStream_t>(stream)));
+                                                cumsum, q2_i8, q2_f16, pts2, expert_idx, q2_bounds,
+                                                static_cast<cudaStream_t>(stream)));
 }
 
-int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cumsum, const int8_t* w2,
-                 const float* s2, uint16_t* c2, void* workspace, size_t workspace_bytes, void* stream) {
+int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cumsum, const int32_t* q2_bounds,
+                 const int8_t* w2, const float* s2, uint16_t* c2, void* workspace, size_t workspace_bytes,
+                 void* stream) {
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!q2_f16 || !cumsum || !w2 || !s2 || !c2 || !workspace) return MOE_ERR_NULL;
@@ -334,6 +353,7 @@ int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cum
   g.N = d->K;
   g.Kd = d->I;
   g.status = static_cast<int32_t*>(workspace);
+  g.bounds = q2_bounds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_LAUNCH;
   return launch_status(moe::launch_grouped_gemm(g, st));

@@ -132,7 +132,9 @@ def test_layer_full_size_sampled(cfg):
     R = w.R
     ref_rs = oracle.route_sort(inp["expert_idx"], w.E)
     wsb = host(ws)
-    off = 256
+    # the workspace starts with the status word and the two activation-bound arrays,
+    # then (256-byte aligned) the sorted route table
+    off = (16 + 2 * w.E * moe.BOUND_SEGMENTS * 4 + 255) // 256 * 256
     sorted_dev = wsb[off:off + 4 * R].view(np.int32)
     assert_bits_equal(sorted_dev, ref_rs["sorted_src_route"], "sorted_src_route")
     toks = _sample_tokens(w.M, 24, w.seed)

@@ -104,12 +104,49 @@ def test_quant_dispatch_bit_exact(cfg):
     d = _dims(w)
     a1 = torch.full((w.R, w.K), 7.0, dtype=torch.float16, device="cuda")
     pts = empty(w.M, torch.float32)
-    moe.moe_quant_dispatch(d, dev(x), dev(rs["expanded_row_idx"]), a1, pts)
+    moe.moe_quant_dispatch(d, dev(x), None, dev(rs["expanded_row_idx"]), a1, pts, None)
     torch.cuda.synchronize()
     got = host(a1)
     assert_bits_equal(got[:Rv], a1_ref, "a1")
     assert np.all(got[Rv:].astype(np.float32) == 7.0)  # rows past the valid ones untouched
     assert_bits_equal(host(pts), pts_ref, "pts1")
+
+
+def _bounds_ref(codes, cumsum, E):
+    """Per-expert, per-1024-deep-segment maxima of sum |code| over the expert's rows."""
+    S = moe.BOUND_SEGMENTS
+    b = np.zeros((E, S), np.int32)
+    l1 = np.abs(codes.astype(np.int64))
+    nseg = (codes.shape[1] + moe.BOUND_SEGMENT - 1) // moe.BOUND_SEGMENT
+    seg = np.stack([l1[:, s * moe.BOUND_SEGMENT:(s + 1) * moe.BOUND_SEGMENT].sum(1) for s in range(nseg)], 1)
+    lo = 0
+    for e in range(E):
+        hi = int(cumsum[e])
+        if hi > lo:
+            b[e, :nseg] = seg[lo:hi].max(0)
+        lo = hi
+    return b
+
+
+@pytest.mark.parametrize("cfg", ["decode", "prefill", "mid"])
+def test_quant_dispatch_bounds(cfg):
+    """The activation bounds the quant-scatter produces are the exact per-expert
+    segment maxima of sum |code| (invalid routes contribute nothing)."""
+    w = synth.CONFIGS[cfg]
+    x = synth.normal_f16(w.seed, 1, (w.M, w.K))
+    ei, _ = synth.routing(w.seed, w.M, w.E, w.topK, w.routing)
+    ei[1, 0] = -1
+    rs = oracle.route_sort(ei, w.E)
+    xq_ref, _ = oracle.quant_tokens(x)
+    Rv = w.R - rs["invalid"]
+    a1_ref = xq_ref[rs["sorted_src_route"][:Rv] // w.topK]
+    d = _dims(w)
+    a1 = empty((w.R, w.K), torch.float16)
+    pts = empty(w.M, torch.float32)
+    bounds = torch.zeros((w.E, moe.BOUND_SEGMENTS), dtype=torch.int32, device="cuda")
+    moe.moe_quant_dispatch(d, dev(x), dev(ei), dev(rs["expanded_row_idx"]), a1, pts, bounds)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(bounds), _bounds_ref(a1_ref, rs["cumsum"], w.E), "a1 bounds")
 
 
 # ------------------------------------------------------------------ GEMMs
@@ -141,21 +178,25 @@ GEMM_CASES = [
 ]
 
 
+@pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
 @pytest.mark.parametrize("w", GEMM_CASES, ids=[w.name for w in GEMM_CASES])
-def test_gmm1_bit_exact(w):
+def test_gmm1_bit_exact(w, bounded):
     inp, rs, xq, pts1 = _stage_inputs(w)
     Rv = w.R - rs["invalid"]
     _, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], inp["expert_idx"], inp["w1"], inp["s1"], Rv)
     d = _dims(w)
     c1 = torch.full((w.R, 2 * w.I), float("nan"), dtype=torch.float16, device="cuda")
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(_a1(xq, rs, w.topK, w.R)), dev(rs["cumsum"]), dev(inp["w1"]), dev(inp["s1"]), c1, ws)
+    a1 = _a1(xq, rs, w.topK, w.R)
+    bounds = dev(_bounds_ref(a1, rs["cumsum"], w.E)) if bounded else None
+    moe.moe_gmm1(d, dev(a1), dev(rs["cumsum"]), bounds, dev(inp["w1"]), dev(inp["s1"]), c1, ws)
     assert moe.moe_workspace_status(ws) == 0
     assert_bits_equal(host(c1)[:Rv], c1_ref, "c1")
 
 
+@pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
 @pytest.mark.parametrize("w", GEMM_CASES, ids=[w.name for w in GEMM_CASES])
-def test_gmm2_bit_exact(w):
+def test_gmm2_bit_exact(w, bounded):
     inp, rs, xq, pts1 = _stage_inputs(w)
     Rv = w.R - rs["invalid"]
     q2 = synth.int8_sym127(w.seed, 77, (Rv, w.I))
@@ -165,7 +206,8 @@ def test_gmm2_bit_exact(w):
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
     q2f = np.zeros((w.R, w.I), np.float16)
     q2f[:Rv] = q2
-    moe.moe_gmm2(d, dev(q2f), dev(rs["cumsum"]), dev(inp["w2"]), dev(inp["s2"]), c2, ws)
+    bounds = dev(_bounds_ref(q2f, rs["cumsum"], w.E)) if bounded else None
+    moe.moe_gmm2(d, dev(q2f), dev(rs["cumsum"]), bounds, dev(inp["w2"]), dev(inp["s2"]), c2, ws)
     assert moe.moe_workspace_status(ws) == 0
     assert_bits_equal(host(c2)[:Rv], c2_ref, "c2")
 
@@ -197,9 +239,41 @@ def test_gmm_accumulator_exact_beyond_fp32_mantissa(M, wv):
     d = moe.dims(M, K, I, E, 1)
     c1 = empty((M, 2 * I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(_a1(xq, rs, 1, M)), dev(rs["cumsum"]), dev(w1), dev(s1), c1, ws)
+    moe.moe_gmm1(d, dev(_a1(xq, rs, 1, M)), dev(rs["cumsum"]), None, dev(w1), dev(s1), c1, ws)
     got = host(c1).astype(np.float64)
     assert np.array_equal(got, acc_ref.astype(np.float64))
+
+
+@pytest.mark.parametrize("K", [4096, 7168])
+def test_gmm_bounds_at_the_limit(K):
+    """Chunks merged by the activation bounds, with partial sums reaching 2^24.
+    Every row has sum |code| = 131072 = 2^24 / 128 over the first 2048 k (so those
+    two segments form one chunk only when their bounds allow it) and small codes
+    after; weights are -128 where the codes are large, so the fp32 partial sums of
+    the merged chunk reach -2^24 exactly before the small terms are added."""
+    M, I, E = 40, 64, 1
+    rng = np.random.default_rng(K)
+    xq = rng.integers(-1, 2, (M, K)).astype(np.int8)
+    xq[:, :1024] = 64
+    xq[:, 1024:2048] = 64           # 2048 * 64 = 131072 in the first two segments
+    xq[:, 2048:] = 0                # nothing after: one merged chunk holds the whole sum
+    xq[:, 3000:3010] = rng.integers(-3, 4, (M, 10))
+    w1 = rng.integers(-2, 3, (E, 2 * I, K)).astype(np.int8)
+    w1[0, :, :2048] = -128
+    s1 = np.ones((E, 2 * I), np.float32) / 4096
+    ei = np.zeros((M, 1), np.int32)
+    rs = oracle.route_sort(ei, E)
+    acc_ref, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], ei, w1, s1, M, want_acc=True)
+    assert acc_ref.min() <= -(1 << 24) + 100
+    a1 = _a1(xq, rs, 1, M)
+    b = _bounds_ref(a1, rs["cumsum"], E)
+    assert b[0, :2].sum() * 128 <= (1 << 24) and b[0, :3].sum() * 128 > (1 << 24) - (1 << 17)
+    d = moe.dims(M, K, I, E, 1)
+    c1 = empty((M, 2 * I), torch.float16)
+    ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
+    moe.moe_gmm1(d, dev(a1), dev(rs["cumsum"]), dev(b), dev(w1), dev(s1), c1, ws)
+    assert moe.moe_workspace_status(ws) == 0
+    assert_bits_equal(host(c1), c1_ref, "c1")
 
 
 def test_gmm_empty_experts_and_single_rows():
@@ -212,7 +286,7 @@ def test_gmm_empty_experts_and_single_rows():
     d = _dims(w)
     c1 = empty((w.R, 2 * w.I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(_a1(xq, rs, 1, w.R)), dev(rs["cumsum"]), dev(inp["w1"]), dev(inp["s1"]), c1, ws)
+    moe.moe_gmm1(d, dev(_a1(xq, rs, 1, w.R)), dev(rs["cumsum"]), None, dev(inp["w1"]), dev(inp["s1"]), c1, ws)
     assert_bits_equal(host(c1), c1_ref, "c1")
 
 
@@ -233,11 +307,29 @@ def test_swiglu_quant(R, I, spread):
     q2_ref, pts2_ref = oracle.swiglu_quant(c1, pts1, sorted_src, topK)
     d = moe.dims(M, 128, I, 1, 1)
     q8, q16, p2 = empty((R, I), torch.int8), empty((R, I), torch.float16), empty(R, torch.float32)
-    moe.moe_swiglu_quant(d, dev(c1), dev(pts1), dev(sorted_src), dev(cumsum), q8, q16, p2)
+    moe.moe_swiglu_quant(d, dev(c1), dev(pts1), dev(sorted_src), dev(cumsum), None, q8, q16, p2, None)
     torch.cuda.synchronize()
     assert_q2_close(host(q8), q2_ref)
     assert np.array_equal(host(q16).astype(np.int8), host(q8))
     np.testing.assert_allclose(host(p2), pts2_ref, rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("R,I,E", [(300, 2048, 5), (2000, 1408, 16)])
+def test_swiglu_quant_bounds(R, I, E):
+    """The requant's activation bounds are the exact per-expert segment maxima of
+    sum |q2| of the codes it writes (row d belongs to expert expert_idx[src])."""
+    rng = np.random.default_rng(R * I)
+    c1 = (rng.standard_normal((R, 2 * I)) * 200).astype(np.float16)
+    pts1 = rng.uniform(0.02, 0.05, R).astype(np.float32)
+    ei = np.sort(rng.integers(0, E, R)).astype(np.int32).reshape(R, 1)   # expert-major rows, topK = 1
+    sorted_src = np.arange(R, dtype=np.int32)
+    cumsum = np.cumsum(np.bincount(ei.ravel(), minlength=E)).astype(np.int32)
+    d = moe.dims(R, 128, I, E, 1)
+    q8, q16, p2 = empty((R, I), torch.int8), empty((R, I), torch.float16), empty(R, torch.float32)
+    bounds = torch.zeros((E, moe.BOUND_SEGMENTS), dtype=torch.int32, device="cuda")
+    moe.moe_swiglu_quant(d, dev(c1), dev(pts1), dev(sorted_src), dev(cumsum), dev(ei), q8, q16, p2, bounds)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(bounds), _bounds_ref(host(q8), cumsum, E), "q2 bounds")
 
 
 # ------------------------------------------------------------------ Combine + Unpermute
