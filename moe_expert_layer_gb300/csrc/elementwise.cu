@@ -227,6 +227,46 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
 // --------------------------------------------------------------------------
 constexpr int kCombineThreads = 128;
 
+// The same for a compile-time topK (the common 1..8): every slot's loads are issued
+// before any is used (invalid routes load row 0 and are skipped), so a thread keeps
+// topK 16-byte row loads in flight instead of one.
+template <int TK>
+__global__ void __launch_bounds__(kCombineThreads) combine_unpermute_tk_kernel(
+    const __half* __restrict__ c2, const float* __restrict__ pts2, const int32_t* __restrict__ expanded_row_idx,
+    const float* __restrict__ probs, int K, __half* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int vec = blockIdx.y * kCombineThreads + threadIdx.x;
+  if (vec * 8 >= K) return;
+  int d[TK];
+  float p[TK], sc[TK];
+  Vec8h c[TK];
+#pragma unroll
+  for (int u = 0; u < TK; ++u) d[u] = __ldg(expanded_row_idx + (size_t)t * TK + u);
+#pragma unroll
+  for (int u = 0; u < TK; ++u) {
+    const int row = d[u] < 0 ? 0 : d[u];
+    p[u] = __ldg(probs + (size_t)t * TK + u);
+    sc[u] = __ldg(pts2 + row);
+    c[u].v = __ldg(reinterpret_cast<const int4*>(c2 + (size_t)row * K) + vec);
+  }
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+#pragma unroll
+  for (int u = 0; u < TK; ++u) {
+    if (d[u] < 0) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float dv = __half2float(f2h_sat(__fmul_rn(__half2float(c[u].h[j]), sc[u])));
+      acc[j] = __fadd_rn(acc[j], __fmul_rn(dv, p[u]));
+    }
+  }
+  Vec8h o;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) o.h[j] = f2h_sat(acc[j]);
+  reinterpret_cast<int4*>(out + (size_t)t * K)[vec] = o.v;
+}
+
 __global__ void __launch_bounds__(kCombineThreads) combine_unpermute_kernel(
     const __half* __restrict__ c2, const float* __restrict__ pts2, const int32_t* __restrict__ expanded_row_idx,
     const float* __restrict__ probs, int K, int topK, __half* __restrict__ out) {
@@ -317,8 +357,26 @@ cudaError_t launch_combine_unpermute(const uint16_t* c2, const float* pts2, cons
                                      const float* probs, int M, int K, int topK, uint16_t* out,
                                      cudaStream_t stream) {
   dim3 grid(M, (K / 8 + kCombineThreads - 1) / kCombineThreads);
-  combine_unpermute_kernel<<<grid, kCombineThreads, 0, stream>>>(
-      reinterpret_cast<const __half*>(c2), pts2, expanded_row_idx, probs, K, topK, reinterpret_cast<__half*>(out));
+  const __half* ch = reinterpret_cast<const __half*>(c2);
+  __half* oh = reinterpret_cast<__half*>(out);
+  switch (topK) {
+#define MOE_COMBINE_TK(TK)                                                                                   \
+  case TK:                                                                                                   \
+    combine_unpermute_tk_kernel<TK><<<grid, kCombineThreads, 0, stream>>>(ch, pts2, expanded_row_idx, probs, K, \
+                                                                          oh);                               \
+    break;
+    MOE_COMBINE_TK(1)
+    MOE_COMBINE_TK(2)
+    MOE_COMBINE_TK(3)
+    MOE_COMBINE_TK(4)
+    MOE_COMBINE_TK(5)
+    MOE_COMBINE_TK(6)
+    MOE_COMBINE_TK(7)
+    MOE_COMBINE_TK(8)
+#undef MOE_COMBINE_TK
+    default:
+      combine_unpermute_kernel<<<grid, kCombineThreads, 0, stream>>>(ch, pts2, expanded_row_idx, probs, K, topK, oh);
+  }
   return cudaGetLastError();
 }
 

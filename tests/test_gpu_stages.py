@@ -333,9 +333,14 @@ def test_swiglu_quant_bounds(R, I, E):
 
 
 # ------------------------------------------------------------------ Combine + Unpermute
-@pytest.mark.parametrize("cfg", ["tiny", "decode", "prefill"])
+COMBINE_CASES = ["tiny", "decode", "prefill",
+                 synth.Workload("topk12", 37, 512, 64, 20, 12, "uniform", 71),   # slots beyond the unrolled 8
+                 synth.Workload("topk3", 45, 384, 64, 7, 3, "biased", 72)]
+
+
+@pytest.mark.parametrize("cfg", COMBINE_CASES, ids=[c if isinstance(c, str) else c.name for c in COMBINE_CASES])
 def test_combine_unpermute_bit_exact(cfg):
-    w = synth.CONFIGS[cfg]
+    w = synth.CONFIGS[cfg] if isinstance(cfg, str) else cfg
     ei, probs = synth.routing(w.seed, w.M, w.E, w.topK, w.routing)
     ei[0, 0] = -1  # one invalid route
     rs = oracle.route_sort(ei, w.E)
