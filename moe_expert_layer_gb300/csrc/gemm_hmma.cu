@@ -49,16 +49,21 @@ constexpr int kMaxExperts = 1024;
 
 template <int T>
 struct TileShape;
+// ALT_EPI: the two MMA groups take turns running the item epilogue (16-row tiles,
+// whose short GMM2 items make the epilogue group the critical one); 32-row tiles
+// keep it on group 0, which leaves the other group's code free of the epilogue's
+// registers.
 template <>
-struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 4; };
+struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 4; static constexpr bool ALT_EPI = true; };
 template <>
-struct TileShape<32> { static constexpr int WM = 8, WN = 1, STAGES = 4; };
+struct TileShape<32> { static constexpr int WM = 8, WN = 1, STAGES = 4; static constexpr bool ALT_EPI = false; };
 
 template <int T>
 struct GemmCfg {
   static constexpr int WARPS_M = TileShape<T>::WM;
   static constexpr int WARPS_N = TileShape<T>::WN;
   static constexpr int STAGES = TileShape<T>::STAGES;
+  static constexpr bool ALT_EPI = TileShape<T>::ALT_EPI;
   static constexpr int MT = kBN / (16 * WARPS_M);  // m16 tiles per warp
   static constexpr int NT = T / (8 * WARPS_N);     // n8 tiles per warp
   // independent fp32 partial accumulators per output fragment (k-slices are dealt
@@ -70,7 +75,7 @@ struct GemmCfg {
   static constexpr int W_BYTES = (kBK / kSubK) * W_SUB_BYTES;
   static constexpr int STAGE_BYTES = X_BYTES + W_BYTES;
   static constexpr int EPI_BYTES = T * kBN * 2;
-  static constexpr int PART_BYTES = (kGroups - 1) * kGroupWarps * MT * NT * 4 * 32 * 4;  // groups 1.. partials
+  static constexpr int PART_BYTES = kGroupWarps * MT * NT * 4 * 32 * 4;  // one group's partials
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + PART_BYTES + 1024;
   static_assert(WARPS_M * WARPS_N == kGroupWarps, "warp grid");
   // stage n is computed by group n % kGroups: with STAGES a multiple of kGroups every
@@ -199,7 +204,8 @@ __device__ __forceinline__ void drain_chunk(float (&accf)[Cfg::P][Cfg::MT][Cfg::
 }
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
-__device__ __forceinline__ void group0_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kGroupWarps * 32)); }
+// the 8 warps of the group that runs an item's epilogue (one group at a time)
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kGroupWarps * 32)); }
 
 __device__ __forceinline__ bool wait_part(uint64_t* bar, uint32_t parity, int32_t* status) {
   if (mbar_wait_bounded(bar, parity)) return true;
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[S];
   __shared__ __align__(8) uint64_t empty_bar[S];
-  __shared__ __align__(8) uint64_t part_full_bar, part_empty_bar;  // k-half-1 partials hand-off
+  __shared__ __align__(8) uint64_t part_full_bar, part_empty_bar;  // partials hand-off to the epilogue group
   __shared__ int s_pref[kMaxExperts + 1];  // first work item of each expert
   __shared__ int s_end[kMaxExperts];       // cumsum
   __shared__ int s_wsum[kConsumerWarps];
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kGroupWarps);  // one group consumes each stage
     }
-    mbar_init(&part_full_bar, (kGroups - 1) * kGroupWarps);
+    mbar_init(&part_full_bar, kGroupWarps);
     mbar_init(&part_empty_bar, kGroupWarps);
     s_abort = 0;
     s_issued = 0;
@@ -369,7 +375,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     __half* stile = reinterpret_cast<__half*>(smem_gen + S * Cfg::STAGE_BYTES);
     constexpr int kPartWarp = Cfg::MT * Cfg::NT * 4 * 32;  // ints per warp
     int* spart_base = reinterpret_cast<int*>(smem_gen + S * Cfg::STAGE_BYTES + Cfg::EPI_BYTES) + wig * kPartWarp + lane;
-    int* spart = spart_base + (grp > 0 ? (grp - 1) : 0) * kGroupWarps * kPartWarp;
+    int* spart = spart_base;
     int slot = 0;
     uint32_t phase = 0;
     int consumed = 0, n_items = 0;
@@ -425,12 +431,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
       }
       if (own % 2 != 0) drain_chunk<Cfg>(accf, acci);
-      // ---- epilogue.  Group 1 hands its int32 partials to group 0 through shared
-      // memory (part_full / part_empty) and moves on to the next item; group 0 adds
-      // them, scales, converts, stages [T][128] binary16 and stores it coalesced.
-      if (grp > 0) {
+      // ---- epilogue.  One group runs the item's epilogue; the other hands its int32
+      // partials over through shared memory (part_full) and moves on to the next
+      // item; the epilogue group adds them, scales, converts, stages [T][128]
+      // binary16 and stores it coalesced.
+      // With ALT_EPI the groups take turns (item n: group n % 2).  Each warp owns one
+      // slice of the partials buffer, and the sender of item n is the group that read
+      // item n-1's partials, so a warp rewrites its slice only after it has read it;
+      // item n's epilogue ends (its staging-tile reads included) before the same group
+      // sends item n+1's partials, so the two groups' epilogues never overlap.
+      // Otherwise group 0 always runs it and group 1 waits for part_empty before it
+      // rewrites the buffer.
+      const int epi_grp = Cfg::ALT_EPI ? (n_items & 1) : 0;
+      if (grp != epi_grp) {
         bool got = true;
-        if (n_items > 0) got = wait_part(&part_empty_bar, (n_items - 1) & 1, args.status);
+        if (!Cfg::ALT_EPI && n_items > 0) got = wait_part(&part_empty_bar, (n_items - 1) & 1, args.status);
         got = __all_sync(0xffffffffu, got);
         if (got && ok) {
 #pragma unroll
@@ -459,10 +474,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 sum += got ? spart_base[(q - 1) * kGroupWarps * kPartWarp + ((mt * Cfg::NT + nt) * 4 + i) * 32] : 0;
               v[mt][nt][i] = sum;
             }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&part_empty_bar);
+        if (!Cfg::ALT_EPI) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&part_empty_bar);
+        }
         ok = ok && got;
-        group0_bar();  // group 0's stores of the previous item have read the staging tile
+        epilogue_bar();  // the previous epilogue's staging-tile reads are done
         if (ok) {
 #pragma unroll
           for (int mt = 0; mt < Cfg::MT; ++mt) {
@@ -477,12 +494,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             }
           }
         }
-        group0_bar();
+        epilogue_bar();
         ok = ok && !*(volatile int*)&s_abort;
         if (ok) {
           const int4* src = reinterpret_cast<const int4*>(stile);
           __half* dst = args.C + (size_t)it.row0 * args.N + it.cb * kBN;
-          for (int i = threadIdx.x; i < it.rows * (kBN / 8); i += kGroupWarps * 32) {
+          for (int i = wig * 32 + lane; i < it.rows * (kBN / 8); i += kGroupWarps * 32) {
             const int r = i / (kBN / 8), c = i % (kBN / 8);
             reinterpret_cast<int4*>(dst + (size_t)r * args.N)[c] = src[r * (kBN / 8) + c];
           }
