@@ -55,6 +55,27 @@ def test_layer_small_full_parity(w):
     assert same > 0.99, "only %.4f of outputs bit-identical" % same
 
 
+EXTREME = [
+    synth.Workload("max_k_i_warp", 3, 16384, 8192, 2, 1, "uniform", 121),     # largest K and I, warp-MMA engine
+    synth.Workload("max_k_i_pairs", 40, 16384, 8192, 1, 1, "uniform", 122),   # largest K and I, tcgen05 pairs
+    synth.Workload("max_e", 2048, 128, 64, 1023, 8, "zipf", 123),             # largest expert count
+    synth.Workload("topk_all", 20, 256, 64, 5, 5, "uniform", 124),            # every token on every expert
+]
+
+
+@pytest.mark.parametrize("w", EXTREME, ids=[w.name for w in EXTREME])
+def test_layer_extreme_dims(w):
+    """The ABI's limits (K = 16384, I = 8192, E = 1023, topK = E), full parity."""
+    inp = synth.make_inputs(w)
+    ref = oracle.layer_fwd(inp)
+    out, ws = run_layer(w, upload_inputs(inp))
+    got = host(out)
+    assert moe.moe_workspace_status(ws) == 0
+    assert_out_close(got, ref)
+    same = (got.view(np.uint16) == ref.view(np.uint16)).mean()
+    assert same > 0.99, "only %.4f of outputs bit-identical" % same
+
+
 def test_layer_invalid_routes_and_zero_tokens():
     w = synth.Workload("edge", 50, 256, 128, 6, 3, "uniform", 111)
     inp = synth.make_inputs(w)
