@@ -533,12 +533,13 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, T) ||
       !encode_tensor_map_2d(&tx8, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, 8))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!attr_set[dev]) {
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<T>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   GemmArgs a;
   a.cumsum = p.cumsum;

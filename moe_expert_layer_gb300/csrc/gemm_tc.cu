@@ -691,8 +691,9 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
   if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64,
                             kHalfRows))
     return cudaErrorInvalidValue;
-  static bool checked = false;
-  if (!checked) {
+  static bool checked[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!checked[dev]) {
     // The warpgroups' register split (setmaxnreg) adds up to exactly the registers
     // the CTA is launched with; a build that launches with another count would
     // leave the drains' increase waiting forever, so it is refused here.
@@ -702,7 +703,7 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
     err = cudaFuncSetAttribute(grouped_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
-    checked = true;
+    checked[dev] = true;
   }
   Args a;
   a.cumsum = p.cumsum;
