@@ -49,26 +49,23 @@ constexpr int kMaxExperts = 1024;
 
 template <int T>
 struct TileShape;
-// ALT_EPI: the two MMA groups take turns running the item epilogue (16-row tiles,
-// whose short GMM2 items make the epilogue group the critical one); 32-row tiles
-// keep it on group 0, which leaves the other group's code free of the epilogue's
-// registers.
+// P: independent fp32 partial accumulators per output fragment (k-slices are dealt
+// round-robin to them). 16-row tiles have 2 fragments per warp and take 4 partials
+// so that 8 MMA chains are in flight; 32-row tiles have 4 fragments and measure
+// faster with a single partial (fewer registers, no fold in the epilogue).
 template <>
-struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 4; static constexpr bool ALT_EPI = true; };
+struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 4, P = 4; };
 template <>
-struct TileShape<32> { static constexpr int WM = 8, WN = 1, STAGES = 4; static constexpr bool ALT_EPI = false; };
+struct TileShape<32> { static constexpr int WM = 8, WN = 1, STAGES = 4, P = 1; };
 
 template <int T>
 struct GemmCfg {
   static constexpr int WARPS_M = TileShape<T>::WM;
   static constexpr int WARPS_N = TileShape<T>::WN;
   static constexpr int STAGES = TileShape<T>::STAGES;
-  static constexpr bool ALT_EPI = TileShape<T>::ALT_EPI;
   static constexpr int MT = kBN / (16 * WARPS_M);  // m16 tiles per warp
   static constexpr int NT = T / (8 * WARPS_N);     // n8 tiles per warp
-  // independent fp32 partial accumulators per output fragment (k-slices are dealt
-  // round-robin), so that at least 8 MMA chains are in flight per warp
-  static constexpr int P = (MT * NT >= 8) ? 1 : 8 / (MT * NT);
+  static constexpr int P = TileShape<T>::P;
   static constexpr int X_HALF_BYTES = T * 128;     // one k quarter: [T][64] binary16, 128-B swizzled rows
   static constexpr int X_BYTES = kQuarters * X_HALF_BYTES;
   static constexpr int W_SUB_BYTES = kBN * kSubK;  // [128][128] int8, 128-B swizzled rows
@@ -265,7 +262,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[S];
   __shared__ __align__(8) uint64_t empty_bar[S];
-  __shared__ __align__(8) uint64_t part_full_bar, part_empty_bar;  // partials hand-off to the epilogue group
+  __shared__ __align__(8) uint64_t part_full_bar;  // partials hand-off to the epilogue group
   __shared__ int s_pref[kMaxExperts + 1];  // first work item of each expert
   __shared__ int s_end[kMaxExperts];       // cumsum
   __shared__ int s_wsum[kConsumerWarps];
@@ -310,7 +307,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       mbar_init(&empty_bar[s], kGroupWarps);  // one group consumes each stage
     }
     mbar_init(&part_full_bar, kGroupWarps);
-    mbar_init(&part_empty_bar, kGroupWarps);
     s_abort = 0;
     s_issued = 0;
     fence_barrier_init();
@@ -435,19 +431,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       // partials over through shared memory (part_full) and moves on to the next
       // item; the epilogue group adds them, scales, converts, stages [T][128]
       // binary16 and stores it coalesced.
-      // With ALT_EPI the groups take turns (item n: group n % 2).  Each warp owns one
-      // slice of the partials buffer, and the sender of item n is the group that read
-      // item n-1's partials, so a warp rewrites its slice only after it has read it;
-      // item n's epilogue ends (its staging-tile reads included) before the same group
-      // sends item n+1's partials, so the two groups' epilogues never overlap.
-      // Otherwise group 0 always runs it and group 1 waits for part_empty before it
-      // rewrites the buffer.
-      const int epi_grp = Cfg::ALT_EPI ? (n_items & 1) : 0;
+      // The groups take turns (item n: group n % 2), so that one item's epilogue
+      // overlaps the other group's MMAs of the next.  Each warp owns one slice of the
+      // partials buffer, and the sender of item n is the group that read item n-1's
+      // partials, so a warp rewrites its slice only after it has read it; item n's
+      // epilogue ends (its staging-tile reads included) before the same group sends
+      // item n+1's partials, so the two groups' epilogues never overlap.
+      const int epi_grp = n_items & 1;
       if (grp != epi_grp) {
-        bool got = true;
-        if (!Cfg::ALT_EPI && n_items > 0) got = wait_part(&part_empty_bar, (n_items - 1) & 1, args.status);
-        got = __all_sync(0xffffffffu, got);
-        if (got && ok) {
+        if (ok) {
 #pragma unroll
           for (int mt = 0; mt < Cfg::MT; ++mt)
 #pragma unroll
@@ -457,7 +449,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&part_full_bar);
-        ok = ok && got;
       } else {
         bool got = wait_part(&part_full_bar, n_items & 1, args.status);
         got = __all_sync(0xffffffffu, got);
@@ -474,10 +465,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 sum += got ? spart_base[(q - 1) * kGroupWarps * kPartWarp + ((mt * Cfg::NT + nt) * 4 + i) * 32] : 0;
               v[mt][nt][i] = sum;
             }
-        if (!Cfg::ALT_EPI) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&part_empty_bar);
-        }
         ok = ok && got;
         epilogue_bar();  // the previous epilogue's staging-tile reads are done
         if (ok) {
