@@ -301,7 +301,7 @@ def main():
         evs[1].record(stream)
         moe.moe_quant_dispatch(d, dev["x"], dev["expert_idx"], expanded, a1, pts1, bounds[0], stream)
         evs[2].record(stream)
-        moe.moe_gmm1(d, a1, cs, bounds[0], dev["w1"], dev["s1"], c1, gws, stream)
+        moe.moe_gmm1(d, a1, None, cs, bounds[0], dev["w1"], dev["s1"], c1, gws, stream)
         evs[3].record(stream)
         moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, dev["expert_idx"], None, q2, pts2, bounds[1], stream)
         evs[4].record(stream)

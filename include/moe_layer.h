@@ -151,13 +151,17 @@ int32_t moe_route_sort(const moe_dims_t* d, const int32_t* expert_idx, int32_t* 
  * quantisation, once per token: pts1[t] = max_k |x[t,k]| / 127 and
  * q = round-half-away(x / pts1), clamped to [-127, 127]; an all-zero token gets
  * pts1 = 0 and zero codes.
+ *   expert_idx [M][topK] (read only when a1_bounds is given)
  *   xq_i8  [M][K] int8 codes (may be NULL)
  *   xq_f16 [M][K] the same codes as binary16 integers (may be NULL; at least
- *          one of the two must be given)
+ *          one of the two must be given): the operand GMM1 gathers from
  *   pts1   [M]    fp32 scales
+ *   a1_bounds: NULL, or a zero-filled int32 [E][MOE_BOUND_SEGMENTS] that receives,
+ *          for every expert, the segment maxima of sum |code| over the tokens routed
+ *          to it (see "Activation bounds"; invalid routes contribute nothing)
  */
-int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, int8_t* xq_i8, uint16_t* xq_f16,
-                         float* pts1, void* stream);
+int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx, int8_t* xq_i8,
+                         uint16_t* xq_f16, float* pts1, int32_t* a1_bounds, void* stream);
 
 /*
  * Allocation-free route sort.  The paper has no counterpart: this entry point
@@ -195,7 +199,7 @@ int32_t moe_route_sort_noalloc(const moe_dims_t* d, const int32_t* expert_idx, i
  *   sum over k in the segment of |a[row][k]|      for every row of expert e,
  * so a chunk of consecutive segments S is exact when 128 * sum_{s in S} bound[e][s]
  * <= 2^24 (|w| <= 128); the GEMMs then use the longest such uniform chunk per
- * expert.  moe_quant_dispatch and moe_swiglu_quant produce exact maxima when
+ * expert.  moe_quant_tokens, moe_quant_dispatch and moe_swiglu_quant produce exact maxima when
  * given a zero-filled array (atomic max); a bound that is too small makes the
  * GEMM results inexact.  Passing NULL everywhere keeps the 1024-deep chunks.
  */
@@ -221,17 +225,24 @@ int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t
 size_t moe_gmm_workspace_size(const moe_dims_t* d);
 
 /*
- * GMM1 (page section "3. GMM1"): for each valid expanded row d of expert e
- * (rows cumsum[e]-count_e .. cumsum[e]-1):
+ * GMM1 (page section "3. GMM1", with "2. Dispatch" fused as a gather): for each
+ * valid expanded row d of expert e (rows cumsum[e]-count_e .. cumsum[e]-1):
  *   acc[n]   = sum_k a1[d][k] * w1[e][n][k]                (exact integer)
  *   c1[d][n] = binary16(float(acc[n]) * s1[e][n])          n < 2I
- *   a1_f16 [R][K] expert-major binary16-coded int8 codes (moe_quant_dispatch);
- *   a1_bounds: NULL or the activation bounds of a1_f16 (see "Activation bounds");
+ * where a1[d] is
+ *   a1_f16[d]  when sorted_src_route is NULL: a1_f16 is [R][K] expert-major
+ *          (moe_quant_dispatch; the layer's path);
+ *   a1_f16[sorted_src_route[d] / topK]  when sorted_src_route is given: a1_f16 is
+ *          [M][K] token-major binary16-coded codes (moe_quant_tokens), gathered by
+ *          TMA in 4-row groups.  This needs topK times less activation memory but
+ *          runs GMM1 1.2x (16-row tiles) to 3.2x (tcgen05 pairs) slower on GB300:
+ *          a gather moves 512 B per TMA instruction, a tiled box up to 16 KB.
+ *   a1_bounds: NULL or the activation bounds of the rows a1[d] (see "Activation bounds");
  *   c1 [R][2I] (rows >= cumsum[E-1] untouched)
  */
-int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int32_t* a1_bounds,
-                 const int8_t* w1, const float* s1, uint16_t* c1, void* workspace, size_t workspace_bytes,
-                 void* stream);
+int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* sorted_src_route, const int32_t* cumsum,
+                 const int32_t* a1_bounds, const int8_t* w1, const float* s1, uint16_t* c1, void* workspace,
+                 size_t workspace_bytes, void* stream);
 
 /*
  * SwiGLU + dynamic requant (page section "4. SwiGLU"), per valid expanded row d

@@ -68,10 +68,10 @@ def load_library(path=None):
         "moe_workspace_clear_status": ([vp, vp], i32),
         "moe_route_sort_workspace_size": ([D], sz),
         "moe_route_sort": ([D] + [vp] * 6 + [sz, vp], i32),
-        "moe_quant_tokens": ([D] + [vp] * 5, i32),
+        "moe_quant_tokens": ([D] + [vp] * 7, i32),
         "moe_gmm_workspace_size": ([D], sz),
         "moe_quant_dispatch": ([D] + [vp] * 7, i32),
-        "moe_gmm1": ([D] + [vp] * 7 + [sz, vp], i32),
+        "moe_gmm1": ([D] + [vp] * 8 + [sz, vp], i32),
         "moe_swiglu_quant": ([D] + [vp] * 10, i32),
         "moe_gmm2": ([D] + [vp] * 7 + [sz, vp], i32),
         "moe_combine_unpermute": ([D] + [vp] * 6, i32),
@@ -159,9 +159,9 @@ def moe_route_sort(d, expert_idx, sorted_src_route, expanded_row_idx, tokens_per
         _p(tokens_per_expert), _p(cumsum), _p(workspace), nbytes, _stream(stream)))
 
 
-def moe_quant_tokens(d, x, xq_i8, xq_f16, pts1, stream=None):
+def moe_quant_tokens(d, x, expert_idx, xq_i8, xq_f16, pts1, a1_bounds, stream=None):
     _check("moe_quant_tokens", load_library().moe_quant_tokens(
-        ctypes.byref(d), _p(x), _p(xq_i8), _p(xq_f16), _p(pts1), _stream(stream)))
+        ctypes.byref(d), _p(x), _p(expert_idx), _p(xq_i8), _p(xq_f16), _p(pts1), _p(a1_bounds), _stream(stream)))
 
 
 def moe_quant_dispatch(d, x, expert_idx, expanded_row_idx, a1_f16, pts1, a1_bounds, stream=None):
@@ -170,9 +170,10 @@ def moe_quant_dispatch(d, x, expert_idx, expanded_row_idx, a1_f16, pts1, a1_boun
         _stream(stream)))
 
 
-def moe_gmm1(d, a1_f16, cumsum, a1_bounds, w1, s1, c1, workspace, stream=None):
+def moe_gmm1(d, a1_f16, sorted_src_route, cumsum, a1_bounds, w1, s1, c1, workspace, stream=None):
     _check("moe_gmm1", load_library().moe_gmm1(
-        ctypes.byref(d), _p(a1_f16), _p(cumsum), _p(a1_bounds), _p(w1), _p(s1), _p(c1), _p(workspace),
+        ctypes.byref(d), _p(a1_f16), _p(sorted_src_route), _p(cumsum), _p(a1_bounds), _p(w1), _p(s1), _p(c1),
+        _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

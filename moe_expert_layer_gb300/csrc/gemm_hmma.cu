@@ -90,6 +90,8 @@ struct GemmArgs {
   int32_t* status;
   int E, N, Kd;
   int split_rows;  // this engine serves the experts with at most split_rows rows
+  const int32_t* gather_route;  // null: tiled token boxes; else row d gathers token gather_route[d] / topK
+  int topK;
 };
 
 // 4 int8 (one 32-bit word) -> two half2 {b0,b1}, {b2,b3}, exactly.
@@ -252,7 +254,9 @@ __device__ __forceinline__ Item decode_item(int j, const int* s_pref, const int*
   return it;
 }
 
-template <int T>
+// GATHER: token rows gathered by index (args.gather_route) instead of tiled boxes of
+// expert-major rows; a separate instantiation, so the tiled kernel carries none of it.
+template <int T, bool GATHER>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                                                                        const __grid_constant__ CUtensorMap tm_x,
                                                                        const __grid_constant__ CUtensorMap tm_x8,
@@ -317,19 +321,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
 
+  if (GATHER) {
+    // Gathered stages leave the rows past a tile's last 4-row group, and quarters
+    // past K, unwritten.  Starting every token stage at zero keeps such rows finite
+    // codes (zero, or a previous stage's), so their products with the zero-filled
+    // weight columns past K vanish and the outputs of the extra rows, never stored,
+    // cannot disturb anything.
+    for (int s = 0; s < S; ++s) {
+      int4* xz = reinterpret_cast<int4*>(smem_gen + s * Cfg::STAGE_BYTES);
+      for (int i = threadIdx.x; i < Cfg::X_BYTES / 16; i += kGemmThreads) xz[i] = make_int4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+  }
+
   if (warp == kConsumerWarps) {
     // ================= TMA producer warp =================
+    constexpr bool gather = GATHER;
     int slot = 0;
     uint32_t phase = 0;
     int issued = 0;
     for (int j = blockIdx.x; j < total; j += gridDim.x) {
       const Item it = decode_item<T>(j, s_pref, s_end, E, n_cb);
       const int w_row = it.e * args.N + it.cb * kBN;
-      // tiles of at most 8 rows (most decode tiles) load an 8-row token box
+      // Token rows.  Tiled: a box of T rows from the expert-major operand (tiles of at
+      // most 8 rows, most decode tiles, load an 8-row box).  Gathered: the tile's rows
+      // in 4-row groups, only the groups that hold real rows; lane l issues group
+      // l % g4 of quarter l / g4, and its group's rows past the tile's last real row
+      // repeat that row's token (their outputs are never stored).
       const bool small = (T > 8) && (it.rows <= 8);
       const void* tmx = small ? static_cast<const void*>(&tm_x8) : static_cast<const void*>(&tm_x);
-      const uint32_t tx = (uint32_t)Cfg::W_BYTES + (uint32_t)(small ? 8 : T) * 128u * kQuarters;
+      const int g4 = (it.rows + 3) >> 2;
+      int4 tok = make_int4(0, 0, 0, 0);
+      if (gather) {
+        const int r0 = it.row0 + 4 * (lane % g4), last = it.row0 + it.rows - 1;
+        tok.x = __ldg(args.gather_route + min(r0, last)) / args.topK;
+        tok.y = __ldg(args.gather_route + min(r0 + 1, last)) / args.topK;
+        tok.z = __ldg(args.gather_route + min(r0 + 2, last)) / args.topK;
+        tok.w = __ldg(args.gather_route + min(r0 + 3, last)) / args.topK;
+      }
       for (int kb = 0; kb < nk; ++kb) {
+        const int kx = kb * kBK;
+        // quarters of this stage inside K (K % 128 == 0: a tail stage has 2); the
+        // tiled boxes read zero fill past K, the gathers are not issued there
+        const int nq = gather ? min(kQuarters, (args.Kd - kx) / 64) : kQuarters;
+        const uint32_t tx = (uint32_t)Cfg::W_BYTES + (uint32_t)(gather ? 4 * g4 : (small ? 8 : T)) * 128u * nq;
         bool ok = true;
         if (lane == 0) {
           ok = !*(volatile int*)&s_abort && mbar_wait_bounded(&empty_bar[slot], phase ^ 1u);
@@ -341,14 +377,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) goto producer_done;
         uint8_t* xs = smem_gen + slot * Cfg::STAGE_BYTES;
         uint8_t* ws = xs + Cfg::X_BYTES;
-        const int kx = kb * kBK;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full_bar[slot], tx);
           tma_load_2d(ws, &tm_w, kx, w_row, &full_bar[slot]);
           tma_load_2d(ws + Cfg::W_SUB_BYTES, &tm_w, kx + kSubK, w_row, &full_bar[slot]);
+          if (!gather) {
 #pragma unroll
-          for (int q = 0; q < kQuarters; ++q)
-            tma_load_2d(xs + q * Cfg::X_HALF_BYTES, tmx, kx + 64 * q, it.row0, &full_bar[slot]);
+            for (int q = 0; q < kQuarters; ++q)
+              tma_load_2d(xs + q * Cfg::X_HALF_BYTES, tmx, kx + 64 * q, it.row0, &full_bar[slot]);
+          }
+        }
+        if (gather) {
+          __syncwarp();  // the stage's expected bytes are posted before any gather lands
+          if (lane < g4 * nq) {
+            const int q = lane / g4, r = lane - q * g4;
+            tma_gather4(xs + q * Cfg::X_HALF_BYTES + r * 512, &tm_x, kx + 64 * q, tok, &full_bar[slot]);
+          }
         }
         ++issued;
         if (++slot == S) {
@@ -509,21 +553,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 // ------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------
-template <int T>
+template <int T, bool GATHER>
 cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   using Cfg = GemmCfg<T>;
   CUtensorMap tw, tx;
   if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kSubK,
                             kBN))
     return cudaErrorInvalidValue;
+  // token operand: tiled boxes of T and 8 rows, or (gathering) one-row boxes over the
+  // token rows, passed in both slots
   CUtensorMap tx8;
-  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, T) ||
-      !encode_tensor_map_2d(&tx8, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64, 8))
+  constexpr bool gather = GATHER;
+  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.act_rows, 64,
+                            gather ? 1 : T) ||
+      !encode_tensor_map_2d(&tx8, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.act_rows, 64,
+                            gather ? 1 : 8))
     return cudaErrorInvalidValue;
   static bool attr_set[kMaxDevices] = {};
   const int dev = current_device();
   if (!attr_set[dev]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<T>,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<T, GATHER>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
@@ -537,15 +586,18 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.N = p.N;
   a.Kd = p.Kd;
   a.split_rows = p.split_rows;
-  grouped_gemm_kernel<T><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
+  a.gather_route = p.gather_route;
+  a.topK = p.topK;
+  grouped_gemm_kernel<T, GATHER><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream) {
-  if (T == 32) return launch_t<32>(p, stream);
-  return launch_t<16>(p, stream);
+  const bool g = p.gather_route != nullptr;
+  if (T == 32) return g ? launch_t<32, true>(p, stream) : launch_t<32, false>(p, stream);
+  return g ? launch_t<16, true>(p, stream) : launch_t<16, false>(p, stream);
 }
 
 }  // namespace moe

@@ -110,6 +110,8 @@ struct Args {
   int E, N, Kd;
   int split_rows;  // this engine serves the experts with more than split_rows rows
   const int32_t* bounds;  // [E][kBoundSegments] activation bounds, or null (1024-deep chunks)
+  const int32_t* gather_route;  // null: tiled token boxes; else row d gathers token gather_route[d] / topK
+  int topK;
 #ifdef MOE_GEMM_PROFILE
   unsigned long long* prof;
 #endif
@@ -352,6 +354,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
+// GATHER: token rows gathered by index (args.gather_route) instead of tiled boxes of
+// expert-major rows; a separate instantiation, so the tiled kernel carries none of it.
+template <bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                              const Args args) {
@@ -468,23 +473,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         PROF_FLUSH(0);
       }
     } else if (warp == kXProducerWarp) {
-      // ======================= token producer (one lane) =======================
-      if (lane == 0) {
-        int n = 0;
-        for (int j = pair; j < total; j += npairs) {
-          const Item it = decode_item(j, s_pref, s_end, E);
-          const int y = it.row0 + (int)rank * (it.n_mma >> 1);
-          for (int kb = 0; kb < nk; ++kb, ++n) {
-            const int slot = n % S;
-            if (!PROF_WAIT(0, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status)))
-              goto x_done;
-            uint8_t* xs_g = smem_gen + SW * kWBytes + slot * kXBytes;
-            mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)kXBytes);
-            tma_load_2d(xs_g, &tm_x, kb * kBK, y, &xfull_bar[slot]);
-            tma_load_2d(xs_g + kXHalfBytes, &tm_x, kb * kBK + 64, y, &xfull_bar[slot]);
+      // ======================= token producer =======================
+      // This CTA's half of the item's N rows (hr = N/2), as two [hr][64] boxes per
+      // stage.  Tiled: lane 0 loads two 128-row boxes of the expert-major operand.
+      // Gathered: the half's 4-row groups (G = hr/4 of them) are gathered by token
+      // index, lane l issuing group l % G of both boxes (G = 32) or of box l / G
+      // (G = 8, 16); rows past the item's last real row repeat that row's token
+      // (their outputs are never stored).
+      int n = 0;
+      if (!GATHER) {
+        if (lane == 0) {
+          for (int j = pair; j < total; j += npairs) {
+            const Item it = decode_item(j, s_pref, s_end, E);
+            const int y = it.row0 + (int)rank * (it.n_mma >> 1);
+            for (int kb = 0; kb < nk; ++kb, ++n) {
+              const int slot = n % S;
+              if (!PROF_WAIT(0, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status)))
+                goto x_done;
+              uint8_t* xs_g = smem_gen + SW * kWBytes + slot * kXBytes;
+              mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)kXBytes);
+              tma_load_2d(xs_g, &tm_x, kb * kBK, y, &xfull_bar[slot]);
+              tma_load_2d(xs_g + kXHalfBytes, &tm_x, kb * kBK + 64, y, &xfull_bar[slot]);
+            }
           }
         }
-      x_done:
+      } else {
+        for (int j = pair; j < total; j += npairs) {
+          const Item it = decode_item(j, s_pref, s_end, E);
+          const int hr = it.n_mma >> 1;
+          const int G = hr >> 2;
+          const int r0 = it.row0 + (int)rank * hr + 4 * (lane % G), last = it.row0 + it.rows - 1;
+          int4 tok;
+          tok.x = __ldg(args.gather_route + min(r0, last)) / args.topK;
+          tok.y = __ldg(args.gather_route + min(r0 + 1, last)) / args.topK;
+          tok.z = __ldg(args.gather_route + min(r0 + 2, last)) / args.topK;
+          tok.w = __ldg(args.gather_route + min(r0 + 3, last)) / args.topK;
+          for (int kb = 0; kb < nk; ++kb, ++n) {
+            const int slot = n % S;
+            bool ok = true;
+            if (lane == 0)
+              ok = PROF_WAIT(0, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status));
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) goto x_done;
+            uint8_t* xs_g = smem_gen + SW * kWBytes + slot * kXBytes;
+            if (lane == 0) mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)hr * 256u);
+            __syncwarp();  // the stage's expected bytes are posted before any gather lands
+            for (int i = lane; i < 2 * G; i += 32) {
+              const int box = i / G;
+              tma_gather4(xs_g + box * kXHalfBytes + (i - box * G) * 512, &tm_x, kb * kBK + 64 * box, tok,
+                          &xfull_bar[slot]);
+            }
+          }
+        }
+      }
+    x_done:
+      if (lane == 0) {
         s_x_issued = n;
         PROF_FLUSH(2);
       }
@@ -681,15 +723,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-}  // namespace
-
-cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream) {
+template <bool GATHER>
+cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   CUtensorMap tw, tx;
   if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kBK,
                             kBM))
     return cudaErrorInvalidValue;
-  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.R, 64,
-                            kHalfRows))
+  // token operand: 128-row tiled boxes, or (gathering) one-row boxes over the token rows
+  if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.act_rows, 64,
+                            GATHER ? 1 : kHalfRows))
     return cudaErrorInvalidValue;
   static bool checked[kMaxDevices] = {};
   const int dev = current_device();
@@ -698,10 +740,11 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
     // the CTA is launched with; a build that launches with another count would
     // leave the drains' increase waiting forever, so it is refused here.
     cudaFuncAttributes fa;
-    cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_pair_kernel);
+    cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_pair_kernel<GATHER>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
     if (err != cudaSuccess) return err;
     checked[dev] = true;
   }
@@ -715,13 +758,21 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
   a.Kd = p.Kd;
   a.split_rows = p.split_rows;
   a.bounds = p.bounds;
+  a.gather_route = p.gather_route;
+  a.topK = p.topK;
 #ifdef MOE_GEMM_PROFILE
   a.prof = g_gemm_prof;
   if (!a.prof) return cudaErrorInvalidValue;
 #endif
   const int grid = sm_count() & ~1;  // whole pairs, one CTA per SM
-  grouped_gemm_pair_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tw, tx, a);
+  grouped_gemm_pair_kernel<GATHER><<<grid, kThreads, kSmemBytes, stream>>>(tw, tx, a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream) {
+  return p.gather_route ? launch_pair<true>(p, stream) : launch_pair<false>(p, stream);
 }
 
 // Engine choice.  A tcgen05.mma costs ~90 cycles for any N up to 128 (measured on

@@ -30,7 +30,11 @@ cudaError_t launch_combine_unpermute(const uint16_t* c2, const float* pts2, cons
 // Grouped W8A8 GEMM over expert-major rows (GMM1 and GMM2):
 //   C[row][n] = sat_f16(float(sum_k act[row][k] * W[e][n][k]) * scale[e][n]),  n < N
 struct GroupedGemmProblem {
-  const uint16_t* act;              // [R][Kd] binary16-coded int8 activations, expert-major rows
+  const uint16_t* act;              // [act_rows][Kd] binary16-coded int8 activations: expert-major
+                                    // rows, or (gather_route set) token rows
+  const int32_t* gather_route;      // null, or [R] route of each expert-major row: row d's
+                                    // activations are act[gather_route[d] / topK] (TMA gather)
+  int topK, act_rows;
   const int32_t* cumsum;            // [E] inclusive prefix of rows per expert
   const int8_t* w;                  // [E][N][Kd]
   const float* scale;               // [E][N]

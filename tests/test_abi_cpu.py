@@ -60,8 +60,8 @@ def test_entry_points_reject_before_touching_the_device(lib):
     # invalid shape -> MOE_ERR_SHAPE, NULL pointers -> MOE_ERR_NULL; no GPU needed for either
     assert lib.moe_layer_fwd(ctypes.byref(bad), *([None] * 9), 0, None) == -2
     assert lib.moe_layer_fwd(ctypes.byref(d), *([None] * 9), 0, None) == -1
-    assert lib.moe_quant_tokens(ctypes.byref(d), None, None, None, None, None) == -1
-    assert lib.moe_gmm1(ctypes.byref(bad), *([None] * 7), 0, None) == -2
+    assert lib.moe_quant_tokens(ctypes.byref(d), *([None] * 7)) == -1
+    assert lib.moe_gmm1(ctypes.byref(bad), *([None] * 8), 0, None) == -2
     assert lib.moe_quant_dispatch(ctypes.byref(d), *([None] * 7)) == -1
     assert lib.moe_status_string(-5) == b"workspace missing or too small"
     # misaligned pointers -> MOE_ERR_ALIGN

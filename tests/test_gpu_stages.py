@@ -83,7 +83,7 @@ def test_quant_tokens_bit_exact(M, K):
     xq_ref, pts_ref = oracle.quant_tokens(x)
     d = moe.dims(M, K, 64, 4, 1)
     xq8, xq16, pts = empty((M, K), torch.int8), empty((M, K), torch.float16), empty(M, torch.float32)
-    moe.moe_quant_tokens(d, dev(x), xq8, xq16, pts)
+    moe.moe_quant_tokens(d, dev(x), None, xq8, xq16, pts, None)
     torch.cuda.synchronize()
     assert_bits_equal(host(xq8), xq_ref, "xq")
     assert_bits_equal(host(pts), pts_ref, "pts1")
@@ -126,6 +126,29 @@ def _bounds_ref(codes, cumsum, E):
             b[e, :nseg] = seg[lo:hi].max(0)
         lo = hi
     return b
+
+
+@pytest.mark.parametrize("cfg", ["decode", "prefill", "mid"])
+def test_quant_tokens_bounds(cfg):
+    """The token quant's activation bounds (the layer's path: codes stay token-major,
+    GMM1 gathers them) are the exact per-expert segment maxima of sum |code| over the
+    expert's routed tokens, as if the codes had been dispatched to expert-major rows."""
+    w = synth.CONFIGS[cfg]
+    x = synth.normal_f16(w.seed, 1, (w.M, w.K))
+    ei, _ = synth.routing(w.seed, w.M, w.E, w.topK, w.routing)
+    ei[1, 0] = -1
+    rs = oracle.route_sort(ei, w.E)
+    xq_ref, pts_ref = oracle.quant_tokens(x)
+    Rv = w.R - rs["invalid"]
+    a1_ref = xq_ref[rs["sorted_src_route"][:Rv] // w.topK]
+    d = _dims(w)
+    xq16, pts = empty((w.M, w.K), torch.float16), empty(w.M, torch.float32)
+    bounds = torch.zeros((w.E, moe.BOUND_SEGMENTS), dtype=torch.int32, device="cuda")
+    moe.moe_quant_tokens(d, dev(x), dev(ei), None, xq16, pts, bounds)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(xq16), xq_ref.astype(np.float16), "xq as binary16")
+    assert_bits_equal(host(pts), pts_ref, "pts1")
+    assert_bits_equal(host(bounds), _bounds_ref(a1_ref, rs["cumsum"], w.E), "a1 bounds")
 
 
 @pytest.mark.parametrize("cfg", ["decode", "prefill", "mid"])
@@ -178,18 +201,28 @@ GEMM_CASES = [
 ]
 
 
+def _gmm1(d, xq, rs, topK, R, gather, bounds, w1, s1, c1, ws):
+    """GMM1 on the oracle's token codes: gathered from token rows by the kernel
+    (the layer's path), or from expert-major rows dispatched here."""
+    if gather:
+        moe.moe_gmm1(d, dev(xq.astype(np.float16)), dev(rs["sorted_src_route"]), dev(rs["cumsum"]), bounds,
+                     dev(w1), dev(s1), c1, ws)
+    else:
+        moe.moe_gmm1(d, dev(_a1(xq, rs, topK, R)), None, dev(rs["cumsum"]), bounds, dev(w1), dev(s1), c1, ws)
+
+
+@pytest.mark.parametrize("gather", [True, False], ids=["gather", "rows"])
 @pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
 @pytest.mark.parametrize("w", GEMM_CASES, ids=[w.name for w in GEMM_CASES])
-def test_gmm1_bit_exact(w, bounded):
+def test_gmm1_bit_exact(w, bounded, gather):
     inp, rs, xq, pts1 = _stage_inputs(w)
     Rv = w.R - rs["invalid"]
     _, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], inp["expert_idx"], inp["w1"], inp["s1"], Rv)
     d = _dims(w)
     c1 = torch.full((w.R, 2 * w.I), float("nan"), dtype=torch.float16, device="cuda")
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    a1 = _a1(xq, rs, w.topK, w.R)
-    bounds = dev(_bounds_ref(a1, rs["cumsum"], w.E)) if bounded else None
-    moe.moe_gmm1(d, dev(a1), dev(rs["cumsum"]), bounds, dev(inp["w1"]), dev(inp["s1"]), c1, ws)
+    bounds = dev(_bounds_ref(_a1(xq, rs, w.topK, w.R), rs["cumsum"], w.E)) if bounded else None
+    _gmm1(d, xq, rs, w.topK, w.R, gather, bounds, inp["w1"], inp["s1"], c1, ws)
     assert moe.moe_workspace_status(ws) == 0
     assert_bits_equal(host(c1)[:Rv], c1_ref, "c1")
 
@@ -239,7 +272,7 @@ def test_gmm_accumulator_exact_beyond_fp32_mantissa(M, wv):
     d = moe.dims(M, K, I, E, 1)
     c1 = empty((M, 2 * I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(_a1(xq, rs, 1, M)), dev(rs["cumsum"]), None, dev(w1), dev(s1), c1, ws)
+    _gmm1(d, xq, rs, 1, M, True, None, w1, s1, c1, ws)
     got = host(c1).astype(np.float64)
     assert np.array_equal(got, acc_ref.astype(np.float64))
 
@@ -271,12 +304,13 @@ def test_gmm_bounds_at_the_limit(K):
     d = moe.dims(M, K, I, E, 1)
     c1 = empty((M, 2 * I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(a1), dev(rs["cumsum"]), dev(b), dev(w1), dev(s1), c1, ws)
+    _gmm1(d, xq, rs, 1, M, True, dev(b), w1, s1, c1, ws)
     assert moe.moe_workspace_status(ws) == 0
     assert_bits_equal(host(c1), c1_ref, "c1")
 
 
-def test_gmm_empty_experts_and_single_rows():
+@pytest.mark.parametrize("gather", [True, False], ids=["gather", "rows"])
+def test_gmm_empty_experts_and_single_rows(gather):
     """Experts with 0 and 1 rows, and a row tile tail of every length."""
     w = synth.Workload("sparse", 23, 256, 64, 12, 1, "uniform", 61)
     inp, rs, xq, pts1 = _stage_inputs(w)
@@ -286,7 +320,7 @@ def test_gmm_empty_experts_and_single_rows():
     d = _dims(w)
     c1 = empty((w.R, 2 * w.I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    moe.moe_gmm1(d, dev(_a1(xq, rs, 1, w.R)), dev(rs["cumsum"]), None, dev(inp["w1"]), dev(inp["s1"]), c1, ws)
+    _gmm1(d, xq, rs, 1, w.R, gather, None, inp["w1"], inp["s1"], c1, ws)
     assert_bits_equal(host(c1), c1_ref, "c1")
 
 
