@@ -326,7 +326,8 @@ def test_gmm_empty_experts_and_single_rows(gather):
 
 # ------------------------------------------------------------------ SwiGLU
 @pytest.mark.parametrize("R,I,spread", [(64, 256, 1500), (300, 2048, 1500), (77, 1408, 1500), (5, 8192, 1500),
-                                         (2000, 1408, 100), (300, 2048, 30)])
+                                         (2000, 1408, 100), (300, 2048, 30), (4096, 1408, 1500), (4101, 2048, 30),
+                                         (4096, 8192, 100)])
 def test_swiglu_quant(R, I, spread):
     """spread 1500 puts the SwiGLU inputs h at |h| ~ 45 (as the workloads do);
     100 and 30 at |h| ~ 3 and ~1, where exp(-h) and the division shape every value."""
