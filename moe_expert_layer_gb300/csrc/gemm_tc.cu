@@ -317,15 +317,24 @@ struct WorkList {
 
 // Work item j -> (expert, channel block, first row, rows, MMA N).  In the first
 // stretch, the last expert whose first item is <= j (experts without N = 256 tiles
-// leave the prefix flat and are skipped).
-__device__ __forceinline__ Item decode_item(int j, const WorkList& wl) {
+// leave the prefix flat and are skipped).  A role's items only move forward, so the
+// search starts at its previous item's expert (e_hint): the next four prefixes are
+// read at once, and a binary search covers longer jumps.
+__device__ __forceinline__ Item decode_item(int j, const WorkList& wl, int& e_hint) {
   Item it;
   if (j < wl.n_full) {
-    int lo = 0, hi = wl.E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (wl.pref[mid] <= j) lo = mid; else hi = mid;
+    int lo = e_hint, c = 0;
+#pragma unroll
+    for (int step = 1; step <= 4; ++step) c += wl.pref[min(lo + step, wl.E)] <= j ? 1 : 0;  // pref[E] > j
+    lo += c;
+    if (c == 4) {
+      int hi = wl.E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (wl.pref[mid] <= j) lo = mid; else hi = mid;
+      }
     }
+    e_hint = lo;
     const int start = lo ? wl.end[lo - 1] : 0;
     const int cnt = wl.end[lo] - start;
     const int n_rt = cnt / kTileRows + (cnt % kTileRows > kTileRows / 2 ? 1 : 0);
@@ -519,8 +528,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ======================= weight producer (one lane) =======================
       if (lane == 0) {
         int n = 0;
+        int e_hint = 0;
         for (int j = pair; j < total; j += npairs) {
-          const Item it = decode_item(j, wl);
+          const Item it = decode_item(j, wl, e_hint);
           const int w_row = it.e * args.N + it.cb * kPairCh + (int)rank * kBM;
           for (int kb = 0; kb < nk; ++kb, ++n) {
             const int slot = n % SW;
@@ -545,8 +555,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int n = 0;
       if (!GATHER) {
         if (lane == 0) {
+          int e_hint = 0;
           for (int j = pair; j < total; j += npairs) {
-            const Item it = decode_item(j, wl);
+            const Item it = decode_item(j, wl, e_hint);
             const int y = it.row0 + (int)rank * (it.n_mma >> 1);
             for (int kb = 0; kb < nk; ++kb, ++n) {
               const int slot = n % S;
@@ -560,8 +571,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        int e_hint = 0;
         for (int j = pair; j < total; j += npairs) {
-          const Item it = decode_item(j, wl);
+          const Item it = decode_item(j, wl, e_hint);
           const int hr = it.n_mma >> 1;
           const int G = hr >> 2;
           const int r0 = it.row0 + (int)rank * hr + 4 * (lane % G), last = it.row0 + it.rows - 1;
@@ -613,8 +625,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (rank == 0 && lane == 0) {
         int n = 0, c = 0;
         bool ok = true;
+        int e_hint = 0;
         for (int j = pair; j < total && ok; j += npairs) {
-          const Item it = decode_item(j, wl);
+          const Item it = decode_item(j, wl, e_hint);
           const uint32_t idesc = kIdescBase | ((uint32_t)(it.n_mma >> 3) << 17);
           const int cs = s_chunk[it.e];
           int kc = 0;  // stage index within the current exact chunk
@@ -719,8 +732,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t accempty_remote = cluster_addr(&accempty_bar, 0);
     int c = 0;
     bool ok = true;
+    int e_hint = 0;
     for (int j = pair; j < total && ok; j += npairs) {
-      const Item it = decode_item(j, wl);
+      const Item it = decode_item(j, wl, e_hint);
       const bool active = cg * 64 < it.n_mma;
       const int cs = s_chunk[it.e];
       const int nch = (nk + cs - 1) / cs;

@@ -7,10 +7,13 @@
 namespace moe {
 
 // route_sort.cu
-size_t route_sort_workspace_bytes(int R, int E);
+// The multi-block path (more than 8192 routes) uses at most max_blocks blocks; its
+// scratch (two [blocks][E+1] int32 tables) grows with them.
+constexpr int kMaxSortBlocks = 2048;
+size_t route_sort_workspace_bytes(int R, int E, int max_blocks = kMaxSortBlocks);
 cudaError_t launch_route_sort(const int32_t* expert_idx, int R, int E, int32_t* sorted_src_route,
                               int32_t* expanded_row_idx, int32_t* tokens_per_expert, int32_t* cumsum,
-                              void* workspace, cudaStream_t stream);
+                              void* workspace, cudaStream_t stream, int max_blocks = kMaxSortBlocks);
 
 // elementwise.cu
 // Activation bounds (include/moe_layer.h): per expert, per 1024-deep segment

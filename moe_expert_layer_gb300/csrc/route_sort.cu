@@ -15,6 +15,7 @@
 // all valid routes with expandedRowIdx = -1.
 #include "common.cuh"
 #include "kernels.h"
+#include "tensor_map.h"
 
 namespace moe {
 
@@ -55,71 +56,111 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums) {
   return r;
 }
 
-// Stable scatter of routes [r0, r1) given the first free expanded row of each
-// bucket in `running` (smem, E+1 entries, advanced in place).
-// `cnt` is a [kSortWarps][pitch] byte table in smem.
-__device__ void scatter_chunk(const int32_t* expert_idx, int r0, int r1, int E, int* running,
-                              uint8_t* cnt, int pitch, int32_t* sorted_src_route,
-                              int32_t* expanded_row_idx) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  uint32_t* cnt32 = reinterpret_cast<uint32_t*>(cnt);
-  const int table_words = kSortWarps * pitch / 4;
-  for (int base = r0; base < r1; base += kSortThreads) {
-    const int r = base + threadIdx.x;
-    const bool live = r < r1;
-    const int b = live ? bucket_of(expert_idx, r, E) : -1;
-    for (int i = threadIdx.x; i < table_words; i += kSortThreads) cnt32[i] = 0u;
-    __syncthreads();
-    const unsigned same = __match_any_sync(0xffffffffu, b);
-    const int rank_in_warp = __popc(same & lt_mask);
-    if (live && rank_in_warp == 0) cnt[warp * pitch + b] = (uint8_t)__popc(same);
-    __syncthreads();
-    if (live) {
-      int pos = running[b] + rank_in_warp;
-      for (int w = 0; w < warp; ++w) pos += cnt[w * pitch + b];
-      sorted_src_route[pos] = r;
-      expanded_row_idx[r] = (b < E) ? pos : -1;
+// A block ranks up to kSortThreads * kMaxGroups routes [r0, r0 + n): warp w takes
+// the consecutive range [r0 + w*rpw, r0 + (w+1)*rpw) (rpw a multiple of 32) and
+// walks it 32 routes at a time, in order; __match_any_sync groups a step's routes by
+// bucket, and the group's first lane advances the warp's own count of that bucket
+// in `hist` (smem, [kSortWarps][pitch] uint16).  A route's rank among its range's
+// routes of the same bucket is the count before its step plus the lanes below it
+// in its group, so ranks follow route order (a stable sort) and no step needs a
+// block-wide barrier.
+constexpr int kMaxGroups = 8;
+
+__device__ __forceinline__ void warp_rank(const int (&b)[kMaxGroups], int ng, uint16_t* hist_w,
+                                          int (&rank)[kMaxGroups]) {
+  const int lane = threadIdx.x & 31;
+  const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+  for (int g = 0; g < kMaxGroups; ++g) {
+    if (g < ng) {  // warp-uniform
+      const unsigned same = __match_any_sync(0xffffffffu, b[g]);
+      const int leader = __ffs(same) - 1;
+      int before = 0;
+      if (lane == leader && b[g] >= 0) {
+        before = hist_w[b[g]];
+        hist_w[b[g]] = (uint16_t)(before + __popc(same));
+      }
+      before = __shfl_sync(0xffffffffu, before, leader);
+      rank[g] = before + __popc(same & below);
+      __syncwarp();  // the count is visible to the next step's leader
     }
-    __syncthreads();
-    for (int j = threadIdx.x; j <= E; j += kSortThreads) {
-      int add = 0;
-      for (int w = 0; w < kSortWarps; ++w) add += cnt[w * pitch + j];
-      running[j] += add;
-    }
-    __syncthreads();
   }
 }
 
-__device__ __forceinline__ int table_pitch(int E) { return ((E + 1) + 3) & ~3; }
+__device__ __forceinline__ int table_pitch(int E) { return ((E + 1) + 1) & ~1; }  // uint16 entries, even
 
-// Single-block sort for small route counts: histogram, scan and scatter in one launch.
+// Shared memory of the sort kernels: two int arrays of 1024, 32 warp sums, the
+// uint16 count table.
+__host__ __device__ inline size_t sort_smem_bytes(int E) {
+  return (1024 + 1024 + 32) * 4 + (size_t)kSortWarps * (size_t)(((E + 1) + 1) & ~1) * 2;
+}
+
+// Loads the buckets of this thread's routes (-1 past r1) and ranks them.
+__device__ __forceinline__ void load_and_rank(const int32_t* expert_idx, int r0, int r1, int E, int rpw,
+                                              uint16_t* hist, int pitch, int (&b)[kMaxGroups],
+                                              int (&rank)[kMaxGroups]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ng = rpw / 32;
+#pragma unroll
+  for (int g = 0; g < kMaxGroups; ++g) {
+    const int r = r0 + warp * rpw + g * 32 + lane;
+    b[g] = (g < ng && r < r1) ? bucket_of(expert_idx, r, E) : -1;
+  }
+  uint32_t* h32 = reinterpret_cast<uint32_t*>(hist);
+  for (int i = threadIdx.x; i < kSortWarps * pitch / 2; i += kSortThreads) h32[i] = 0u;
+  __syncthreads();
+  warp_rank(b, ng, hist + warp * pitch, rank);
+  __syncthreads();
+}
+
+// Routes per warp range for n routes in one block: a multiple of 32.
+__device__ __forceinline__ int range_per_warp(int n) { return ((n + kSortThreads - 1) / kSortThreads) * 32; }
+
+// Single-block sort for small route counts (at most kSortThreads * kMaxGroups):
+// ranking, histogram, scan and scatter in one launch.
 __global__ void __launch_bounds__(kSortThreads) route_sort_single_kernel(
     const int32_t* __restrict__ expert_idx, int R, int E, int32_t* __restrict__ sorted_src_route,
     int32_t* __restrict__ expanded_row_idx, int32_t* __restrict__ tokens_per_expert,
     int32_t* __restrict__ cumsum) {
   extern __shared__ int smem_i[];
-  int* hist = smem_i;                      // E+1
-  int* warp_sums = hist + 1024;            // 32
-  uint8_t* cnt = reinterpret_cast<uint8_t*>(warp_sums + 32);
+  int* warp_sums = smem_i + 2048;
+  uint16_t* hist = reinterpret_cast<uint16_t*>(warp_sums + 32);
   const int pitch = table_pitch(E);
-  for (int j = threadIdx.x; j < 1024; j += kSortThreads) hist[j] = 0;
-  __syncthreads();
-  for (int r = threadIdx.x; r < R; r += kSortThreads) atomicAdd(&hist[bucket_of(expert_idx, r, E)], 1);
-  __syncthreads();
+  const int rpw = range_per_warp(R);
+  int b[kMaxGroups], rank[kMaxGroups];
+  load_and_rank(expert_idx, 0, R, E, rpw, hist, pitch, b, rank);
+  // bucket totals, their exclusive scan, and each warp's first row in every bucket
   const int j = threadIdx.x;
-  const int total = (j <= E) ? hist[j] : 0;
+  int total = 0;
+  if (j <= E)
+    for (int w = 0; w < kSortWarps; ++w) total += hist[w * pitch + j];
   const int start = block_exclusive_scan(total, warp_sums);
   if (j < E) {
     tokens_per_expert[j] = total;
     cumsum[j] = start + total;
   }
-  // hist becomes the running insertion point of each bucket
-  if (j <= E) hist[j] = start;
+  if (j <= E) {
+    int run = start;  // <= R <= 8192: fits the table
+    for (int w = 0; w < kSortWarps; ++w) {
+      const int c = hist[w * pitch + j];
+      hist[w * pitch + j] = (uint16_t)run;
+      run += c;
+    }
+  }
   __syncthreads();
-  scatter_chunk(expert_idx, 0, R, E, hist, cnt, pitch, sorted_src_route, expanded_row_idx);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int g = 0; g < kMaxGroups; ++g) {
+    if (b[g] >= 0) {
+      const int r = warp * rpw + g * 32 + lane;
+      const int pos = hist[warp * pitch + b[g]] + rank[g];
+      sorted_src_route[pos] = r;
+      expanded_row_idx[r] = (b[g] < E) ? pos : -1;
+    }
+  }
 }
 
+// Multi-block sort: `chunk` routes per block (at most kSortThreads * kMaxGroups).
 __global__ void __launch_bounds__(kSortThreads) route_hist_kernel(const int32_t* __restrict__ expert_idx,
                                                                   int R, int E, int chunk,
                                                                   int32_t* __restrict__ block_hist) {
@@ -161,45 +202,82 @@ __global__ void __launch_bounds__(kSortThreads) route_scatter_kernel(
     const int32_t* __restrict__ expert_idx, int R, int E, int chunk, const int32_t* __restrict__ block_off,
     int32_t* __restrict__ sorted_src_route, int32_t* __restrict__ expanded_row_idx) {
   extern __shared__ int smem_i[];
-  int* running = smem_i;  // E+1 (padded to 1024)
-  uint8_t* cnt = reinterpret_cast<uint8_t*>(running + 1024);
-  for (int j = threadIdx.x; j <= E; j += kSortThreads) running[j] = block_off[blockIdx.x * (E + 1) + j];
-  __syncthreads();
+  int* base = smem_i;  // this block's first expanded row of each bucket
+  uint16_t* hist = reinterpret_cast<uint16_t*>(smem_i + 2048 + 32);
+  const int pitch = table_pitch(E);
   const int r0 = blockIdx.x * chunk, r1 = min(R, r0 + chunk);
-  scatter_chunk(expert_idx, r0, r1, E, running, cnt, table_pitch(E), sorted_src_route, expanded_row_idx);
+  for (int j = threadIdx.x; j <= E; j += kSortThreads) base[j] = block_off[blockIdx.x * (E + 1) + j];
+  const int rpw = range_per_warp(chunk);
+  int b[kMaxGroups], rank[kMaxGroups];
+  load_and_rank(expert_idx, r0, r1, E, rpw, hist, pitch, b, rank);
+  // each warp's offset within the block's routes of every bucket
+  for (int j = threadIdx.x; j <= E; j += kSortThreads) {
+    int run = 0;
+    for (int w = 0; w < kSortWarps; ++w) {
+      const int c = hist[w * pitch + j];
+      hist[w * pitch + j] = (uint16_t)run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int g = 0; g < kMaxGroups; ++g) {
+    if (b[g] >= 0) {
+      const int r = r0 + warp * rpw + g * 32 + lane;
+      const int pos = base[b[g]] + hist[warp * pitch + b[g]] + rank[g];
+      sorted_src_route[pos] = r;
+      expanded_row_idx[r] = (b[g] < E) ? pos : -1;
+    }
+  }
 }
 
-constexpr int kSingleBlockMaxRoutes = 8192;
-constexpr int kMultiBlockChunk = 8192;
+constexpr int kSingleBlockMaxRoutes = kSortThreads * kMaxGroups;
 
-size_t smem_single(int E) { return 1024 * 4 + 32 * 4 + (size_t)kSortWarps * (((E + 1) + 3) & ~3); }
-size_t smem_scatter(int E) { return 1024 * 4 + (size_t)kSortWarps * (((E + 1) + 3) & ~3); }
+// Routes per block of the multi-block path: one pass of kSortThreads while that
+// needs at most max_blocks blocks, more passes per block beyond.
+int sort_chunk(int R, int max_blocks) {
+  const int passes = (R + kSortThreads * max_blocks - 1) / (kSortThreads * max_blocks);
+  return kSortThreads * (passes < 1 ? 1 : passes);
+}
 
 }  // namespace
 
-size_t route_sort_workspace_bytes(int R, int E) {
+size_t route_sort_workspace_bytes(int R, int E, int max_blocks) {
   if (R <= kSingleBlockMaxRoutes) return 0;
-  const size_t nb = (size_t)((R + kMultiBlockChunk - 1) / kMultiBlockChunk);
+  const int chunk = sort_chunk(R, max_blocks);
+  const size_t nb = (size_t)((R + chunk - 1) / chunk);
   return 2 * nb * (size_t)(E + 1) * sizeof(int32_t);
 }
 
 cudaError_t launch_route_sort(const int32_t* expert_idx, int R, int E, int32_t* sorted_src_route,
                               int32_t* expanded_row_idx, int32_t* tokens_per_expert, int32_t* cumsum,
-                              void* workspace, cudaStream_t stream) {
+                              void* workspace, cudaStream_t stream, int max_blocks) {
+  const size_t smem = sort_smem_bytes(E);  // 74 KB at E = 1023
+  static bool attr_set[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!attr_set[dev]) {
+    const int most = (int)sort_smem_bytes(1023);
+    cudaError_t e = cudaFuncSetAttribute(route_sort_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
   if (R <= kSingleBlockMaxRoutes) {
-    route_sort_single_kernel<<<1, kSortThreads, smem_single(E), stream>>>(
-        expert_idx, R, E, sorted_src_route, expanded_row_idx, tokens_per_expert, cumsum);
+    route_sort_single_kernel<<<1, kSortThreads, smem, stream>>>(expert_idx, R, E, sorted_src_route,
+                                                                expanded_row_idx, tokens_per_expert, cumsum);
     return cudaGetLastError();
   }
-  const int nb = (R + kMultiBlockChunk - 1) / kMultiBlockChunk;
+  const int chunk = sort_chunk(R, max_blocks);
+  if (chunk > kSingleBlockMaxRoutes) return cudaErrorInvalidValue;  // R >= 2^24 or too few blocks
+  const int nb = (R + chunk - 1) / chunk;
   int32_t* block_hist = static_cast<int32_t*>(workspace);
   int32_t* block_off = block_hist + (size_t)nb * (E + 1);
-  route_hist_kernel<<<nb, kSortThreads, (size_t)(E + 1) * 4, stream>>>(expert_idx, R, E, kMultiBlockChunk,
-                                                                       block_hist);
+  route_hist_kernel<<<nb, kSortThreads, (size_t)(E + 1) * 4, stream>>>(expert_idx, R, E, chunk, block_hist);
   route_scan_kernel<<<1, kSortThreads, 0, stream>>>(block_hist, nb, E, tokens_per_expert, cumsum, block_off);
-  route_scatter_kernel<<<nb, kSortThreads, smem_scatter(E), stream>>>(expert_idx, R, E, kMultiBlockChunk,
-                                                                      block_off, sorted_src_route,
-                                                                      expanded_row_idx);
+  route_scatter_kernel<<<nb, kSortThreads, smem, stream>>>(expert_idx, R, E, chunk, block_off, sorted_src_route,
+                                                           expanded_row_idx);
   return cudaGetLastError();
 }
 

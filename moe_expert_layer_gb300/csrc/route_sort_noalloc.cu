@@ -22,9 +22,10 @@
 
 namespace {
 
-// Multi-block path: 8192 routes per block, E + 1 <= 1024 buckets, two tables.
-constexpr int kRoutesPerBlock = 8192;
-constexpr int kMaxBlocks = MOE_ROUTE_SORT_NOALLOC_MAX_ROUTES / kRoutesPerBlock;
+// Multi-block path: at most kMaxBlocks blocks (8192 routes each at the largest R),
+// E + 1 <= 1024 buckets, two tables.
+constexpr int kMaxBlocks = 64;
+static_assert(MOE_ROUTE_SORT_NOALLOC_MAX_ROUTES <= kMaxBlocks * 8192, "blocks of the largest sort");
 constexpr size_t kScratchInts = 2u * kMaxBlocks * 1024u;  // 128 Ki int32 = 512 KiB
 
 static __device__ __align__(256) int32_t g_route_sort_scratch[kScratchInts];
@@ -71,6 +72,7 @@ extern "C" int32_t moe_route_sort_noalloc(const moe_dims_t* d, const int32_t* ex
   // The kernels write every scratch entry they later read (histogram, then
   // offsets), so the previous call's contents need no clearing.
   const cudaError_t e = moe::launch_route_sort(expert_idx, (int)R, d->E, sorted_src_route, expanded_row_idx,
-                                               tokens_per_expert, cumsum, scratch, static_cast<cudaStream_t>(stream));
+                                               tokens_per_expert, cumsum, scratch, static_cast<cudaStream_t>(stream),
+                                               kMaxBlocks);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
