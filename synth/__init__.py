@@ -17,11 +17,15 @@ mid         512   7168   2048  256     8  biased      2
 skewed     2048   7168   2048  256     8  zipf1.2     3
 prefill    8192   4096   1408   64     6  uniform     4
 decode16      8   7168   2048   16     8  uniform     5
+mid16       512   7168   2048   16     8  biased      6
+midrows16    32   7168   2048   16     8  biased      7
 ========  =====  =====  =====  ===  ====  =======  ====
 
 ``decode16`` keeps decode's shapes and rows per expert (about 4) with 16
 experts, so that its weights (0.7 GB) stay above the L2 size while a
-counter capture of one GEMM launch remains small.
+counter capture of one GEMM launch remains small.  ``mid16`` keeps mid's
+token count (the quant and combine shapes) and ``midrows16`` mid's rows per
+expert (about 16, the 32-row warp-MMA tiles), both with 16 experts.
 
 x is binary16 N(0,1); w1/w2 are int8 uniform over [-127, 127]; s1/s2 are
 fp32 uniform on [1e-3, 1e-2).  Weight layout: w1[E][2I][K] and w2[E][K][I]
@@ -70,6 +74,7 @@ CONFIGS = {
     "prefill": Workload("prefill", 8192, 4096, 1408, 64, 6, "uniform", 4),
     "decode16": Workload("decode16", 8, 7168, 2048, 16, 8, "uniform", 5),
     "mid16": Workload("mid16", 512, 7168, 2048, 16, 8, "biased", 6),
+    "midrows16": Workload("midrows16", 32, 7168, 2048, 16, 8, "biased", 7),
 }
 
 
