@@ -2,8 +2,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode] [--impl reference]
 
-One step = one pass of the whole layer (route sort, token quant with the scatter
-to expert-major rows, GMM1, SwiGLU + requant, GMM2, Combine + Unpermute) over one
+One step = one pass of the whole layer (FrontReorder: route sort and token quant
+with the scatter to expert-major rows, GMM1, SwiGLU + requant, GMM2, Combine + Unpermute) over one
 batch of the workload's seeded synthetic inputs.  With N > 1 (torchrun, one process per GPU)
 every rank runs an independent replica of the layer on its own batch: the path
 has no exchange step, so there is no collective on the data path (weak scaling).
@@ -69,8 +69,9 @@ def algorithmic(w, expert_idx):
     active = int(np.unique(expert_idx[(expert_idx >= 0) & (expert_idx < w.E)]).size)
     K, I, M = w.K, w.I, w.M
     st = {}
-    st["route_sort"] = {"bytes": 4 * R + 8 * R + 8 * w.E}
-    st["quant"] = {"bytes": 2 * M * K + 2 * R * K + 4 * M}  # read x, write the expert-major codes
+    # FrontReorder: the route sort (expert ids in, two route tables and the counts out)
+    # and the token quant with the scatter (read x, write the expert-major codes)
+    st["front_reorder"] = {"bytes": 4 * R + 8 * R + 8 * w.E + 2 * M * K + 2 * R * K + 4 * M}
     st["gmm1"] = {"bytes": active * 2 * I * K + active * 2 * I * 4 + R * K * 2 + R * 2 * I * 2,
                   "ops": 2 * R * K * 2 * I}
     st["swiglu"] = {"bytes": R * 2 * I * 2 + R * I * 2 + 8 * R}
@@ -291,29 +292,28 @@ def main():
     c2 = torch.empty((R, w.K), dtype=f16, device="cuda")
     gws = torch.empty(moe.moe_gmm_workspace_size(d), dtype=torch.uint8, device="cuda")
     bounds = torch.zeros((2, w.E, moe.BOUND_SEGMENTS), dtype=i32, device="cuda")  # activation bounds of a1, q2
-    names = ["route_sort", "quant", "gmm1", "swiglu", "gmm2", "combine"]
+    names = ["front_reorder", "gmm1", "swiglu", "gmm2", "combine"]
 
     def stages(evs):
         with torch.cuda.stream(stream):
             bounds.zero_()  # the layer clears them with its status word
         evs[0].record(stream)
-        moe.moe_route_sort(d, dev["expert_idx"], sorted_, expanded, tpe, cs, sws, stream)
+        moe.moe_front_reorder(d, dev["x"], dev["expert_idx"], sorted_, expanded, tpe, cs, a1, pts1, bounds[0], sws,
+                              stream)
         evs[1].record(stream)
-        moe.moe_quant_dispatch(d, dev["x"], dev["expert_idx"], expanded, a1, pts1, bounds[0], stream)
-        evs[2].record(stream)
         moe.moe_gmm1(d, a1, None, cs, bounds[0], dev["w1"], dev["s1"], c1, gws, stream)
-        evs[3].record(stream)
+        evs[2].record(stream)
         moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, dev["expert_idx"], None, q2, pts2, bounds[1], stream)
-        evs[4].record(stream)
+        evs[3].record(stream)
         moe.moe_gmm2(d, q2, cs, bounds[1], dev["w2"], dev["s2"], c2, gws, stream)
-        evs[5].record(stream)
+        evs[4].record(stream)
         moe.moe_combine_unpermute(d, c2, pts2, expanded, dev["probs"], out, stream)
-        evs[6].record(stream)
+        evs[5].record(stream)
 
     for _ in range(3):
-        stages([torch.cuda.Event(enable_timing=True) for _ in range(7)])
+        stages([torch.cuda.Event(enable_timing=True) for _ in range(6)])
     n_stage_steps = max(3, min(args.steps, 50))
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_stage_steps)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_stage_steps)]
     barrier()
     for i in range(n_stage_steps):
         flush.fill_(i & 0xff)
@@ -404,7 +404,12 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(w, inp)
 
-    launches_per_step = (1 if w.R <= 8192 else 3) + 5
+    # our kernels per layer call: the sort (fused into the quant kernel up to 4096
+    # routes, one kernel up to 8192, three above), the quant, each GEMM (one engine up
+    # to 24 rows per expert on average, both above), SwiGLU, combine
+    sort_launches = 0 if w.R <= 4096 else (1 if w.R <= 8192 else 3)
+    gemm_launches = 1 if w.R / w.E <= 24.0 else 2
+    launches_per_step = sort_launches + 1 + 2 * gemm_launches + 2
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),

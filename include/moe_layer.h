@@ -221,6 +221,21 @@ int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t
                            const int32_t* expanded_row_idx, uint16_t* a1_f16, float* pts1, int32_t* a1_bounds,
                            void* stream);
 
+/*
+ * FrontReorder in one call (page section "1. FrontReorder", phases 1-2c and 4, with
+ * "2. Dispatch"): exactly moe_route_sort followed by moe_quant_dispatch, with the
+ * same outputs.  Up to 4096 routes no sort kernel runs: each token's quant CTA
+ * counts all routes' expert ids itself and places its own routes (one launch
+ * instead of two); above that the route-sort kernels run first.
+ *   workspace: moe_route_sort_workspace_size(d) bytes (0 up to 8192 routes)
+ *   other arguments as for moe_route_sort and moe_quant_dispatch
+ *   (expert_idx is read in any case; a1_bounds may be NULL)
+ */
+int32_t moe_front_reorder(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx,
+                          int32_t* sorted_src_route, int32_t* expanded_row_idx, int32_t* tokens_per_expert,
+                          int32_t* cumsum, uint16_t* a1_f16, float* pts1, int32_t* a1_bounds, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Workspace bytes of moe_gmm1 / moe_gmm2 (status word). */
 size_t moe_gmm_workspace_size(const moe_dims_t* d);
 

@@ -24,8 +24,8 @@ EXPORTS = [
     "moe_status_string", "moe_layer_workspace_size", "moe_layer_fwd",
     "moe_layer_host_workspace_size", "moe_layer_fwd_host", "moe_workspace_status",
     "moe_workspace_clear_status", "moe_route_sort_workspace_size", "moe_route_sort",
-    "moe_quant_tokens", "moe_quant_dispatch", "moe_gmm_workspace_size", "moe_gmm1", "moe_swiglu_quant", "moe_gmm2",
-    "moe_combine_unpermute", "moe_route_sort_noalloc", "moe_selftest_wait_timeout",
+    "moe_quant_tokens", "moe_quant_dispatch", "moe_front_reorder", "moe_gmm_workspace_size", "moe_gmm1",
+    "moe_swiglu_quant", "moe_gmm2", "moe_combine_unpermute", "moe_route_sort_noalloc", "moe_selftest_wait_timeout",
 ]
 
 
@@ -71,6 +71,7 @@ def load_library(path=None):
         "moe_quant_tokens": ([D] + [vp] * 7, i32),
         "moe_gmm_workspace_size": ([D], sz),
         "moe_quant_dispatch": ([D] + [vp] * 7, i32),
+        "moe_front_reorder": ([D] + [vp] * 10 + [sz, vp], i32),
         "moe_gmm1": ([D] + [vp] * 8 + [sz, vp], i32),
         "moe_swiglu_quant": ([D] + [vp] * 10, i32),
         "moe_gmm2": ([D] + [vp] * 7 + [sz, vp], i32),
@@ -168,6 +169,14 @@ def moe_quant_dispatch(d, x, expert_idx, expanded_row_idx, a1_f16, pts1, a1_boun
     _check("moe_quant_dispatch", load_library().moe_quant_dispatch(
         ctypes.byref(d), _p(x), _p(expert_idx), _p(expanded_row_idx), _p(a1_f16), _p(pts1), _p(a1_bounds),
         _stream(stream)))
+
+
+def moe_front_reorder(d, x, expert_idx, sorted_src_route, expanded_row_idx, tokens_per_expert, cumsum, a1_f16,
+                      pts1, a1_bounds, workspace=None, stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("moe_front_reorder", load_library().moe_front_reorder(
+        ctypes.byref(d), _p(x), _p(expert_idx), _p(sorted_src_route), _p(expanded_row_idx), _p(tokens_per_expert),
+        _p(cumsum), _p(a1_f16), _p(pts1), _p(a1_bounds), _p(workspace), nbytes, _stream(stream)))
 
 
 def moe_gmm1(d, a1_f16, sorted_src_route, cumsum, a1_bounds, w1, s1, c1, workspace, stream=None):

@@ -54,7 +54,44 @@ __device__ __forceinline__ uint32_t codes_to_half2(int q0, int q1) {
 // expert-major GMM1 operand (FrontReorder's quant-scatter into offsetA).
 // With `bounds` set, the token's sum of |code| over each 1024-deep segment of k is
 // folded (atomic max) into bounds[e][segment] of every expert e it is routed to.
-template <int VPT>
+//
+// SORT (the fused FrontReorder, R <= kFusedSortRoutes): the kernel also sorts the
+// routes, without a kernel of its own.  Every CTA reads all R expert ids, counts the
+// routes of each bucket (bucket E: invalid ids) and those that come before its own
+// token's routes, and scans the counts: a route's expanded row is its bucket's start
+// plus the number of earlier routes in the bucket (the stable order the sort
+// defines).  Each CTA writes sorted_src_route and expanded_row_idx for its own
+// routes; CTA 0 writes tokens_per_expert and cumsum.
+constexpr int kFusedSortRoutes = 4096;
+
+// Exclusive scan over the block of one value per thread (blockDim a multiple of 32).
+__device__ __forceinline__ int block_scan_excl(int v, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? warp_sums[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < nw) warp_sums[lane] = wi - w;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+template <int VPT, bool SORT>
 __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half* __restrict__ x, int K,
                                                                    int8_t* __restrict__ xq_i8,
                                                                    __half* __restrict__ xq_f16,
@@ -62,20 +99,78 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
                                                                    const int32_t* __restrict__ expanded_row_idx,
                                                                    int topK, __half* __restrict__ a1,
                                                                    const int32_t* __restrict__ expert_idx, int E,
-                                                                   int32_t* __restrict__ bounds) {
+                                                                   int32_t* __restrict__ bounds, int R,
+                                                                   int32_t* __restrict__ sorted_src_route,
+                                                                   int32_t* __restrict__ expanded_out,
+                                                                   int32_t* __restrict__ tokens_per_expert,
+                                                                   int32_t* __restrict__ cumsum) {
   __shared__ float red[kRowThreads / 32];
   __shared__ int s_l1[kBoundSegments];
+  __shared__ int s_pos[SORT ? 1024 : 1];  // expanded row of each of the token's routes (-1: invalid)
   if (threadIdx.x < kBoundSegments) s_l1[threadIdx.x] = 0;  // visible after the row-max barriers
   const int t = blockIdx.x;
   const int nvec = K >> 3;
   const int4* row = reinterpret_cast<const int4*>(x + (size_t)t * K);
   Vec8h v[VPT];
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int idx = threadIdx.x + i * (int)blockDim.x;
+    if (idx < nvec) v[i].v = __ldg(row + idx);
+  }
+  if constexpr (SORT) {
+    // the row loads above are in flight while the routes are counted
+    __shared__ int s_cnt[1024], s_before[1024], s_ws[32];
+    const int nb = E + 1;
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+      s_cnt[b] = 0;
+      s_before[b] = 0;
+    }
+    __syncthreads();
+    const int first = t * topK;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+      const int e = __ldg(expert_idx + r);
+      const int b = (e >= 0 && e < E) ? e : E;
+      atomicAdd(&s_cnt[b], 1);
+      if (r < first) atomicAdd(&s_before[b], 1);
+    }
+    __syncthreads();
+    // exclusive scan of the bucket counts: thread i owns buckets [i*per, i*per + per)
+    const int per = (nb + blockDim.x - 1) / blockDim.x;
+    const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) local += s_cnt[b];
+    int run = block_scan_excl(local, s_ws);
+    for (int b = b0; b < b1; ++b) {
+      const int c = s_cnt[b];
+      if (t == 0 && b < E) {
+        tokens_per_expert[b] = c;
+        cumsum[b] = run + c;
+      }
+      s_before[b] += run;  // first expanded row of this token's routes in bucket b
+      run += c;
+    }
+    __syncthreads();
+    for (int sl = threadIdx.x; sl < topK; sl += blockDim.x) {
+      const int r = first + sl;
+      const int e = __ldg(expert_idx + r);
+      const int b = (e >= 0 && e < E) ? e : E;
+      int pos = s_before[b];
+      for (int s2 = 0; s2 < sl; ++s2) {  // this token's earlier routes in the same bucket
+        const int e2 = __ldg(expert_idx + first + s2);
+        pos += ((e2 >= 0 && e2 < E) ? e2 : E) == b ? 1 : 0;
+      }
+      sorted_src_route[pos] = r;
+      const int d = b < E ? pos : -1;
+      expanded_out[r] = d;
+      s_pos[sl] = d;
+    }
+    __syncthreads();
+  }
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * (int)blockDim.x;
     if (idx < nvec) {
-      v[i].v = __ldg(row + idx);
 #pragma unroll
       for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(__half2float(v[i].h[j])));
     }
@@ -105,14 +200,19 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
                    ((uint32_t)(q[7] & 0xff) << 24);
         reinterpret_cast<uint2*>(xq_i8 + (size_t)t * K)[idx] = packed;
       }
-      if (xq_f16 || expanded_row_idx) {
+      if (SORT || xq_f16 || expanded_row_idx) {
         int4 o;
         o.x = (int)codes_to_half2(q[0], q[1]);
         o.y = (int)codes_to_half2(q[2], q[3]);
         o.z = (int)codes_to_half2(q[4], q[5]);
         o.w = (int)codes_to_half2(q[6], q[7]);
         if (xq_f16) reinterpret_cast<int4*>(xq_f16 + (size_t)t * K)[idx] = o;
-        if (expanded_row_idx) {
+        if (SORT) {
+          for (int s = 0; s < topK; ++s) {
+            const int d = s_pos[s];
+            if (d >= 0) reinterpret_cast<int4*>(a1 + (size_t)d * K)[idx] = o;
+          }
+        } else if (expanded_row_idx) {
           for (int s = 0; s < topK; ++s) {
             const int d = __ldg(expanded_row_idx + (size_t)t * topK + s);
             if (d >= 0) reinterpret_cast<int4*>(a1 + (size_t)d * K)[idx] = o;
@@ -317,30 +417,61 @@ int row_threads(int nvec, int vpt) {
 
 }  // namespace
 
-cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16, float* pts1,
-                                const int32_t* expanded_row_idx, int topK, uint16_t* a1, const int32_t* expert_idx,
-                                int E, int32_t* bounds, cudaStream_t stream) {
+namespace {
+
+// One CTA per token, a 16-byte vector per thread and VPT vectors per thread at most.
+template <bool SORT>
+cudaError_t launch_quant(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16, float* pts1,
+                         const int32_t* expanded_row_idx, int topK, uint16_t* a1, const int32_t* expert_idx, int E,
+                         int32_t* bounds, int32_t* sorted_src_route, int32_t* expanded_out,
+                         int32_t* tokens_per_expert, int32_t* cumsum, cudaStream_t stream) {
   const int nvec = K / 8;
   const int vpt = (nvec + kRowThreads - 1) / kRowThreads;
   const int threads = row_threads(nvec, vpt);
   const __half* xh = reinterpret_cast<const __half*>(x);
   __half* qf = reinterpret_cast<__half*>(xq_f16);
   __half* ah = reinterpret_cast<__half*>(a1);
+  const int R = M * topK;
+#define MOE_QUANT(V)                                                                                            \
+  quant_tokens_kernel<V, SORT><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,  \
+                                                          expert_idx, E, bounds, R, sorted_src_route,          \
+                                                          expanded_out, tokens_per_expert, cumsum)
   if (vpt <= 1)
-    quant_tokens_kernel<1><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,
-                                                        expert_idx, E, bounds);
+    MOE_QUANT(1);
   else if (vpt <= 2)
-    quant_tokens_kernel<2><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,
-                                                        expert_idx, E, bounds);
+    MOE_QUANT(2);
   else if (vpt <= 4)
-    quant_tokens_kernel<4><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,
-                                                        expert_idx, E, bounds);
+    MOE_QUANT(4);
   else if (vpt <= 8)
-    quant_tokens_kernel<8><<<M, threads, 0, stream>>>(xh, K, xq_i8, qf, pts1, expanded_row_idx, topK, ah,
-                                                        expert_idx, E, bounds);
+    MOE_QUANT(8);
   else
     return cudaErrorInvalidValue;
+#undef MOE_QUANT
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16, float* pts1,
+                                const int32_t* expanded_row_idx, int topK, uint16_t* a1, const int32_t* expert_idx,
+                                int E, int32_t* bounds, cudaStream_t stream) {
+  return launch_quant<false>(x, M, K, xq_i8, xq_f16, pts1, expanded_row_idx, topK, a1, expert_idx, E, bounds,
+                             nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+cudaError_t launch_front_reorder(const uint16_t* x, int M, int K, const int32_t* expert_idx, int topK, int E,
+                                 int32_t* sorted_src_route, int32_t* expanded_row_idx, int32_t* tokens_per_expert,
+                                 int32_t* cumsum, uint16_t* a1, float* pts1, int32_t* bounds, void* sort_workspace,
+                                 cudaStream_t stream) {
+  const int R = M * topK;
+  if (R <= kFusedSortRoutes)
+    return launch_quant<true>(x, M, K, nullptr, nullptr, pts1, nullptr, topK, a1, expert_idx, E, bounds,
+                              sorted_src_route, expanded_row_idx, tokens_per_expert, cumsum, stream);
+  cudaError_t e = launch_route_sort(expert_idx, R, E, sorted_src_route, expanded_row_idx, tokens_per_expert, cumsum,
+                                    sort_workspace, stream);
+  if (e != cudaSuccess) return e;
+  return launch_quant<false>(x, M, K, nullptr, nullptr, pts1, expanded_row_idx, topK, a1, expert_idx, E, bounds,
+                             nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int topK, const float* pts1,

@@ -22,6 +22,13 @@ constexpr int kBoundSegments = 16;
 cudaError_t launch_quant_tokens(const uint16_t* x, int M, int K, int8_t* xq_i8, uint16_t* xq_f16,
                                 float* pts1, const int32_t* expanded_row_idx, int topK, uint16_t* a1,
                                 const int32_t* expert_idx, int E, int32_t* bounds, cudaStream_t stream);
+// FrontReorder in one call: the route sort and the quant-scatter.  Up to 4096 routes
+// the sort runs inside the quant kernel (each token's CTA counts all routes itself);
+// above, the route-sort kernels run first (sort_workspace: route_sort_workspace_bytes).
+cudaError_t launch_front_reorder(const uint16_t* x, int M, int K, const int32_t* expert_idx, int topK, int E,
+                                 int32_t* sorted_src_route, int32_t* expanded_row_idx, int32_t* tokens_per_expert,
+                                 int32_t* cumsum, uint16_t* a1, float* pts1, int32_t* bounds, void* sort_workspace,
+                                 cudaStream_t stream);
 cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int topK, const float* pts1,
                                 const int32_t* sorted_src_route, const int32_t* cumsum, int8_t* q2_i8,
                                 uint16_t* q2_f16, float* pts2, const int32_t* expert_idx, int32_t* bounds,

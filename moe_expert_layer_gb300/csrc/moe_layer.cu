@@ -111,14 +111,11 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   cudaError_t e;
   if ((e = cudaMemsetAsync(status, 0, L.bounds2 + (size_t)E * moe::kBoundSegments * 4, st)) != cudaSuccess)
     return launch_status(e);
-  if ((e = moe::launch_route_sort(expert_idx, R, E, sorted, expanded, tpe, cumsum, at<void>(ws, L.sort_ws), st)) !=
-      cudaSuccess)
-    return launch_status(e);
-  // quantise each token once and scatter its codes to its expert-major rows (a TMA
-  // gather of token rows inside GMM1 measured 1.2-3.2x slower GMM1 on GB300: one
-  // gather4 moves 512 B, a tiled box up to 16 KB)
-  if ((e = moe::launch_quant_tokens(x, M, K, nullptr, nullptr, pts1, expanded, topK, a1, expert_idx, E, bounds1,
-                                    st)) != cudaSuccess)
+  // FrontReorder: sort the routes, quantise each token once and scatter its codes to
+  // its expert-major rows (a TMA gather of token rows inside GMM1 measured 1.2-3.2x
+  // slower GMM1 on GB300: one gather4 moves 512 B, a tiled box up to 16 KB)
+  if ((e = moe::launch_front_reorder(x, M, K, expert_idx, topK, E, sorted, expanded, tpe, cumsum, a1, pts1, bounds1,
+                                     at<void>(ws, L.sort_ws), st)) != cudaSuccess)
     return launch_status(e);
 
   moe::GroupedGemmProblem g1{};
@@ -290,6 +287,24 @@ int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t
   return launch_status(moe::launch_quant_tokens(x, d->M, d->K, nullptr, nullptr, pts1, expanded_row_idx, d->topK,
                                                 a1_f16, expert_idx, d->E, a1_bounds,
                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_front_reorder(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx,
+                          int32_t* sorted_src_route, int32_t* expanded_row_idx, int32_t* tokens_per_expert,
+                          int32_t* cumsum, uint16_t* a1_f16, float* pts1, int32_t* a1_bounds, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!x || !expert_idx || !sorted_src_route || !expanded_row_idx || !tokens_per_expert || !cumsum || !a1_f16 ||
+      !pts1)
+    return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(a1_f16)) return MOE_ERR_ALIGN;
+  const size_t need = moe::route_sort_workspace_bytes(d->M * d->topK, d->E);
+  if (need && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  return launch_status(moe::launch_front_reorder(x, d->M, d->K, expert_idx, d->topK, d->E, sorted_src_route,
+                                                 expanded_row_idx, tokens_per_expert, cumsum, a1_f16, pts1, a1_bounds,
+                                                 workspace, static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_gmm_workspace_size(const moe_dims_t* d) {

@@ -63,6 +63,8 @@ def test_entry_points_reject_before_touching_the_device(lib):
     assert lib.moe_quant_tokens(ctypes.byref(d), *([None] * 7)) == -1
     assert lib.moe_gmm1(ctypes.byref(bad), *([None] * 8), 0, None) == -2
     assert lib.moe_quant_dispatch(ctypes.byref(d), *([None] * 7)) == -1
+    assert lib.moe_front_reorder(ctypes.byref(d), *([None] * 10), 0, None) == -1
+    assert lib.moe_front_reorder(ctypes.byref(bad), *([None] * 10), 0, None) == -2
     assert lib.moe_status_string(-5) == b"workspace missing or too small"
     # misaligned pointers -> MOE_ERR_ALIGN
     p = 4096 + 2

@@ -112,6 +112,54 @@ def test_quant_dispatch_bit_exact(cfg):
     assert_bits_equal(host(pts), pts_ref, "pts1")
 
 
+FRONT_CASES = [
+    ("tiny", None), ("decode", None), ("mid", None),
+    ("r4096", synth.Workload("r4096", 1024, 256, 64, 64, 4, "zipf", 31)),      # the largest fused sort
+    ("r4100", synth.Workload("r4100", 1025, 256, 64, 64, 4, "zipf", 32)),      # the route-sort kernels first
+    ("skewed", None),
+    ("e1023", synth.Workload("e1023", 300, 128, 64, 1023, 8, "biased", 33)),
+    ("topk64", synth.Workload("topk64", 40, 128, 64, 96, 64, "uniform", 34)),  # more routes than threads
+    ("m1", synth.Workload("m1", 1, 384, 64, 4, 3, "uniform", 35)),
+]
+
+
+@pytest.mark.parametrize("name,w", FRONT_CASES, ids=[c[0] for c in FRONT_CASES])
+def test_front_reorder_bit_exact(name, w):
+    """FrontReorder in one call equals the sort and the quant-scatter done apart: the
+    same route tables, codes, scales and activation bounds, bit for bit (invalid
+    routes and an expert repeated within a token included)."""
+    w = w or synth.CONFIGS[name]
+    x = synth.normal_f16(w.seed, 1, (w.M, w.K))
+    ei, _ = synth.routing(w.seed, w.M, w.E, w.topK, w.routing)
+    ei[0, 0] = -1          # invalid routes: sorted last, no row written
+    if w.M > 2:
+        ei[2, -1] = w.E + 5
+    if w.topK > 1:
+        ei[-1, 1] = ei[-1, 0]  # the same expert twice in one token: slot order decides
+    ref = oracle.route_sort(ei, w.E)
+    xq_ref, pts_ref = oracle.quant_tokens(x)
+    Rv = w.R - ref["invalid"]
+    a1_ref = xq_ref[ref["sorted_src_route"][:Rv] // w.topK]
+    d = _dims(w)
+    s, xr = empty(w.R, torch.int32), empty(w.R, torch.int32)
+    tpe, cs = empty(w.E, torch.int32), empty(w.E, torch.int32)
+    ws = empty(max(16, moe.moe_route_sort_workspace_size(d)), torch.uint8)
+    a1 = torch.full((w.R, w.K), 7.0, dtype=torch.float16, device="cuda")
+    pts = empty(w.M, torch.float32)
+    bounds = torch.zeros((w.E, moe.BOUND_SEGMENTS), dtype=torch.int32, device="cuda")
+    moe.moe_front_reorder(d, dev(x), dev(ei), s, xr, tpe, cs, a1, pts, bounds, ws)
+    torch.cuda.synchronize()
+    assert_bits_equal(host(s), ref["sorted_src_route"], "sorted_src_route")
+    assert_bits_equal(host(xr), ref["expanded_row_idx"], "expanded_row_idx")
+    assert_bits_equal(host(tpe), ref["tokens_per_expert"], "tokens_per_expert")
+    assert_bits_equal(host(cs), ref["cumsum"], "cumsum")
+    got = host(a1)
+    assert_bits_equal(got[:Rv], a1_ref.astype(np.float16), "a1")
+    assert np.all(got[Rv:].astype(np.float32) == 7.0)
+    assert_bits_equal(host(pts), pts_ref, "pts1")
+    assert_bits_equal(host(bounds), _bounds_ref(a1_ref, ref["cumsum"], w.E), "a1 bounds")
+
+
 def _bounds_ref(codes, cumsum, E):
     """Per-expert, per-1024-deep-segment maxima of sum |code| over the expert's rows."""
     S = moe.BOUND_SEGMENTS
