@@ -70,8 +70,11 @@ def algorithmic(w, expert_idx):
     K, I, M = w.K, w.I, w.M
     st = {}
     # FrontReorder: the route sort (expert ids in, two route tables and the counts out)
-    # and the token quant with the scatter (read x, write the expert-major codes)
-    st["front_reorder"] = {"bytes": 4 * R + 8 * R + 8 * w.E + 2 * M * K + 2 * R * K + 4 * M}
+    # and the token quant with the scatter (read x, write the expert-major codes); one
+    # kernel up to 4096 routes, where the stage is timed whole
+    st["route_sort"] = {"bytes": 4 * R + 8 * R + 8 * w.E}
+    st["quant"] = {"bytes": 2 * M * K + 2 * R * K + 4 * M}
+    st["front_reorder"] = {"bytes": st["route_sort"]["bytes"] + st["quant"]["bytes"]}
     st["gmm1"] = {"bytes": active * 2 * I * K + active * 2 * I * 4 + R * K * 2 + R * 2 * I * 2,
                   "ops": 2 * R * K * 2 * I}
     st["swiglu"] = {"bytes": R * 2 * I * 2 + R * I * 2 + 8 * R}
@@ -292,28 +295,36 @@ def main():
     c2 = torch.empty((R, w.K), dtype=f16, device="cuda")
     gws = torch.empty(moe.moe_gmm_workspace_size(d), dtype=torch.uint8, device="cuda")
     bounds = torch.zeros((2, w.E, moe.BOUND_SEGMENTS), dtype=i32, device="cuda")  # activation bounds of a1, q2
-    names = ["front_reorder", "gmm1", "swiglu", "gmm2", "combine"]
+    fused_front = w.R <= 4096  # the layer's FrontReorder is one kernel
+    names = (["front_reorder"] if fused_front else ["route_sort", "quant"]) + ["gmm1", "swiglu", "gmm2", "combine"]
+    nev = len(names) + 1
 
     def stages(evs):
         with torch.cuda.stream(stream):
             bounds.zero_()  # the layer clears them with its status word
-        evs[0].record(stream)
-        moe.moe_front_reorder(d, dev["x"], dev["expert_idx"], sorted_, expanded, tpe, cs, a1, pts1, bounds[0], sws,
-                              stream)
-        evs[1].record(stream)
+        ev = iter(evs)
+        next(ev).record(stream)
+        if fused_front:
+            moe.moe_front_reorder(d, dev["x"], dev["expert_idx"], sorted_, expanded, tpe, cs, a1, pts1, bounds[0],
+                                  sws, stream)
+        else:  # what moe_front_reorder launches above 4096 routes, timed apart
+            moe.moe_route_sort(d, dev["expert_idx"], sorted_, expanded, tpe, cs, sws, stream)
+            next(ev).record(stream)
+            moe.moe_quant_dispatch(d, dev["x"], dev["expert_idx"], expanded, a1, pts1, bounds[0], stream)
+        next(ev).record(stream)
         moe.moe_gmm1(d, a1, None, cs, bounds[0], dev["w1"], dev["s1"], c1, gws, stream)
-        evs[2].record(stream)
+        next(ev).record(stream)
         moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, dev["expert_idx"], None, q2, pts2, bounds[1], stream)
-        evs[3].record(stream)
+        next(ev).record(stream)
         moe.moe_gmm2(d, q2, cs, bounds[1], dev["w2"], dev["s2"], c2, gws, stream)
-        evs[4].record(stream)
+        next(ev).record(stream)
         moe.moe_combine_unpermute(d, c2, pts2, expanded, dev["probs"], out, stream)
-        evs[5].record(stream)
+        next(ev).record(stream)
 
     for _ in range(3):
-        stages([torch.cuda.Event(enable_timing=True) for _ in range(6)])
+        stages([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
     n_stage_steps = max(3, min(args.steps, 50))
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_stage_steps)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n_stage_steps)]
     barrier()
     for i in range(n_stage_steps):
         flush.fill_(i & 0xff)
