@@ -738,32 +738,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool active = cg * 64 < it.n_mma;
       const int cs = s_chunk[it.e];
       const int nch = (nk + cs - 1) / cs;
-      int acci[64];
+      // One exact chunk for the whole reduction (activation bounds permitting): its
+      // fp32 sums are the exact integers (|sum| <= 2^24), so the raw values are kept,
+      // the accumulator is handed back to the MMAs right after the loads, and the
+      // epilogue scales them as they are (float(acc) is the same value).  Otherwise
+      // each chunk is converted to int32 and added before the hand-back.
+      const bool single = nch == 1;
+      int acc[64];  // int32 sums, or (single) the chunk's fp32 bits
 #pragma unroll
-      for (int t = 0; t < 64; ++t) acci[t] = 0;
-      for (int ch = 0; ch < nch; ++ch, ++c) {
+      for (int t = 0; t < 64; ++t) acc[t] = 0;
+      if (single) {
         ok = PROF_WAIT(0, wait_or_abort(&accfull_bar, c & 1, abort_flag, args.status));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        PROF_T0(t_drain);
+        ++c;
         tc_fence_after();
         if (active) {
-#pragma unroll
-          for (int t0 = 0; t0 < 64; t0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(lane_base + t0, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float f = __uint_as_float(v[i]);
-              acci[t0 + i] += (i % 3 == 0) ? __float2int_rn(f) : f2i_exact(f);
-            }
-          }
+          tmem_ld16(lane_base, *reinterpret_cast<uint32_t(*)[16]>(&acc[0]));
+          tmem_ld16(lane_base + 16, *reinterpret_cast<uint32_t(*)[16]>(&acc[16]));
+          tmem_ld16(lane_base + 32, *reinterpret_cast<uint32_t(*)[16]>(&acc[32]));
+          tmem_ld16(lane_base + 48, *reinterpret_cast<uint32_t(*)[16]>(&acc[48]));
+          tmem_wait_ld();
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(accempty_remote);
-        PROF_ADD(1, t_drain);
+      } else {
+        for (int ch = 0; ch < nch; ++ch, ++c) {
+          ok = PROF_WAIT(0, wait_or_abort(&accfull_bar, c & 1, abort_flag, args.status));
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          PROF_T0(t_drain);
+          tc_fence_after();
+          if (active) {
+#pragma unroll
+            for (int t0 = 0; t0 < 64; t0 += 16) {
+              uint32_t v[16];
+              tmem_ld16(lane_base + t0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float f = __uint_as_float(v[i]);
+                acc[t0 + i] += (i % 3 == 0) ? __float2int_rn(f) : f2i_exact(f);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(accempty_remote);
+          PROF_ADD(1, t_drain);
+        }
       }
       if (!ok) break;
       if (!active) continue;
@@ -774,9 +798,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float sc = __ldg(args.scale + (size_t)it.e * args.N + ch);
         const int t_lo = cg * 64;
         __half* dst = args.C + (size_t)(it.row0 + t_lo) * args.N + ch;
+        if (single) {
 #pragma unroll
-        for (int t = 0; t < 64; ++t)
-          if (t_lo + t < it.rows) dst[(size_t)t * args.N] = f2h_sat(__fmul_rn(__int2float_rn(acci[t]), sc));
+          for (int t = 0; t < 64; ++t)
+            if (t_lo + t < it.rows) dst[(size_t)t * args.N] = f2h_sat(__fmul_rn(__int_as_float(acc[t]), sc));
+        } else {
+#pragma unroll
+          for (int t = 0; t < 64; ++t)
+            if (t_lo + t < it.rows) dst[(size_t)t * args.N] = f2h_sat(__fmul_rn(__int2float_rn(acc[t]), sc));
+        }
       }
       PROF_ADD(2, t_epi);
     }
