@@ -112,10 +112,17 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
   const int nvec = K >> 3;
   const int4* row = reinterpret_cast<const int4*>(x + (size_t)t * K);
   Vec8h v[VPT];
+  float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * (int)blockDim.x;
-    if (idx < nvec) v[i].v = __ldg(row + idx);
+    if (idx < nvec) {
+      v[i].v = __ldg(row + idx);
+      if constexpr (!SORT) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(__half2float(v[i].h[j])));
+      }
+    }
   }
   if constexpr (SORT) {
     // the row loads above are in flight while the routes are counted
@@ -166,13 +173,14 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
     }
     __syncthreads();
   }
-  float amax = 0.0f;
+  if constexpr (SORT) {  // the row max once the routes are placed (the loads had that time to land)
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int idx = threadIdx.x + i * (int)blockDim.x;
-    if (idx < nvec) {
+    for (int i = 0; i < VPT; ++i) {
+      const int idx = threadIdx.x + i * (int)blockDim.x;
+      if (idx < nvec) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(__half2float(v[i].h[j])));
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(__half2float(v[i].h[j])));
+      }
     }
   }
   amax = block_max_nonneg(amax, red);

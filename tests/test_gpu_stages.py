@@ -325,9 +325,10 @@ def test_gmm_accumulator_exact_beyond_fp32_mantissa(M, wv):
     assert np.array_equal(got, acc_ref.astype(np.float64))
 
 
-@pytest.mark.parametrize("K", [4096, 7168])
+@pytest.mark.parametrize("K", [2048, 4096, 7168])
 def test_gmm_bounds_at_the_limit(K):
-    """Chunks merged by the activation bounds, with partial sums reaching 2^24.
+    """Chunks merged by the activation bounds, with partial sums reaching 2^24 (at
+    K=2048 the merged chunk is the whole reduction: the single-chunk epilogue).
     Every row has sum |code| = 131072 = 2^24 / 128 over the first 2048 k (so those
     two segments form one chunk only when their bounds allow it) and small codes
     after; weights are -128 where the codes are large, so the fp32 partial sums of
@@ -338,7 +339,8 @@ def test_gmm_bounds_at_the_limit(K):
     xq[:, :1024] = 64
     xq[:, 1024:2048] = 64           # 2048 * 64 = 131072 in the first two segments
     xq[:, 2048:] = 0                # nothing after: one merged chunk holds the whole sum
-    xq[:, 3000:3010] = rng.integers(-3, 4, (M, 10))
+    if K > 3010:
+        xq[:, 3000:3010] = rng.integers(-3, 4, (M, 10))
     w1 = rng.integers(-2, 3, (E, 2 * I, K)).astype(np.int8)
     w1[0, :, :2048] = -128
     s1 = np.ones((E, 2 * I), np.float32) / 4096
