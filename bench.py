@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time moe_layer_fwd stream launches instead of the layer's CUDA graph")
     return ap.parse_args()
 
 
@@ -246,12 +248,19 @@ def main():
     d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
     ws = torch.empty(moe.moe_layer_workspace_size(d), dtype=torch.uint8, device="cuda")
     out = torch.empty((w.M, w.K), dtype=torch.float16, device="cuda")
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()  # a capturable stream (not the legacy default stream)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # > L2 (126 MB)
+    graph = None
+    if not args.no_graph:  # the layer's launches recorded once, replayed every step
+        graph = moe.moe_layer_graph_create(d, dev["x"], dev["expert_idx"], dev["probs"], dev["w1"], dev["s1"],
+                                           dev["w2"], dev["s2"], out, ws, stream)
 
     def step():
-        moe.moe_layer_fwd(d, dev["x"], dev["expert_idx"], dev["probs"], dev["w1"], dev["s1"],
-                          dev["w2"], dev["s2"], out, ws, stream)
+        if graph is not None:
+            moe.moe_layer_graph_launch(graph, stream)
+        else:
+            moe.moe_layer_fwd(d, dev["x"], dev["expert_idx"], dev["probs"], dev["w1"], dev["s1"],
+                              dev["w2"], dev["s2"], out, ws, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -267,14 +276,18 @@ def main():
           for _ in range(args.steps)]
     barrier()
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(i & 0xff)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
     barrier()
     t_wall = time.perf_counter() - t_wall
     clocks.stop()
+    use_graph = graph is not None
+    if use_graph:
+        moe.moe_layer_graph_destroy(graph)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = sum(step_ms) / len(step_ms)
     if world > 1:
@@ -326,9 +339,10 @@ def main():
     n_stage_steps = max(3, min(args.steps, 50))
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n_stage_steps)]
     barrier()
-    for i in range(n_stage_steps):
-        flush.fill_(i & 0xff)
-        stages(sev[i])
+    with torch.cuda.stream(stream):
+        for i in range(n_stage_steps):
+            flush.fill_(i & 0xff)
+            stages(sev[i])
     barrier()
     stage_ms = {n: statistics.mean(s[j].elapsed_time(s[j + 1]) for s in sev) for j, n in enumerate(names)}
 
@@ -427,6 +441,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic",
         "config": {"workload": workload_desc(w), "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch": ("CUDA graph of the layer's launches (moe_layer_graph_launch)" if use_graph
+                              else "stream launches (moe_layer_fwd)"),
                    "l2": "flushed before every timed step (512 MB write); int8 weights %.2f GB per step"
                          % ((alg["gmm1"]["bytes"] + alg["gmm2"]["bytes"]) / 1e9),
                    "active_experts": active},

@@ -99,6 +99,27 @@ int32_t moe_layer_fwd(const moe_dims_t* d, const uint16_t* x, const int32_t* exp
                       const float* s2, uint16_t* out, void* workspace, size_t workspace_bytes,
                       void* stream);
 
+/*
+ * The layer as a CUDA graph, for calls repeated on the same buffers (a serving
+ * loop that writes each batch into fixed device buffers): moe_layer_graph_create
+ * records exactly the launches of moe_layer_fwd with these arguments (same
+ * preconditions and error codes) by stream capture on `stream`, which must not be
+ * the legacy default stream (NULL: MOE_ERR_LAUNCH), and instantiates the graph;
+ * nothing runs yet.  moe_layer_graph_launch runs it on `stream` (any stream of the
+ * same device), asynchronously, with the same result as moe_layer_fwd on the
+ * buffers' contents at that time; it saves part of the per-kernel launch gaps
+ * (measured: 0.7% at decode, 1.7% at prefill).  The buffers must stay allocated
+ * while the graph exists.  moe_layer_graph_destroy releases the graph (host
+ * memory and CUDA graph objects; NULL is a no-op).
+ */
+typedef struct moe_layer_graph moe_layer_graph_t;
+int32_t moe_layer_graph_create(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx,
+                               const float* probs, const int8_t* w1, const float* s1, const int8_t* w2,
+                               const float* s2, uint16_t* out, void* workspace, size_t workspace_bytes,
+                               void* stream, moe_layer_graph_t** graph);
+int32_t moe_layer_graph_launch(moe_layer_graph_t* graph, void* stream);
+int32_t moe_layer_graph_destroy(moe_layer_graph_t* graph);
+
 /* Bytes of device workspace moe_layer_fwd_host needs (layer workspace plus
  * staging for the per-call host inputs and the output). */
 size_t moe_layer_host_workspace_size(const moe_dims_t* d);

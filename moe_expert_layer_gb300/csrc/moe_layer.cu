@@ -3,6 +3,7 @@
 // page, section "key implementation logic").  See include/moe_layer.h for the
 // contract of every entry point.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include <cuda_runtime.h>
@@ -197,6 +198,66 @@ int32_t moe_layer_fwd(const moe_dims_t* d, const uint16_t* x, const int32_t* exp
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   return run_layer(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspace, L, static_cast<cudaStream_t>(stream));
+}
+
+struct moe_layer_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+int32_t moe_layer_graph_create(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx,
+                               const float* probs, const int8_t* w1, const float* s1, const int8_t* w2,
+                               const float* s2, uint16_t* out, void* workspace, size_t workspace_bytes,
+                               void* stream, moe_layer_graph_t** graph) {
+  if (!graph) return MOE_ERR_NULL;
+  *graph = nullptr;
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!x || !expert_idx || !probs || !w1 || !s1 || !w2 || !s2 || !out || !workspace) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(expert_idx) || !aligned16(probs) || !aligned16(w1) || !aligned16(s1) ||
+      !aligned16(w2) || !aligned16(s2) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MOE_ERR_ALIGN;
+  const Layout L = layout_of(d);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (!stream) return MOE_ERR_LAUNCH;  // the legacy default stream cannot be captured
+  if ((rc = check_device()) != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return MOE_ERR_LAUNCH;
+  rc = run_layer(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspace, L, st);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e_end = cudaStreamEndCapture(st, &g);
+  if (rc != MOE_OK || e_end != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    return rc != MOE_OK ? rc : MOE_ERR_LAUNCH;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return MOE_ERR_LAUNCH;
+  }
+  moe_layer_graph_t* h = static_cast<moe_layer_graph_t*>(std::malloc(sizeof(moe_layer_graph_t)));
+  if (!h) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(g);
+    return MOE_ERR_LAUNCH;
+  }
+  h->graph = g;
+  h->exec = exec;
+  *graph = h;
+  return MOE_OK;
+}
+
+int32_t moe_layer_graph_launch(moe_layer_graph_t* graph, void* stream) {
+  if (!graph) return MOE_ERR_NULL;
+  return launch_status(cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_layer_graph_destroy(moe_layer_graph_t* graph) {
+  if (!graph) return MOE_OK;
+  const cudaError_t a = cudaGraphExecDestroy(graph->exec);
+  const cudaError_t b = cudaGraphDestroy(graph->graph);
+  std::free(graph);
+  return (a == cudaSuccess && b == cudaSuccess) ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
 int32_t moe_layer_fwd_host(const moe_dims_t* d, const uint16_t* x_host, const int32_t* expert_idx_host,

@@ -66,6 +66,12 @@ def test_entry_points_reject_before_touching_the_device(lib):
     assert lib.moe_front_reorder(ctypes.byref(d), *([None] * 10), 0, None) == -1
     assert lib.moe_front_reorder(ctypes.byref(bad), *([None] * 10), 0, None) == -2
     assert lib.moe_status_string(-5) == b"workspace missing or too small"
+    h = ctypes.c_void_p(1234)
+    assert lib.moe_layer_graph_create(ctypes.byref(d), *([None] * 9), 0, None, ctypes.byref(h)) == -1
+    assert h.value is None  # the handle is cleared on failure
+    assert lib.moe_layer_graph_create(ctypes.byref(bad), *([None] * 9), 0, None, ctypes.byref(h)) == -2
+    assert lib.moe_layer_graph_launch(None, None) == -1
+    assert lib.moe_layer_graph_destroy(None) == 0
     # misaligned pointers -> MOE_ERR_ALIGN
     p = 4096 + 2
     assert lib.moe_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, 4096, 1 << 30, None) == -3

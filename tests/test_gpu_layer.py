@@ -99,6 +99,52 @@ def test_layer_repeated_calls_identical():
         assert np.array_equal(host(out2).view(np.uint16), a.view(np.uint16))
 
 
+@pytest.mark.parametrize("name", ["ragged", "zipf_small"])
+def test_layer_graph_matches_stream_launches(name):
+    """The CUDA-graph form runs the same kernels: bit-identical output, and a replay
+    after the inputs are rewritten in place follows the new contents."""
+    w = next(c for c in SMALL if c.name == name)
+    inp = synth.make_inputs(w)
+    dv = upload_inputs(inp)
+    d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
+    ref, _ = run_layer(w, dv)
+    stream = torch.cuda.Stream()
+    ws = empty(moe.moe_layer_workspace_size(d), torch.uint8)
+    out = torch.full((w.M, w.K), float("nan"), dtype=torch.float16, device="cuda")
+    g = moe.moe_layer_graph_create(d, dv["x"], dv["expert_idx"], dv["probs"], dv["w1"], dv["s1"], dv["w2"],
+                                   dv["s2"], out, ws, stream)
+    try:
+        torch.cuda.synchronize()
+        assert torch.isnan(out).all()  # creating the graph ran nothing
+        moe.moe_layer_graph_launch(g, stream)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+        # new tokens and routes in the same buffers
+        w2 = synth.Workload(w.name, w.M, w.K, w.I, w.E, w.topK, w.routing, w.seed + 1000)
+        inp2 = synth.make_inputs(w2, with_weights=False)
+        dv["x"].copy_(torch.from_numpy(inp2["x"]).cuda())
+        dv["expert_idx"].copy_(torch.from_numpy(inp2["expert_idx"]).cuda())
+        dv["probs"].copy_(torch.from_numpy(inp2["probs"]).cuda())
+        moe.moe_layer_graph_launch(g, stream)
+        torch.cuda.synchronize()
+        ref2, _ = run_layer(w, dv)
+        assert torch.equal(out, ref2)
+        assert moe.moe_workspace_status(ws) == 0
+    finally:
+        moe.moe_layer_graph_destroy(g)
+
+
+def test_layer_graph_rejects_the_legacy_stream():
+    w = SMALL[0]
+    d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
+    dv = upload_inputs(synth.make_inputs(w))
+    ws = empty(moe.moe_layer_workspace_size(d), torch.uint8)
+    out = empty((w.M, w.K), torch.float16)
+    with pytest.raises(moe.MoeError):
+        moe.moe_layer_graph_create(d, dv["x"], dv["expert_idx"], dv["probs"], dv["w1"], dv["s1"], dv["w2"],
+                                   dv["s2"], out, ws, 0)
+
+
 def test_layer_host_entry_point_matches_device():
     w = synth.Workload("hostio", 48, 512, 128, 8, 2, "uniform", 113)
     inp = synth.make_inputs(w)
