@@ -39,6 +39,16 @@ __device__ __forceinline__ void add_segment_l1(int* s_l1, int idx, int l1) {
   if ((int)(threadIdx.x & 31) == __ffs(mask) - 1) atomicAdd(&s_l1[(idx * 8) / kBoundSegment], sum);
 }
 
+// Two codes given as the bits 0x4B400000 + q of fl(q + 1.5 * 2^23) -> their binary16
+// pair: 0x6480 + q (= 1152 + q in the mantissa of 1024) in each half, minus 1152.
+__device__ __forceinline__ uint32_t code_bits_to_half2(uint32_t b0, uint32_t b1) {
+  const uint32_t k = 0x6480u - 0x4B400000u;
+  const uint32_t w = __byte_perm(b0 + k, b1 + k, 0x5410);
+  uint32_t r;
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0x64806480u));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t codes_to_half2(int q0, int q1) {
   const uint32_t w = (uint32_t)(0x6400 + q0 + 128) | ((uint32_t)(0x6400 + q1 + 128) << 16);
   uint32_t r;
@@ -299,35 +309,41 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
   }
   amax = block_max_nonneg(amax, red);
   const bool nz = amax > 0.0f;
+  // inv = 0 for an all-zero row: every y * inv is then +-0 and its code 0
   const float inv = nz ? __fdiv_rn(127.0f, amax) : 0.0f;
   if (threadIdx.x == 0) pts2[d] = nz ? __fdiv_rn(amax, 127.0f) : 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * (int)blockDim.x;
     if (idx < nvec) {
-      int q[8];
+      // r = fl(y * inv) + 1.5 * 2^23 rounds y * inv to the nearest integer q (ties to
+      // even) and its bits are 0x4B400000 + q.  |y| <= amax keeps |y * inv| below
+      // 127 * (1 + 2^-23) < 127.5, so q needs no clamp.  (SwiGLU is issue-bound: the
+      // codes, their binary16 form and the segment sums take few instructions.)
+      float r[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) q[j] = nz ? clamp127(rint_small(__fmul_rn(y[i][j], inv))) : 0;
+      for (int j = 0; j < 8; ++j) r[j] = __fadd_rn(__fmul_rn(y[i][j], inv), 12582912.0f);
       if (bounds) {
-        int l1 = 0;
+        float l1 = 0.0f;  // at most 8 * 127: exact
 #pragma unroll
-        for (int j = 0; j < 8; ++j) l1 += abs(q[j]);
-        add_segment_l1(s_l1, idx, l1);
+        for (int j = 0; j < 8; ++j) l1 = __fadd_rn(l1, fabsf(__fsub_rn(r[j], 12582912.0f)));
+        add_segment_l1(s_l1, idx, (int)l1);
       }
       if (q2_i8) {
+        // the low byte of 0x4B400000 + q is q's two's-complement byte
         uint2 packed;
-        packed.x = (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
-                   ((uint32_t)(q[3] & 0xff) << 24);
-        packed.y = (uint32_t)(q[4] & 0xff) | ((uint32_t)(q[5] & 0xff) << 8) | ((uint32_t)(q[6] & 0xff) << 16) |
-                   ((uint32_t)(q[7] & 0xff) << 24);
+        packed.x = __byte_perm(__byte_perm(__float_as_uint(r[0]), __float_as_uint(r[1]), 0x0040),
+                               __byte_perm(__float_as_uint(r[2]), __float_as_uint(r[3]), 0x0040), 0x5410);
+        packed.y = __byte_perm(__byte_perm(__float_as_uint(r[4]), __float_as_uint(r[5]), 0x0040),
+                               __byte_perm(__float_as_uint(r[6]), __float_as_uint(r[7]), 0x0040), 0x5410);
         reinterpret_cast<uint2*>(q2_i8 + (size_t)d * I)[idx] = packed;
       }
       if (q2_f16) {
         int4 o;
-        o.x = (int)codes_to_half2(q[0], q[1]);
-        o.y = (int)codes_to_half2(q[2], q[3]);
-        o.z = (int)codes_to_half2(q[4], q[5]);
-        o.w = (int)codes_to_half2(q[6], q[7]);
+        o.x = (int)code_bits_to_half2(__float_as_uint(r[0]), __float_as_uint(r[1]));
+        o.y = (int)code_bits_to_half2(__float_as_uint(r[2]), __float_as_uint(r[3]));
+        o.z = (int)code_bits_to_half2(__float_as_uint(r[4]), __float_as_uint(r[5]));
+        o.w = (int)code_bits_to_half2(__float_as_uint(r[6]), __float_as_uint(r[7]));
         reinterpret_cast<int4*>(q2_f16 + (size_t)d * I)[idx] = o;
       }
     }
