@@ -16,6 +16,16 @@ __device__ __forceinline__ __half f2h_sat(float v) {
   return __float2half_rn(v);
 }
 
+// Two fp32 -> a binary16 pair (lo, hi), each as f2h_sat (round to nearest even,
+// saturating at +-65504), in one conversion.
+__device__ __forceinline__ __half2 f2h2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  __half2 h;
+  *reinterpret_cast<uint32_t*>(&h) = r;
+  return h;
+}
+
 __device__ __forceinline__ int clamp127(int v) { return max(-127, min(127, v)); }
 
 __device__ __forceinline__ float warp_max(float v) {

@@ -393,14 +393,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_unpermute_tk_kernel(
   for (int u = 0; u < TK; ++u) {
     if (d[u] < 0) continue;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float dv = __half2float(f2h_sat(__fmul_rn(__half2float(c[u].h[j]), sc[u])));
-      acc[j] = __fadd_rn(acc[j], __fmul_rn(dv, p[u]));
+    for (int j = 0; j < 8; j += 2) {
+      // D = sat_f16(C2 * pts2), two at a time
+      const __half2 dh = f2h2_sat(__fmul_rn(__half2float(c[u].h[j]), sc[u]),
+                                  __fmul_rn(__half2float(c[u].h[j + 1]), sc[u]));
+      acc[j] = __fadd_rn(acc[j], __fmul_rn(__low2float(dh), p[u]));
+      acc[j + 1] = __fadd_rn(acc[j + 1], __fmul_rn(__high2float(dh), p[u]));
     }
   }
   Vec8h o;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) o.h[j] = f2h_sat(acc[j]);
+  for (int j = 0; j < 4; ++j) o.h2[j] = f2h2_sat(acc[2 * j], acc[2 * j + 1]);
   reinterpret_cast<int4*>(out + (size_t)t * K)[vec] = o.v;
 }
 
