@@ -895,10 +895,14 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
 // (K=7168, I=2048, E=256, Zipf): GMM1 1.90 ms at 32 rows, 1.97 at 16.
 constexpr int kSplitRows = 32;
 
+// The warp-MMA engine alone (up to 24 rows per expert on average) keeps 512-deep
+// chunks and reads no activation bounds.
+bool grouped_gemm_reads_bounds(int R, int E) { return (double)R / (double)E > 24.0; }
+
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream) {
   GroupedGemmProblem q = p;
   const double mean_rows = (double)p.R / (double)p.E;
-  if (mean_rows <= 24.0) {
+  if (!grouped_gemm_reads_bounds(p.R, p.E)) {
     // 16-row tiles up to 8 rows per expert on average (decode); 32-row tiles above,
     // so that an expert of up to 32 rows streams its weights through one work item
     q.split_rows = 0x7fffffff;

@@ -56,6 +56,7 @@ struct GroupedGemmProblem {
   const int32_t* bounds;            // [E][kBoundSegments] activation bounds, or null
 };
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream);     // picks an engine
+bool grouped_gemm_reads_bounds(int R, int E);  // whether the engine it picks uses activation bounds
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream);  // gemm_hmma.cu
 cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream);  // gemm_tc.cu
 

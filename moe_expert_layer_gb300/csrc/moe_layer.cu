@@ -107,8 +107,10 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   float* pts2 = at<float>(ws, L.pts2);
   uint16_t* c2 = at<uint16_t>(ws, L.c2);
 
-  int32_t* bounds1 = at<int32_t>(ws, L.bounds1);
-  int32_t* bounds2 = at<int32_t>(ws, L.bounds2);
+  // activation bounds only where the GEMM engine reads them (above 24 rows per expert)
+  const bool use_bounds = moe::grouped_gemm_reads_bounds(R, E);
+  int32_t* bounds1 = use_bounds ? at<int32_t>(ws, L.bounds1) : nullptr;
+  int32_t* bounds2 = use_bounds ? at<int32_t>(ws, L.bounds2) : nullptr;
   cudaError_t e;
   if ((e = cudaMemsetAsync(status, 0, L.bounds2 + (size_t)E * moe::kBoundSegments * 4, st)) != cudaSuccess)
     return launch_status(e);
