@@ -117,6 +117,17 @@ int32_t moe_layer_graph_create(const moe_dims_t* d, const uint16_t* x, const int
                                const float* probs, const int8_t* w1, const float* s1, const int8_t* w2,
                                const float* s2, uint16_t* out, void* workspace, size_t workspace_bytes,
                                void* stream, moe_layer_graph_t** graph);
+/*
+ * The same for moe_layer_fwd_host: the graph holds the copies of x_host,
+ * expert_idx_host and probs_host into the workspace, the layer and the copy of the
+ * output to out_host.  A launch does not synchronise: read out_host after the stream
+ * has (cudaStreamSynchronize).  The host buffers must be page-locked (cudaHostAlloc,
+ * cudaHostRegister); pageable memory cannot be captured (MOE_ERR_LAUNCH).
+ */
+int32_t moe_layer_graph_create_host(const moe_dims_t* d, const uint16_t* x_host, const int32_t* expert_idx_host,
+                                    const float* probs_host, const int8_t* w1, const float* s1, const int8_t* w2,
+                                    const float* s2, uint16_t* out_host, void* workspace, size_t workspace_bytes,
+                                    void* stream, moe_layer_graph_t** graph);
 int32_t moe_layer_graph_launch(moe_layer_graph_t* graph, void* stream);
 int32_t moe_layer_graph_destroy(moe_layer_graph_t* graph);
 

@@ -26,7 +26,7 @@ EXPORTS = [
     "moe_workspace_clear_status", "moe_route_sort_workspace_size", "moe_route_sort",
     "moe_quant_tokens", "moe_quant_dispatch", "moe_front_reorder", "moe_gmm_workspace_size", "moe_gmm1",
     "moe_swiglu_quant", "moe_gmm2", "moe_combine_unpermute", "moe_route_sort_noalloc", "moe_selftest_wait_timeout",
-    "moe_layer_graph_create", "moe_layer_graph_launch", "moe_layer_graph_destroy",
+    "moe_layer_graph_create", "moe_layer_graph_create_host", "moe_layer_graph_launch", "moe_layer_graph_destroy",
 ]
 
 
@@ -66,6 +66,7 @@ def load_library(path=None):
         "moe_layer_fwd": ([D] + [vp] * 9 + [sz, vp], i32),
         "moe_layer_fwd_host": ([D] + [vp] * 9 + [sz, vp], i32),
         "moe_layer_graph_create": ([D] + [vp] * 9 + [sz, vp, ctypes.POINTER(vp)], i32),
+        "moe_layer_graph_create_host": ([D] + [vp] * 9 + [sz, vp, ctypes.POINTER(vp)], i32),
         "moe_layer_graph_launch": ([vp, vp], i32),
         "moe_layer_graph_destroy": ([vp], i32),
         "moe_workspace_status": ([vp, ctypes.POINTER(i32), vp], i32),
@@ -142,6 +143,17 @@ def moe_layer_graph_create(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspa
     _check("moe_layer_graph_create", load_library().moe_layer_graph_create(
         ctypes.byref(d), _p(x), _p(expert_idx), _p(probs), _p(w1), _p(s1), _p(w2), _p(s2), _p(out),
         _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream), ctypes.byref(h)))
+    return h
+
+
+def moe_layer_graph_create_host(d, x_host, expert_idx_host, probs_host, w1, s1, w2, s2, out_host, workspace,
+                                stream):
+    """Records moe_layer_fwd_host (copies included, no synchronisation) as a CUDA graph."""
+    h = ctypes.c_void_p()
+    _check("moe_layer_graph_create_host", load_library().moe_layer_graph_create_host(
+        ctypes.byref(d), _p(x_host), _p(expert_idx_host), _p(probs_host), _p(w1), _p(s1), _p(w2), _p(s2),
+        _p(out_host), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
+        ctypes.byref(h)))
     return h
 
 

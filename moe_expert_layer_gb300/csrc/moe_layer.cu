@@ -11,6 +11,11 @@
 #include "../../include/moe_layer.h"
 #include "kernels.h"
 
+struct moe_layer_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -159,6 +164,68 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   return launch_status(e);
 }
 
+// moe_layer_fwd_host's work, enqueued on st without the final synchronisation:
+// the per-call inputs copied into the workspace's staging, the layer, the output
+// copied back.
+int32_t enqueue_layer_host(const moe_dims_t* d, const uint16_t* x_host, const int32_t* expert_idx_host,
+                           const float* probs_host, const int8_t* w1, const float* s1, const int8_t* w2,
+                           const float* s2, uint16_t* out_host, void* workspace, size_t workspace_bytes,
+                           cudaStream_t st) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!x_host || !expert_idx_host || !probs_host || !w1 || !s1 || !w2 || !s2 || !out_host || !workspace)
+    return MOE_ERR_NULL;
+  if (!aligned16(w1) || !aligned16(s1) || !aligned16(w2) || !aligned16(s2) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MOE_ERR_ALIGN;
+  const Layout L = layout_of(d);
+  if (workspace_bytes < L.host_total) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  const size_t M = d->M, K = d->K, R = M * d->topK;
+  uint16_t* dx = at<uint16_t>(workspace, L.hx);
+  int32_t* dei = at<int32_t>(workspace, L.hei);
+  float* dpr = at<float>(workspace, L.hprobs);
+  uint16_t* dout = at<uint16_t>(workspace, L.hout);
+  if (cudaMemcpyAsync(dx, x_host, M * K * 2, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dei, expert_idx_host, R * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dpr, probs_host, R * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  rc = run_layer(d, dx, dei, dpr, w1, s1, w2, s2, dout, workspace, L, st);
+  if (rc != MOE_OK) return rc;
+  if (cudaMemcpyAsync(out_host, dout, M * K * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return MOE_OK;
+}
+
+// Records what `enqueue` puts on st (stream capture) and instantiates it.
+template <class F>
+int32_t capture_graph(cudaStream_t st, F enqueue, moe_layer_graph_t** graph) {
+  if (!st) return MOE_ERR_LAUNCH;  // the legacy default stream cannot be captured
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return MOE_ERR_LAUNCH;
+  const int32_t rc = enqueue();
+  cudaGraph_t g = nullptr;
+  const cudaError_t e_end = cudaStreamEndCapture(st, &g);
+  if (rc != MOE_OK || e_end != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();  // a failed capture leaves no sticky error behind
+    return rc != MOE_OK ? rc : MOE_ERR_LAUNCH;
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return MOE_ERR_LAUNCH;
+  }
+  moe_layer_graph_t* h = static_cast<moe_layer_graph_t*>(std::malloc(sizeof(moe_layer_graph_t)));
+  if (!h) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(g);
+    return MOE_ERR_LAUNCH;
+  }
+  h->graph = g;
+  h->exec = exec;
+  *graph = h;
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -202,11 +269,6 @@ int32_t moe_layer_fwd(const moe_dims_t* d, const uint16_t* x, const int32_t* exp
   return run_layer(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspace, L, static_cast<cudaStream_t>(stream));
 }
 
-struct moe_layer_graph {
-  cudaGraph_t graph;
-  cudaGraphExec_t exec;
-};
-
 int32_t moe_layer_graph_create(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx,
                                const float* probs, const int8_t* w1, const float* s1, const int8_t* w2,
                                const float* s2, uint16_t* out, void* workspace, size_t workspace_bytes,
@@ -224,29 +286,8 @@ int32_t moe_layer_graph_create(const moe_dims_t* d, const uint16_t* x, const int
   if (!stream) return MOE_ERR_LAUNCH;  // the legacy default stream cannot be captured
   if ((rc = check_device()) != MOE_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return MOE_ERR_LAUNCH;
-  rc = run_layer(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspace, L, st);
-  cudaGraph_t g = nullptr;
-  const cudaError_t e_end = cudaStreamEndCapture(st, &g);
-  if (rc != MOE_OK || e_end != cudaSuccess || !g) {
-    if (g) cudaGraphDestroy(g);
-    return rc != MOE_OK ? rc : MOE_ERR_LAUNCH;
-  }
-  cudaGraphExec_t exec = nullptr;
-  if (cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) {
-    cudaGraphDestroy(g);
-    return MOE_ERR_LAUNCH;
-  }
-  moe_layer_graph_t* h = static_cast<moe_layer_graph_t*>(std::malloc(sizeof(moe_layer_graph_t)));
-  if (!h) {
-    cudaGraphExecDestroy(exec);
-    cudaGraphDestroy(g);
-    return MOE_ERR_LAUNCH;
-  }
-  h->graph = g;
-  h->exec = exec;
-  *graph = h;
-  return MOE_OK;
+  return capture_graph(st, [&]() { return run_layer(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspace, L, st); },
+                       graph);
 }
 
 int32_t moe_layer_graph_launch(moe_layer_graph_t* graph, void* stream) {
@@ -266,31 +307,29 @@ int32_t moe_layer_fwd_host(const moe_dims_t* d, const uint16_t* x_host, const in
                            const float* probs_host, const int8_t* w1, const float* s1, const int8_t* w2,
                            const float* s2, uint16_t* out_host, void* workspace, size_t workspace_bytes,
                            void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int32_t rc = enqueue_layer_host(d, x_host, expert_idx_host, probs_host, w1, s1, w2, s2, out_host, workspace,
+                                        workspace_bytes, st);
+  if (rc != MOE_OK) return rc;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  return MOE_OK;
+}
+
+int32_t moe_layer_graph_create_host(const moe_dims_t* d, const uint16_t* x_host, const int32_t* expert_idx_host,
+                                    const float* probs_host, const int8_t* w1, const float* s1, const int8_t* w2,
+                                    const float* s2, uint16_t* out_host, void* workspace, size_t workspace_bytes,
+                                    void* stream, moe_layer_graph_t** graph) {
+  if (!graph) return MOE_ERR_NULL;
+  *graph = nullptr;
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!x_host || !expert_idx_host || !probs_host || !w1 || !s1 || !w2 || !s2 || !out_host || !workspace)
     return MOE_ERR_NULL;
-  if (!aligned16(w1) || !aligned16(s1) || !aligned16(w2) || !aligned16(s2) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return MOE_ERR_ALIGN;
-  const Layout L = layout_of(d);
-  if (workspace_bytes < L.host_total) return MOE_ERR_WORKSPACE;
-  if ((rc = check_device()) != MOE_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t M = d->M, K = d->K, R = M * d->topK;
-  uint16_t* dx = at<uint16_t>(workspace, L.hx);
-  int32_t* dei = at<int32_t>(workspace, L.hei);
-  float* dpr = at<float>(workspace, L.hprobs);
-  uint16_t* dout = at<uint16_t>(workspace, L.hout);
-  if (cudaMemcpyAsync(dx, x_host, M * K * 2, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dei, expert_idx_host, R * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dpr, probs_host, R * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return MOE_ERR_LAUNCH;
-  rc = run_layer(d, dx, dei, dpr, w1, s1, w2, s2, dout, workspace, L, st);
-  if (rc != MOE_OK) return rc;
-  if (cudaMemcpyAsync(out_host, dout, M * K * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_LAUNCH;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_LAUNCH;
-  return MOE_OK;
+  return capture_graph(st, [&]() {
+    return enqueue_layer_host(d, x_host, expert_idx_host, probs_host, w1, s1, w2, s2, out_host, workspace,
+                              workspace_bytes, st);
+  }, graph);
 }
 
 int32_t moe_workspace_status(const void* workspace, int32_t* host_status, void* stream) {

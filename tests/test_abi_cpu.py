@@ -70,6 +70,7 @@ def test_entry_points_reject_before_touching_the_device(lib):
     assert lib.moe_layer_graph_create(ctypes.byref(d), *([None] * 9), 0, None, ctypes.byref(h)) == -1
     assert h.value is None  # the handle is cleared on failure
     assert lib.moe_layer_graph_create(ctypes.byref(bad), *([None] * 9), 0, None, ctypes.byref(h)) == -2
+    assert lib.moe_layer_graph_create_host(ctypes.byref(d), *([None] * 9), 0, None, ctypes.byref(h)) == -1
     assert lib.moe_layer_graph_launch(None, None) == -1
     assert lib.moe_layer_graph_destroy(None) == 0
     # misaligned pointers -> MOE_ERR_ALIGN

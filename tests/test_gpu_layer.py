@@ -134,6 +134,40 @@ def test_layer_graph_matches_stream_launches(name):
         moe.moe_layer_graph_destroy(g)
 
 
+def test_layer_host_graph_matches_host_entry_point():
+    """The host-buffer graph (copies in, layer, copy out) gives moe_layer_fwd_host's
+    output bit for bit, and follows new contents of the pinned input buffers."""
+    w = next(c for c in SMALL if c.name == "ragged")
+    inp = synth.make_inputs(w)
+    dv = upload_inputs(inp)
+    d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
+    hws = empty(moe.moe_layer_host_workspace_size(d), torch.uint8)
+    xh = torch.from_numpy(inp["x"]).pin_memory()
+    eih = torch.from_numpy(inp["expert_idx"]).pin_memory()
+    prh = torch.from_numpy(inp["probs"]).pin_memory()
+    ref = torch.empty((w.M, w.K), dtype=torch.float16).pin_memory()
+    moe.moe_layer_fwd_host(d, xh, eih, prh, dv["w1"], dv["s1"], dv["w2"], dv["s2"], ref, hws)
+    stream = torch.cuda.Stream()
+    outh = torch.full((w.M, w.K), float("nan"), dtype=torch.float16).pin_memory()
+    g = moe.moe_layer_graph_create_host(d, xh, eih, prh, dv["w1"], dv["s1"], dv["w2"], dv["s2"], outh, hws, stream)
+    try:
+        moe.moe_layer_graph_launch(g, stream)
+        stream.synchronize()
+        assert torch.equal(outh, ref)
+        w2 = synth.Workload(w.name, w.M, w.K, w.I, w.E, w.topK, w.routing, w.seed + 2000)
+        inp2 = synth.make_inputs(w2, with_weights=False)
+        xh.copy_(torch.from_numpy(inp2["x"]))
+        eih.copy_(torch.from_numpy(inp2["expert_idx"]))
+        prh.copy_(torch.from_numpy(inp2["probs"]))
+        moe.moe_layer_graph_launch(g, stream)
+        stream.synchronize()
+        ref2 = torch.empty_like(ref).pin_memory()
+        moe.moe_layer_fwd_host(d, xh, eih, prh, dv["w1"], dv["s1"], dv["w2"], dv["s2"], ref2, hws)
+        assert torch.equal(outh, ref2)
+    finally:
+        moe.moe_layer_graph_destroy(g)
+
+
 def test_layer_graph_rejects_the_legacy_stream():
     w = SMALL[0]
     d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
