@@ -215,6 +215,34 @@ def traffic_record(stage, workload, kernel_file):
     return int(m1.group(1))
 
 
+# ----------------------------------------------------------------------------- replicas (N > 1)
+def replica_inputs(w, rank):
+    """The inputs rank `rank` runs: every rank the same weights and scales, its own
+    token batch and routing (rank 0 the workload's own seed, rank r seed + 1000 r)."""
+    inp = synth.make_inputs(w)
+    if rank:
+        r = synth.Workload(w.name, w.M, w.K, w.I, w.E, w.topK, w.routing, w.seed + 1000 * rank)
+        inp.update(synth.make_inputs(r, with_weights=False))
+    return inp
+
+
+def max_over_ranks(v, world, device):
+    """The largest of the ranks' values (every rank gets it); `device` is where the
+    process group's backend reduces (cuda for NCCL, cpu for gloo)."""
+    if world <= 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, M, ms):
+    """Whole-job throughput: every rank's M tokens over the slowest rank's step time."""
+    return world * M / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -238,12 +266,7 @@ def main():
         torch.cuda.synchronize()
 
     w = synth.CONFIGS[args.workload]
-    # each rank its own replica batch: same weights, tokens/routing drawn per rank
-    inp = synth.make_inputs(w)
-    if rank:
-        r = synth.Workload(w.name, w.M, w.K, w.I, w.E, w.topK, w.routing, w.seed + 1000 * rank)
-        extra = synth.make_inputs(r, with_weights=False)
-        inp.update(extra)
+    inp = replica_inputs(w, rank)  # each rank its own batch, the same weights
     dev = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in inp.items()}
     d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
     ws = torch.empty(moe.moe_layer_workspace_size(d), dtype=torch.uint8, device="cuda")
@@ -289,12 +312,8 @@ def main():
     if use_graph:
         moe.moe_layer_graph_destroy(graph)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * w.M / (ms * 1e-3)
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, "cuda")
+    value = job_tokens_per_s(world, w.M, ms)
 
     # ---- per-stage timing through the stage entry points (same kernels), for the roofline
     R = w.R
@@ -424,11 +443,8 @@ def main():
         e_ms = 1e3 * tot / n_e2e
         if hgraph is not None:
             moe.moe_layer_graph_destroy(hgraph)
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * w.M / (e_ms * 1e-3), "unit": UNIT,
+        e_ms = max_over_ranks(e_ms, world, "cuda")
+        e2e = {"value": job_tokens_per_s(world, w.M, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": int(inp["x"].nbytes + inp["expert_idx"].nbytes + inp["probs"].nbytes),
                "d2h_bytes_per_step": int(w.M * w.K * 2), "ms_per_step": round(e_ms, 4),
                "path": ("moe_layer_graph_create_host + moe_layer_graph_launch, then a stream synchronise"
