@@ -39,13 +39,17 @@ __device__ __forceinline__ void add_segment_l1(int* s_l1, int idx, int l1) {
   if ((int)(threadIdx.x & 31) == __ffs(mask) - 1) atomicAdd(&s_l1[(idx * 8) / kBoundSegment], sum);
 }
 
-// Two codes given as the bits 0x4B400000 + q of fl(q + 1.5 * 2^23) -> their binary16
-// pair: 0x6480 + q (= 1152 + q in the mantissa of 1024) in each half, minus 1152.
+// Requant codes read off a float: for |v| < 127.5, r = fl(v + kCodeMagic) is
+// kCodeMagic + q with q = v rounded to the nearest integer, ties to even (the float
+// spacing in [2^23, 2^24) is 1 and kCodeMagic is even), and r's bits are 0x4B406480 + q:
+// the low half-word, 0x6480 + q, is the binary16 1152 + q (the mantissa of 1024) and
+// its low byte 0x80 + q is q's two's-complement byte with the top bit flipped.
+constexpr float kCodeMagic = 12608640.0f;  // 1.5 * 2^23 + 0x6480
+
+// Two such code floats -> the binary16 pair (q0, q1): their low half-words, minus 1152.
 __device__ __forceinline__ uint32_t code_bits_to_half2(uint32_t b0, uint32_t b1) {
-  const uint32_t k = 0x6480u - 0x4B400000u;
-  const uint32_t w = __byte_perm(b0 + k, b1 + k, 0x5410);
   uint32_t r;
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(0x64806480u));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(__byte_perm(b0, b1, 0x5410)), "r"(0x64806480u));
   return r;
 }
 
@@ -297,12 +301,14 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float hg = __fmul_rn(__half2float(g.h[j]), p1);
-        const float hu = __fmul_rn(__half2float(u.h[j]), p1);
         // exp and the division on the MUFU fast paths (ex2 / rcp, a few ulp): SwiGLU
         // is instruction-bound, and the requantised codes tolerate it (the pages'
-        // exp is a different library's in any case)
+        // exp is a different library's in any case).  The up half's token scale p1
+        // is left out of y: it scales the whole row, so the codes y * 127 / max|y|
+        // keep their values (to an ulp or two, like the fast exp) and only pts2
+        // takes it back.
         const float silu = __fdividef(hg, __fadd_rn(1.0f, __expf(-hg)));
-        y[i][j] = __fmul_rn(silu, hu);
+        y[i][j] = __fmul_rn(silu, __half2float(u.h[j]));
         amax = fmaxf(amax, fabsf(y[i][j]));
       }
     }
@@ -311,31 +317,33 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
   const bool nz = amax > 0.0f;
   // inv = 0 for an all-zero row: every y * inv is then +-0 and its code 0
   const float inv = nz ? __fdiv_rn(127.0f, amax) : 0.0f;
-  if (threadIdx.x == 0) pts2[d] = nz ? __fdiv_rn(amax, 127.0f) : 0.0f;
+  if (threadIdx.x == 0) pts2[d] = nz ? __fdiv_rn(__fmul_rn(amax, p1), 127.0f) : 0.0f;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * (int)blockDim.x;
     if (idx < nvec) {
-      // r = fl(y * inv) + 1.5 * 2^23 rounds y * inv to the nearest integer q (ties to
-      // even) and its bits are 0x4B400000 + q.  |y| <= amax keeps |y * inv| below
-      // 127 * (1 + 2^-23) < 127.5, so q needs no clamp.  (SwiGLU is issue-bound: the
-      // codes, their binary16 form and the segment sums take few instructions.)
+      // r = fl(y * inv + kCodeMagic), one rounding of the exact product: its nearest
+      // integer q, ties to even.  |y| <= amax keeps |y * inv| below 127 * (1 + 2^-23)
+      // < 127.5, so q needs no clamp.  (SwiGLU is issue-bound: the codes, their
+      // binary16 form and the segment sums take few instructions.)
       float r[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) r[j] = __fadd_rn(__fmul_rn(y[i][j], inv), 12582912.0f);
+      for (int j = 0; j < 8; ++j) r[j] = __fmaf_rn(y[i][j], inv, kCodeMagic);
       if (bounds) {
         float l1 = 0.0f;  // at most 8 * 127: exact
 #pragma unroll
-        for (int j = 0; j < 8; ++j) l1 = __fadd_rn(l1, fabsf(__fsub_rn(r[j], 12582912.0f)));
+        for (int j = 0; j < 8; ++j) l1 = __fadd_rn(l1, fabsf(__fsub_rn(r[j], kCodeMagic)));
         add_segment_l1(s_l1, idx, (int)l1);
       }
       if (q2_i8) {
-        // the low byte of 0x4B400000 + q is q's two's-complement byte
+        // the low bytes 0x80 + q, top bits flipped back: q's two's-complement bytes
         uint2 packed;
         packed.x = __byte_perm(__byte_perm(__float_as_uint(r[0]), __float_as_uint(r[1]), 0x0040),
-                               __byte_perm(__float_as_uint(r[2]), __float_as_uint(r[3]), 0x0040), 0x5410);
+                               __byte_perm(__float_as_uint(r[2]), __float_as_uint(r[3]), 0x0040), 0x5410) ^
+                   0x80808080u;
         packed.y = __byte_perm(__byte_perm(__float_as_uint(r[4]), __float_as_uint(r[5]), 0x0040),
-                               __byte_perm(__float_as_uint(r[6]), __float_as_uint(r[7]), 0x0040), 0x5410);
+                               __byte_perm(__float_as_uint(r[6]), __float_as_uint(r[7]), 0x0040), 0x5410) ^
+                   0x80808080u;
         reinterpret_cast<uint2*>(q2_i8 + (size_t)d * I)[idx] = packed;
       }
       if (q2_f16) {
