@@ -18,6 +18,7 @@ union Vec8h {
   int4 v;
   __half2 h2[4];
   __half h[8];
+  uint32_t u[4];
 };
 
 constexpr int kRowThreads = 256;
@@ -329,11 +330,17 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
       float r[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) r[j] = __fmaf_rn(y[i][j], inv, kCodeMagic);
-      if (bounds) {
-        float l1 = 0.0f;  // at most 8 * 127: exact
+      Vec8h hc;  // the codes as binary16
 #pragma unroll
-        for (int j = 0; j < 8; ++j) l1 = __fadd_rn(l1, fabsf(__fsub_rn(r[j], kCodeMagic)));
-        add_segment_l1(s_l1, idx, (int)l1);
+      for (int j = 0; j < 4; ++j) hc.u[j] = code_bits_to_half2(__float_as_uint(r[2 * j]), __float_as_uint(r[2 * j + 1]));
+      if (bounds) {
+        // sum of |q| over the 8 codes in binary16 (integers up to 8 * 127 are exact),
+        // read off the bits of s + 1024 = 0x6400 + s
+        __half2 a = __habs2(hc.h2[0]);
+#pragma unroll
+        for (int j = 1; j < 4; ++j) a = __hadd2(a, __habs2(hc.h2[j]));
+        const __half s = __hadd(__hadd(__low2half(a), __high2half(a)), __ushort_as_half(0x6400));
+        add_segment_l1(s_l1, idx, (int)__half_as_ushort(s) - 0x6400);
       }
       if (q2_i8) {
         // the low bytes 0x80 + q, top bits flipped back: q's two's-complement bytes
@@ -346,14 +353,7 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
                    0x80808080u;
         reinterpret_cast<uint2*>(q2_i8 + (size_t)d * I)[idx] = packed;
       }
-      if (q2_f16) {
-        int4 o;
-        o.x = (int)code_bits_to_half2(__float_as_uint(r[0]), __float_as_uint(r[1]));
-        o.y = (int)code_bits_to_half2(__float_as_uint(r[2]), __float_as_uint(r[3]));
-        o.z = (int)code_bits_to_half2(__float_as_uint(r[4]), __float_as_uint(r[5]));
-        o.w = (int)code_bits_to_half2(__float_as_uint(r[6]), __float_as_uint(r[7]));
-        reinterpret_cast<int4*>(q2_f16 + (size_t)d * I)[idx] = o;
-      }
+      if (q2_f16) reinterpret_cast<int4*>(q2_f16 + (size_t)d * I)[idx] = hc.v;
     }
   }
   if (bounds) {
