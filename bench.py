@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time moe_layer_fwd stream launches instead of the layer's CUDA graph")
+    ap.add_argument("--weights", default="tiles", choices=["tiles", "rows"],
+                    help="weight layout the layer reads: 16 KiB tiles packed once before timing "
+                         "(moe_pack_weight_tiles), or the [E][N][D] rows as given")
     return ap.parse_args()
 
 
@@ -268,7 +271,16 @@ def main():
     w = synth.CONFIGS[args.workload]
     inp = replica_inputs(w, rank)  # each rank its own batch, the same weights
     dev = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in inp.items()}
-    d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
+    layout = moe.WEIGHTS_TILES if args.weights == "tiles" else moe.WEIGHTS_ROWS
+    d = moe.dims(w.M, w.K, w.I, w.E, w.topK, layout)
+    if layout == moe.WEIGHTS_TILES:
+        # once, at weight-load time (outside every timed region): the row-layout
+        # weights rewritten as tiles, which the layer then reads instead
+        for g, k in ((1, "w1"), (2, "w2")):
+            t = torch.empty(moe.moe_weight_tiles_bytes(d, g), dtype=torch.int8, device="cuda")
+            moe.moe_pack_weight_tiles(d, g, dev[k], t)
+            dev[k] = t
+        torch.cuda.synchronize()
     ws = torch.empty(moe.moe_layer_workspace_size(d), dtype=torch.uint8, device="cuda")
     out = torch.empty((w.M, w.K), dtype=torch.float16, device="cuda")
     stream = torch.cuda.Stream()  # a capturable stream (not the legacy default stream)
@@ -474,6 +486,8 @@ def main():
         "config": {"workload": workload_desc(w), "parallelism": "replicas" if world > 1 else "single GPU",
                    "launch": ("CUDA graph of the layer's launches (moe_layer_graph_launch)" if use_graph
                               else "stream launches (moe_layer_fwd)"),
+                   "weights": ("16 KiB tiles (MOE_WEIGHTS_TILES), packed once before timing" if args.weights == "tiles"
+                               else "[E][N][D] rows (MOE_WEIGHTS_ROWS)"),
                    "l2": "flushed before every timed step (512 MB write); int8 weights %.2f GB per step"
                          % ((alg["gmm1"]["bytes"] + alg["gmm2"]["bytes"]) / 1e9),
                    "active_experts": active},

@@ -51,7 +51,31 @@ typedef struct {
   int32_t I;    /* intermediate size (GMM1: 2I)   */
   int32_t E;    /* experts                        */
   int32_t topK; /* routes per token               */
+  int32_t weight_layout; /* layout of the w1 / w2 arguments: MOE_WEIGHTS_ROWS (0, what a
+                            zero-initialised field gives) or MOE_WEIGHTS_TILES (1); any
+                            other value is MOE_ERR_SHAPE                              */
 } moe_dims_t;
+
+/*
+ * Weight layouts.  A GEMM weight W has E experts, N output channels and a reduction
+ * depth D (GMM1: N = 2I, D = K; GMM2: N = K, D = I).
+ *   MOE_WEIGHTS_ROWS   W[E][N][D] int8, D contiguous.
+ *   MOE_WEIGHTS_TILES  the same values as 16 KiB tiles of 128 channels x 128 reduction
+ *                      steps, each tile one contiguous block, written by
+ *                      moe_pack_weight_tiles: the GEMMs then stream every pipeline
+ *                      stage of weights as one contiguous copy instead of 128 rows
+ *                      7 KiB apart (a read stream of the decode weights measured
+ *                      7.24 TB/s against 6.78 TB/s in the row order).  It plays the
+ *                      part of the page's packed ("NZ") weight, laid out offline.
+ *     Let NB = N / 128 and KB = 2 * ceil(D / 256) (tiles per channel block: the depth
+ *     is padded with zeros to a multiple of 256).  Tile (e, nb, kb) starts at byte
+ *     ((e * NB + nb) * KB + kb) * 16384; inside it, W[e][nb*128 + r][kb*128 + c]
+ *     (r, c in [0, 128)) sits at byte r * 128 + (((c / 16) ^ (r % 8)) * 16) + c % 16,
+ *     and the bytes of reduction steps kb*128 + c >= D are zero.  This is the image
+ *     a 128-byte-swizzled tensor copy of the 128 x 128 box leaves in shared memory.
+ */
+#define MOE_WEIGHTS_ROWS 0
+#define MOE_WEIGHTS_TILES 1
 
 typedef enum {
   MOE_OK = 0,
@@ -83,9 +107,10 @@ size_t moe_layer_workspace_size(const moe_dims_t* d);
  *   expert_idx [M][topK]   int32 expert of each route
  *   probs      [M][topK]   fp32 route weights (used as given, not renormalised)
  *   w1         [E][2I][K]  int8 GMM1 weights, K contiguous (the page's packed
- *                          weight1[e][k][n], transposed so the reduction runs along rows)
+ *                          weight1[e][k][n], transposed so the reduction runs along rows),
+ *                          or their tiles (d->weight_layout, see "Weight layouts")
  *   s1         [E][2I]     fp32 GMM1 per-channel scales
- *   w2         [E][K][I]   int8 GMM2 weights, I contiguous
+ *   w2         [E][K][I]   int8 GMM2 weights, I contiguous, or their tiles
  *   s2         [E][K]      fp32 GMM2 per-channel scales
  *   out        [M][K]      binary16 result (written for every token; a token with
  *                          no valid route gets zeros)
@@ -272,6 +297,24 @@ int32_t moe_front_reorder(const moe_dims_t* d, const uint16_t* x, const int32_t*
 size_t moe_gmm_workspace_size(const moe_dims_t* d);
 
 /*
+ * Bytes of the MOE_WEIGHTS_TILES form of GMM `gemm`'s weights (1: w1, N = 2I, D = K;
+ * 2: w2, N = K, D = I): E * (N / 128) * KB * 16384 with KB = 2 * ceil(D / 256).
+ * 0 if the dimensions are invalid or gemm is neither 1 nor 2 (d->weight_layout is
+ * not read).
+ */
+size_t moe_weight_tiles_bytes(const moe_dims_t* d, int32_t gemm);
+
+/*
+ * Writes the tiles of a row-layout weight (see "Weight layouts"): w [E][N][D] int8
+ * (MOE_WEIGHTS_ROWS), tiles >= moe_weight_tiles_bytes(d, gemm) bytes, both device
+ * memory, 16-byte aligned, not overlapping.  Done once when the weights are loaded;
+ * the layer then runs with d->weight_layout = MOE_WEIGHTS_TILES on the tile buffers.
+ * d->weight_layout is not read.  Asynchronous on `stream`; errors as the other
+ * entry points (MOE_ERR_SHAPE also for gemm outside {1, 2}).
+ */
+int32_t moe_pack_weight_tiles(const moe_dims_t* d, int32_t gemm, const int8_t* w, int8_t* tiles, void* stream);
+
+/*
  * GMM1 (page section "3. GMM1", with "2. Dispatch" fused as a gather): for each
  * valid expanded row d of expert e (rows cumsum[e]-count_e .. cumsum[e]-1):
  *   acc[n]   = sum_k a1[d][k] * w1[e][n][k]                (exact integer)
@@ -285,6 +328,7 @@ size_t moe_gmm_workspace_size(const moe_dims_t* d);
  *          runs GMM1 1.2x (16-row tiles) to 3.2x (tcgen05 pairs) slower on GB300:
  *          a gather moves 512 B per TMA instruction, a tiled box up to 16 KB.
  *   a1_bounds: NULL or the activation bounds of the rows a1[d] (see "Activation bounds");
+ *   w1: in the layout d->weight_layout names (w1[e][n][k] above is the row form's value);
  *   c1 [R][2I] (rows >= cumsum[E-1] untouched)
  */
 int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* sorted_src_route, const int32_t* cumsum,
@@ -309,7 +353,7 @@ int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* p
  * GMM2 (page section "5. GMM2"): for each valid expanded row d of expert e,
  *   c2[d][k] = binary16(float(sum_i q2[d,i] * w2[e][k][i]) * s2[e][k])
  *   q2_f16 [R][I] binary16-coded int8 codes; q2_bounds: NULL or their activation
- *   bounds (see "Activation bounds"); c2 [R][K]
+ *   bounds (see "Activation bounds"); w2 in the layout d->weight_layout names; c2 [R][K]
  */
 int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cumsum, const int32_t* q2_bounds,
                  const int8_t* w2, const float* s2, uint16_t* c2, void* workspace, size_t workspace_bytes,

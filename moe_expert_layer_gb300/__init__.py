@@ -27,7 +27,12 @@ EXPORTS = [
     "moe_quant_tokens", "moe_quant_dispatch", "moe_front_reorder", "moe_gmm_workspace_size", "moe_gmm1",
     "moe_swiglu_quant", "moe_gmm2", "moe_combine_unpermute", "moe_route_sort_noalloc", "moe_selftest_wait_timeout",
     "moe_layer_graph_create", "moe_layer_graph_create_host", "moe_layer_graph_launch", "moe_layer_graph_destroy",
+    "moe_weight_tiles_bytes", "moe_pack_weight_tiles",
 ]
+
+# weight layouts (moe_dims_t.weight_layout)
+WEIGHTS_ROWS = 0
+WEIGHTS_TILES = 1
 
 
 class MoeError(RuntimeError):
@@ -38,11 +43,11 @@ class MoeError(RuntimeError):
 
 class moe_dims_t(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int32), ("K", ctypes.c_int32), ("I", ctypes.c_int32),
-                ("E", ctypes.c_int32), ("topK", ctypes.c_int32)]
+                ("E", ctypes.c_int32), ("topK", ctypes.c_int32), ("weight_layout", ctypes.c_int32)]
 
 
-def dims(M, K, I, E, topK):
-    return moe_dims_t(M, K, I, E, topK)
+def dims(M, K, I, E, topK, weight_layout=WEIGHTS_ROWS):
+    return moe_dims_t(M, K, I, E, topK, weight_layout)
 
 
 _lib = None
@@ -83,6 +88,8 @@ def load_library(path=None):
         "moe_combine_unpermute": ([D] + [vp] * 6, i32),
         "moe_route_sort_noalloc": ([D] + [vp] * 6, i32),
         "moe_selftest_wait_timeout": ([vp, ctypes.c_uint32, vp], i32),
+        "moe_weight_tiles_bytes": ([D, i32], sz),
+        "moe_pack_weight_tiles": ([D, i32, vp, vp, vp], i32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -129,6 +136,15 @@ def moe_route_sort_workspace_size(d):
 
 def moe_gmm_workspace_size(d):
     return load_library().moe_gmm_workspace_size(ctypes.byref(d))
+
+
+def moe_weight_tiles_bytes(d, gemm):
+    return load_library().moe_weight_tiles_bytes(ctypes.byref(d), gemm)
+
+
+def moe_pack_weight_tiles(d, gemm, w, tiles, stream=None):
+    _check("moe_pack_weight_tiles", load_library().moe_pack_weight_tiles(
+        ctypes.byref(d), gemm, _p(w), _p(tiles), _stream(stream)))
 
 
 def moe_layer_fwd(d, x, expert_idx, probs, w1, s1, w2, s2, out, workspace, stream=None):

@@ -80,6 +80,8 @@ struct GemmCfg {
   // slots in order (a group never tests the parity of a phase it skipped)
   static_assert(STAGES % kGroups == 0, "ring slots per group");
   static_assert(X_HALF_BYTES % 1024 == 0, "1024-B alignment of swizzled tiles");
+  static_assert(kBN == kWTileRows && kSubK == kWTileDepth && W_SUB_BYTES == kWTileBytes && kBK == 2 * kWTileDepth,
+                "a stage is two adjacent weight tiles");
   static_assert(SMEM_BYTES + 9 * 1024 <= 227 * 1024, "shared memory");
 };
 
@@ -92,6 +94,8 @@ struct GemmArgs {
   int split_rows;  // this engine serves the experts with at most split_rows rows
   const int32_t* gather_route;  // null: tiled token boxes; else row d gathers token gather_route[d] / topK
   int topK;
+  const uint8_t* w_tiles;  // null: weights through the tensor map; else the tile layout
+  int w_kb;                // tiles per 128-channel block of the tile layout
 };
 
 // 4 int8 (one 32-bit word) -> two half2 {b0,b1}, {b2,b3}, exactly.
@@ -396,8 +400,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         uint8_t* ws = xs + Cfg::X_BYTES;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full_bar[slot], tx);
-          tma_load_2d(ws, &tm_w, kx, w_row, &full_bar[slot]);
-          tma_load_2d(ws + Cfg::W_SUB_BYTES, &tm_w, kx + kSubK, w_row, &full_bar[slot]);
+          if (args.w_tiles) {
+            // the stage's two 128-deep tiles are adjacent: one contiguous copy
+            const size_t t0 = ((size_t)it.e * n_cb + it.cb) * args.w_kb + 2 * kb;
+            bulk_load(ws, args.w_tiles + t0 * (size_t)Cfg::W_SUB_BYTES, (uint32_t)Cfg::W_BYTES, &full_bar[slot]);
+          } else {
+            tma_load_2d(ws, &tm_w, kx, w_row, &full_bar[slot]);
+            tma_load_2d(ws + Cfg::W_SUB_BYTES, &tm_w, kx + kSubK, w_row, &full_bar[slot]);
+          }
           if (!gather) {
 #pragma unroll
             for (int q = 0; q < kQuarters; ++q)
@@ -605,6 +615,8 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.split_rows = p.split_rows;
   a.gather_route = p.gather_route;
   a.topK = p.topK;
+  a.w_tiles = p.w_kb ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;
+  a.w_kb = p.w_kb;
   grouped_gemm_kernel<T, GATHER><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
   return cudaGetLastError();
 }

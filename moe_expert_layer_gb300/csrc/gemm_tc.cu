@@ -94,6 +94,7 @@ constexpr int kWBytes = kBM * kBK;  // [128][128] int8, 128-B swizzled rows
 constexpr int kXHalfBytes = kHalfRows * 128;  // [128 rows][64] binary16, 128-B swizzled rows
 constexpr int kXBytes = 2 * kXHalfBytes;
 static_assert(kXHalfBytes % 1024 == 0, "1024-B alignment of swizzled tiles");
+static_assert(kBM == kWTileRows && kBK == kWTileDepth && kWBytes == kWTileBytes, "a weight stage is one tile");
 constexpr int kSmemBytes = kWStages * kWBytes + kStages * kXBytes + 1024;
 constexpr int kWProducerWarp = 0, kMmaWarp = 1, kXProducerWarp = 2, kRelayWarp = 3, kConvWarp0 = 4,
               kNumConvWarps = 4, kDrainWarp0 = 8, kNumDrainWarps = 16;
@@ -112,6 +113,8 @@ struct Args {
   const int32_t* bounds;  // [E][kBoundSegments] activation bounds, or null (1024-deep chunks)
   const int32_t* gather_route;  // null: tiled token boxes; else row d gathers token gather_route[d] / topK
   int topK;
+  const uint8_t* w_tiles;  // null: weights through the tensor map; else the tile layout
+  int w_kb;                // tiles per 128-channel block of the tile layout
 #ifdef MOE_GEMM_PROFILE
   unsigned long long* prof;
 #endif
@@ -532,12 +535,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = pair; j < total; j += npairs) {
           const Item it = decode_item(j, wl, e_hint);
           const int w_row = it.e * args.N + it.cb * kPairCh + (int)rank * kBM;
+          // tile layout: this CTA's 128-channel block, its tiles in reduction order.  A
+          // block past the expert's channels (N % 256 == 128, second CTA of the last
+          // channel block) reads the expert's last block instead: finite int8 values
+          // whose output channels are never stored, and never a tile past the buffer.
+          const uint8_t* wt = nullptr;
+          if (args.w_tiles) {
+            const int nbk = args.N / kBM;
+            const int nb = min(it.cb * (kPairCh / kBM) + (int)rank, nbk - 1);
+            wt = args.w_tiles + ((size_t)it.e * nbk + nb) * (size_t)args.w_kb * kWBytes;
+          }
           for (int kb = 0; kb < nk; ++kb, ++n) {
             const int slot = n % SW;
             if (!PROF_WAIT(0, wait_or_abort(&wempty_bar[slot], ((n / SW) & 1) ^ 1, abort_flag, args.status)))
               goto w_done;
             mbar_arrive_expect_tx(&wfull_bar[slot], (uint32_t)kWBytes);
-            tma_load_2d(smem_gen + slot * kWBytes, &tm_w, kb * kBK, w_row, &wfull_bar[slot]);
+            if (wt)
+              bulk_load(smem_gen + slot * kWBytes, wt + (size_t)kb * kWBytes, (uint32_t)kWBytes, &wfull_bar[slot]);
+            else
+              tma_load_2d(smem_gen + slot * kWBytes, &tm_w, kb * kBK, w_row, &wfull_bar[slot]);
           }
         }
       w_done:
@@ -866,6 +882,8 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.bounds = p.bounds;
   a.gather_route = p.gather_route;
   a.topK = p.topK;
+  a.w_tiles = p.w_kb ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;
+  a.w_kb = p.w_kb;
 #ifdef MOE_GEMM_PROFILE
   a.prof = g_gemm_prof;
   if (!a.prof) return cudaErrorInvalidValue;

@@ -46,7 +46,8 @@ struct GroupedGemmProblem {
                                     // activations are act[gather_route[d] / topK] (TMA gather)
   int topK, act_rows;
   const int32_t* cumsum;            // [E] inclusive prefix of rows per expert
-  const int8_t* w;                  // [E][N][Kd]
+  const int8_t* w;                  // [E][N][Kd] rows, or (w_kb > 0) the tile layout
+  int w_kb;                         // 0: rows; else 128-deep tiles per 128-channel block
   const float* scale;               // [E][N]
   uint16_t* C;                      // [R][N]
   int R, E, N, Kd;
@@ -59,5 +60,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream
 bool grouped_gemm_reads_bounds(int R, int E);  // whether the engine it picks uses activation bounds
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream);  // gemm_hmma.cu
 cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream);  // gemm_tc.cu
+
+// weight_tiles.cu: the MOE_WEIGHTS_TILES layout (include/moe_layer.h) of a weight
+// [E][N][D]: 16 KiB tiles of 128 channels x 128 reduction bytes, 128-byte swizzled,
+// weight_tile_kb(D) tiles per 128-channel block (the depth zero-padded to 256).
+constexpr int kWTileRows = 128, kWTileDepth = 128, kWTileBytes = kWTileRows * kWTileDepth;
+inline int weight_tile_kb(int D) { return 2 * ((D + 255) / 256); }
+inline size_t weight_tiles_bytes(int E, int N, int D) {
+  return (size_t)E * (size_t)(N / kWTileRows) * (size_t)weight_tile_kb(D) * kWTileBytes;
+}
+cudaError_t launch_pack_weight_tiles(const int8_t* w, int E, int N, int D, int8_t* tiles, cudaStream_t stream);
 
 }  // namespace moe

@@ -23,7 +23,8 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int32_t check_dims(const moe_dims_t* d) {
+// The shape preconditions (d->weight_layout not read).
+int32_t check_shape(const moe_dims_t* d) {
   if (!d) return MOE_ERR_NULL;
   if (d->M < 1 || d->topK < 1 || d->E < d->topK || d->E > 1023) return MOE_ERR_SHAPE;
   if (d->K < 128 || d->K > 16384 || d->K % 128) return MOE_ERR_SHAPE;
@@ -31,6 +32,18 @@ int32_t check_dims(const moe_dims_t* d) {
   const int64_t R = (int64_t)d->M * d->topK;
   if (R >= (int64_t)1 << 24) return MOE_ERR_SHAPE;
   return MOE_OK;
+}
+
+int32_t check_dims(const moe_dims_t* d) {
+  const int32_t rc = check_shape(d);
+  if (rc != MOE_OK) return rc;
+  if (d->weight_layout != MOE_WEIGHTS_ROWS && d->weight_layout != MOE_WEIGHTS_TILES) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+// Tiles per 128-channel block of a GEMM's weights in the layout d names (0: rows).
+int weight_kb(const moe_dims_t* d, int D) {
+  return d->weight_layout == MOE_WEIGHTS_TILES ? moe::weight_tile_kb(D) : 0;
 }
 
 int32_t check_device() {
@@ -131,6 +144,7 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   g1.act_rows = R;
   g1.cumsum = cumsum;
   g1.w = w1;
+  g1.w_kb = weight_kb(d, K);
   g1.scale = s1;
   g1.C = c1;
   g1.R = R;
@@ -150,6 +164,7 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   g2.act_rows = R;
   g2.cumsum = cumsum;
   g2.w = w2;
+  g2.w_kb = weight_kb(d, I);
   g2.scale = s2;
   g2.C = c2;
   g2.R = R;
@@ -414,6 +429,22 @@ size_t moe_gmm_workspace_size(const moe_dims_t* d) {
   return kAlign;
 }
 
+size_t moe_weight_tiles_bytes(const moe_dims_t* d, int32_t gemm) {
+  if (check_shape(d) != MOE_OK || (gemm != 1 && gemm != 2)) return 0;
+  return gemm == 1 ? moe::weight_tiles_bytes(d->E, 2 * d->I, d->K) : moe::weight_tiles_bytes(d->E, d->K, d->I);
+}
+
+int32_t moe_pack_weight_tiles(const moe_dims_t* d, int32_t gemm, const int8_t* w, int8_t* tiles, void* stream) {
+  int32_t rc = check_shape(d);
+  if (rc != MOE_OK) return rc;
+  if (gemm != 1 && gemm != 2) return MOE_ERR_SHAPE;
+  if (!w || !tiles) return MOE_ERR_NULL;
+  if (!aligned16(w) || !aligned16(tiles)) return MOE_ERR_ALIGN;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  const int N = gemm == 1 ? 2 * d->I : d->K, D = gemm == 1 ? d->K : d->I;
+  return launch_status(moe::launch_pack_weight_tiles(w, d->E, N, D, tiles, static_cast<cudaStream_t>(stream)));
+}
+
 int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* sorted_src_route, const int32_t* cumsum,
                  const int32_t* a1_bounds, const int8_t* w1, const float* s1, uint16_t* c1, void* workspace,
                  size_t workspace_bytes, void* stream) {
@@ -430,6 +461,7 @@ int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* sor
   g.act_rows = sorted_src_route ? d->M : d->M * d->topK;
   g.cumsum = cumsum;
   g.w = w1;
+  g.w_kb = weight_kb(d, d->K);
   g.scale = s1;
   g.C = c1;
   g.R = d->M * d->topK;
@@ -471,6 +503,7 @@ int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cum
   g.act_rows = d->M * d->topK;
   g.cumsum = cumsum;
   g.w = w2;
+  g.w_kb = weight_kb(d, d->I);
   g.scale = s2;
   g.C = c2;
   g.R = d->M * d->topK;

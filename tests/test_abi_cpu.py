@@ -76,3 +76,29 @@ def test_entry_points_reject_before_touching_the_device(lib):
     # misaligned pointers -> MOE_ERR_ALIGN
     p = 4096 + 2
     assert lib.moe_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, 4096, 1 << 30, None) == -3
+
+
+def test_weight_tiles_sizes_and_checks(lib):
+    """Tile-buffer sizes follow the documented layout (E * N/128 * KB * 16 KiB, KB =
+    2 * ceil(D / 256)); invalid layouts and GEMM numbers are refused on the host."""
+    import moe_expert_layer_gb300 as moe
+    d = moe.dims(128, 7168, 2048, 256, 8)
+    assert moe.moe_weight_tiles_bytes(d, 1) == 256 * (4096 // 128) * 56 * 16384   # GMM1: N = 2I, D = K
+    assert moe.moe_weight_tiles_bytes(d, 2) == 256 * (7168 // 128) * 16 * 16384   # GMM2: N = K, D = I
+    p = moe.dims(8192, 4096, 1408, 64, 6)
+    assert moe.moe_weight_tiles_bytes(p, 2) == 64 * 32 * 12 * 16384   # I = 1408: 11 tiles padded to 12
+    assert moe.moe_weight_tiles_bytes(moe.dims(16, 256, 192, 8, 2), 1) == 8 * 3 * 2 * 16384
+    assert moe.moe_weight_tiles_bytes(d, 0) == 0 and moe.moe_weight_tiles_bytes(d, 3) == 0
+    assert moe.moe_weight_tiles_bytes(moe.dims(16, 100, 256, 8, 2), 1) == 0
+    # the layout field: tiles accepted, anything else refused; the size queries ignore it
+    t = moe.dims(128, 7168, 2048, 256, 8, moe.WEIGHTS_TILES)
+    assert moe.moe_layer_workspace_size(t) == moe.moe_layer_workspace_size(d) > 0
+    assert moe.moe_layer_workspace_size(moe.dims(128, 7168, 2048, 256, 8, 2)) == 0
+    assert moe.moe_weight_tiles_bytes(moe.dims(128, 7168, 2048, 256, 8, 7), 1) == moe.moe_weight_tiles_bytes(d, 1)
+    bad_layout = moe.dims(16, 256, 256, 8, 2, -1)
+    assert lib.moe_layer_fwd(ctypes.byref(bad_layout), *([None] * 9), 0, None) == -2
+    assert lib.moe_gmm1(ctypes.byref(bad_layout), *([None] * 8), 0, None) == -2
+    small = moe.dims(16, 256, 256, 8, 2)
+    assert lib.moe_pack_weight_tiles(ctypes.byref(small), 3, 4096, 4096, None) == -2
+    assert lib.moe_pack_weight_tiles(ctypes.byref(small), 1, None, 4096, None) == -1
+    assert lib.moe_pack_weight_tiles(ctypes.byref(small), 1, 4096 + 8, 4096, None) == -3

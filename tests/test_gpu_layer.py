@@ -20,14 +20,32 @@ if torch.cuda.is_available():
     from gpu_util import assert_bits_equal, assert_out_close, dev, empty, host, upload_inputs
 
 
-def run_layer(w, inp_dev, out=None, ws=None):
-    d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
+LAYOUTS = [0, 1]
+LAYOUT_IDS = ["wrows", "wtiles"]
+
+
+def layer_weights(d, inp_dev, layout):
+    """(w1, w2) on the device in the given layout; the tiles are packed once by the
+    library and kept with the uploaded inputs."""
+    if layout == 0:
+        return inp_dev["w1"], inp_dev["w2"]
+    if "w1_tiles" not in inp_dev:
+        for g, k in ((1, "w1"), (2, "w2")):
+            t = empty(moe.moe_weight_tiles_bytes(d, g), torch.int8)
+            moe.moe_pack_weight_tiles(d, g, inp_dev[k], t)
+            inp_dev[k + "_tiles"] = t
+    return inp_dev["w1_tiles"], inp_dev["w2_tiles"]
+
+
+def run_layer(w, inp_dev, out=None, ws=None, layout=0):
+    d = moe.dims(w.M, w.K, w.I, w.E, w.topK, layout)
     if ws is None:
         ws = empty(moe.moe_layer_workspace_size(d), torch.uint8)
     if out is None:
         out = empty((w.M, w.K), torch.float16)
-    moe.moe_layer_fwd(d, inp_dev["x"], inp_dev["expert_idx"], inp_dev["probs"], inp_dev["w1"],
-                      inp_dev["s1"], inp_dev["w2"], inp_dev["s2"], out, ws)
+    w1, w2 = layer_weights(d, inp_dev, layout)
+    moe.moe_layer_fwd(d, inp_dev["x"], inp_dev["expert_idx"], inp_dev["probs"], w1,
+                      inp_dev["s1"], w2, inp_dev["s2"], out, ws)
     return out, ws
 
 
@@ -41,11 +59,12 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
 @pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
-def test_layer_small_full_parity(w):
+def test_layer_small_full_parity(w, layout):
     inp = synth.make_inputs(w)
     ref, it = oracle.layer_fwd(inp, intermediates=True)
-    out, ws = run_layer(w, upload_inputs(inp))
+    out, ws = run_layer(w, upload_inputs(inp), layout=layout)
     got = host(out)
     assert moe.moe_workspace_status(ws) == 0
     assert_out_close(got, ref)
@@ -63,12 +82,13 @@ EXTREME = [
 ]
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
 @pytest.mark.parametrize("w", EXTREME, ids=[w.name for w in EXTREME])
-def test_layer_extreme_dims(w):
+def test_layer_extreme_dims(w, layout):
     """The ABI's limits (K = 16384, I = 8192, E = 1023, topK = E), full parity."""
     inp = synth.make_inputs(w)
     ref = oracle.layer_fwd(inp)
-    out, ws = run_layer(w, upload_inputs(inp))
+    out, ws = run_layer(w, upload_inputs(inp), layout=layout)
     got = host(out)
     assert moe.moe_workspace_status(ws) == 0
     assert_out_close(got, ref)
@@ -134,22 +154,27 @@ def test_layer_graph_matches_stream_launches(name):
         moe.moe_layer_graph_destroy(g)
 
 
-def test_layer_host_graph_matches_host_entry_point():
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
+def test_layer_host_graph_matches_host_entry_point(layout):
     """The host-buffer graph (copies in, layer, copy out) gives moe_layer_fwd_host's
-    output bit for bit, and follows new contents of the pinned input buffers."""
+    output bit for bit, and follows new contents of the pinned input buffers; the
+    weight layout changes nothing in the output."""
     w = next(c for c in SMALL if c.name == "ragged")
     inp = synth.make_inputs(w)
     dv = upload_inputs(inp)
-    d = moe.dims(w.M, w.K, w.I, w.E, w.topK)
+    d = moe.dims(w.M, w.K, w.I, w.E, w.topK, layout)
+    wt1, wt2 = layer_weights(d, dv, layout)
     hws = empty(moe.moe_layer_host_workspace_size(d), torch.uint8)
     xh = torch.from_numpy(inp["x"]).pin_memory()
     eih = torch.from_numpy(inp["expert_idx"]).pin_memory()
     prh = torch.from_numpy(inp["probs"]).pin_memory()
     ref = torch.empty((w.M, w.K), dtype=torch.float16).pin_memory()
-    moe.moe_layer_fwd_host(d, xh, eih, prh, dv["w1"], dv["s1"], dv["w2"], dv["s2"], ref, hws)
+    moe.moe_layer_fwd_host(d, xh, eih, prh, wt1, dv["s1"], wt2, dv["s2"], ref, hws)
+    rows, _ = run_layer(w, dv)  # row-layout weights, device buffers
+    assert torch.equal(ref, rows.cpu())
     stream = torch.cuda.Stream()
     outh = torch.full((w.M, w.K), float("nan"), dtype=torch.float16).pin_memory()
-    g = moe.moe_layer_graph_create_host(d, xh, eih, prh, dv["w1"], dv["s1"], dv["w2"], dv["s2"], outh, hws, stream)
+    g = moe.moe_layer_graph_create_host(d, xh, eih, prh, wt1, dv["s1"], wt2, dv["s2"], outh, hws, stream)
     try:
         moe.moe_layer_graph_launch(g, stream)
         stream.synchronize()
@@ -162,7 +187,7 @@ def test_layer_host_graph_matches_host_entry_point():
         moe.moe_layer_graph_launch(g, stream)
         stream.synchronize()
         ref2 = torch.empty_like(ref).pin_memory()
-        moe.moe_layer_fwd_host(d, xh, eih, prh, dv["w1"], dv["s1"], dv["w2"], dv["s2"], ref2, hws)
+        moe.moe_layer_fwd_host(d, xh, eih, prh, wt1, dv["s1"], wt2, dv["s2"], ref2, hws)
         assert torch.equal(outh, ref2)
     finally:
         moe.moe_layer_graph_destroy(g)
@@ -220,12 +245,13 @@ def _sample_tokens(M, n, seed):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
 @pytest.mark.parametrize("cfg", ["decode", "mid", "skewed", "prefill"])
-def test_layer_full_size_sampled(cfg):
+def test_layer_full_size_sampled(cfg, layout):
     w = synth.CONFIGS[cfg]
     inp = synth.make_inputs(cfg)
     inp_dev = upload_inputs(inp)
-    out, ws = run_layer(w, inp_dev)
+    out, ws = run_layer(w, inp_dev, layout=layout)
     got = host(out)
     assert moe.moe_workspace_status(ws) == 0
     assert np.isfinite(got.astype(np.float32)).all()

@@ -20,8 +20,33 @@ if torch.cuda.is_available():
     from gpu_util import assert_bits_equal, assert_q2_close, dev, empty, host
 
 
-def _dims(w):
-    return moe.dims(w.M, w.K, w.I, w.E, w.topK)
+def _dims(w, layout=0):
+    return moe.dims(w.M, w.K, w.I, w.E, w.topK, layout)
+
+
+def tiles_ref(w):
+    """The weight-tile layout of include/moe_layer.h written out with numpy: w [E][N][D]
+    int8 -> tiles (e, nb, kb) of 128 channels x 128 reduction bytes, depth zero-padded to
+    a multiple of 256, 16-byte chunk c of tile row r stored at chunk c ^ (r % 8)."""
+    E, N, D = w.shape
+    KB = 2 * ((D + 255) // 256)
+    pad = np.zeros((E, N, KB * 128), np.int8)
+    pad[:, :, :D] = w
+    t = pad.reshape(E, N // 128, 128, KB, 8, 16).transpose(0, 1, 3, 2, 4, 5)  # e, nb, kb, r, chunk, byte
+    out = np.empty_like(t)
+    r = np.arange(128)
+    for c in range(8):
+        out[:, :, :, r, c ^ (r % 8), :] = t[:, :, :, r, c, :]
+    return out.reshape(-1)
+
+
+def _weights(d, gemm, w, layout):
+    """The GEMM weight on the device in the given layout (tiles packed by the library)."""
+    if layout == 0:
+        return dev(w)
+    tiles = empty(moe.moe_weight_tiles_bytes(d, gemm), torch.int8)
+    moe.moe_pack_weight_tiles(d, gemm, dev(w), tiles)
+    return tiles
 
 
 def _sort_on_gpu(w, expert_idx):
@@ -251,50 +276,73 @@ GEMM_CASES = [
 
 def _gmm1(d, xq, rs, topK, R, gather, bounds, w1, s1, c1, ws):
     """GMM1 on the oracle's token codes: gathered from token rows by the kernel
-    (the layer's path), or from expert-major rows dispatched here."""
+    (the layer's path), or from expert-major rows dispatched here.  w1 is on the
+    device already, in d's weight layout."""
     if gather:
         moe.moe_gmm1(d, dev(xq.astype(np.float16)), dev(rs["sorted_src_route"]), dev(rs["cumsum"]), bounds,
-                     dev(w1), dev(s1), c1, ws)
+                     w1, dev(s1), c1, ws)
     else:
-        moe.moe_gmm1(d, dev(_a1(xq, rs, topK, R)), None, dev(rs["cumsum"]), bounds, dev(w1), dev(s1), c1, ws)
+        moe.moe_gmm1(d, dev(_a1(xq, rs, topK, R)), None, dev(rs["cumsum"]), bounds, w1, dev(s1), c1, ws)
 
 
+LAYOUTS = [0, 1]
+LAYOUT_IDS = ["wrows", "wtiles"]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
 @pytest.mark.parametrize("gather", [True, False], ids=["gather", "rows"])
 @pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
 @pytest.mark.parametrize("w", GEMM_CASES, ids=[w.name for w in GEMM_CASES])
-def test_gmm1_bit_exact(w, bounded, gather):
+def test_gmm1_bit_exact(w, bounded, gather, layout):
     inp, rs, xq, pts1 = _stage_inputs(w)
     Rv = w.R - rs["invalid"]
     _, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], inp["expert_idx"], inp["w1"], inp["s1"], Rv)
-    d = _dims(w)
+    d = _dims(w, layout)
     c1 = torch.full((w.R, 2 * w.I), float("nan"), dtype=torch.float16, device="cuda")
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
     bounds = dev(_bounds_ref(_a1(xq, rs, w.topK, w.R), rs["cumsum"], w.E)) if bounded else None
-    _gmm1(d, xq, rs, w.topK, w.R, gather, bounds, inp["w1"], inp["s1"], c1, ws)
+    _gmm1(d, xq, rs, w.topK, w.R, gather, bounds, _weights(d, 1, inp["w1"], layout), inp["s1"], c1, ws)
     assert moe.moe_workspace_status(ws) == 0
     assert_bits_equal(host(c1)[:Rv], c1_ref, "c1")
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
 @pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
 @pytest.mark.parametrize("w", GEMM_CASES, ids=[w.name for w in GEMM_CASES])
-def test_gmm2_bit_exact(w, bounded):
+def test_gmm2_bit_exact(w, bounded, layout):
     inp, rs, xq, pts1 = _stage_inputs(w)
     Rv = w.R - rs["invalid"]
     q2 = synth.int8_sym127(w.seed, 77, (Rv, w.I))
     _, c2_ref = oracle.gmm2(q2, rs["sorted_src_route"], inp["expert_idx"], inp["w2"], inp["s2"])
-    d = _dims(w)
+    d = _dims(w, layout)
     c2 = empty((w.R, w.K), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
     q2f = np.zeros((w.R, w.I), np.float16)
     q2f[:Rv] = q2
     bounds = dev(_bounds_ref(q2f, rs["cumsum"], w.E)) if bounded else None
-    moe.moe_gmm2(d, dev(q2f), dev(rs["cumsum"]), bounds, dev(inp["w2"]), dev(inp["s2"]), c2, ws)
+    moe.moe_gmm2(d, dev(q2f), dev(rs["cumsum"]), bounds, _weights(d, 2, inp["w2"], layout), dev(inp["s2"]), c2, ws)
     assert moe.moe_workspace_status(ws) == 0
     assert_bits_equal(host(c2)[:Rv], c2_ref, "c2")
 
 
+@pytest.mark.parametrize("E,N,D", [(3, 128, 128), (2, 384, 192), (2, 256, 64), (1, 128, 1408), (2, 128, 7168),
+                                   (3, 256, 320)])
+def test_pack_weight_tiles_layout(E, N, D):
+    """moe_pack_weight_tiles writes exactly the documented tile layout (bit for bit),
+    zeros in the depth padding included."""
+    w = synth.int8_sym127(E * N + D, 5, (E, N, D))
+    # GMM2 form: N = K (multiple of 128), D = I (multiple of 64)
+    d = moe.dims(1, N, D, E, 1)
+    tiles = torch.full((moe.moe_weight_tiles_bytes(d, 2),), 99, dtype=torch.int8, device="cuda")
+    moe.moe_pack_weight_tiles(d, 2, dev(w), tiles)
+    torch.cuda.synchronize()
+    assert tiles.numel() == tiles_ref(w).size
+    assert_bits_equal(host(tiles), tiles_ref(w), "tiles")
+
+
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
 @pytest.mark.parametrize("M,wv", [(8, 127), (40, 127), (40, -128)])
-def test_gmm_accumulator_exact_beyond_fp32_mantissa(M, wv):
+def test_gmm_accumulator_exact_beyond_fp32_mantissa(M, wv, layout):
     """Partial sums far above 2^24 that cancel to a small integer.  The reduction
     runs +127*wv terms, then small terms, then -127*wv terms: a single fp32
     accumulator would reach ~5.6e7 (ulp 4) while adding the small terms and lose
@@ -317,16 +365,17 @@ def test_gmm_accumulator_exact_beyond_fp32_mantissa(M, wv):
     rs = oracle.route_sort(ei, E)
     acc_ref, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], ei, w1, s1, M, want_acc=True)
     assert np.abs(acc_ref).max() < 2048 and np.count_nonzero(acc_ref) > acc_ref.size // 2
-    d = moe.dims(M, K, I, E, 1)
+    d = moe.dims(M, K, I, E, 1, layout)
     c1 = empty((M, 2 * I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    _gmm1(d, xq, rs, 1, M, True, None, w1, s1, c1, ws)
+    _gmm1(d, xq, rs, 1, M, True, None, _weights(d, 1, w1, layout), s1, c1, ws)
     got = host(c1).astype(np.float64)
     assert np.array_equal(got, acc_ref.astype(np.float64))
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
 @pytest.mark.parametrize("K", [2048, 4096, 7168])
-def test_gmm_bounds_at_the_limit(K):
+def test_gmm_bounds_at_the_limit(K, layout):
     """Chunks merged by the activation bounds, with partial sums reaching 2^24 (at
     K=2048 the merged chunk is the whole reduction: the single-chunk epilogue).
     Every row has sum |code| = 131072 = 2^24 / 128 over the first 2048 k (so those
@@ -351,26 +400,27 @@ def test_gmm_bounds_at_the_limit(K):
     a1 = _a1(xq, rs, 1, M)
     b = _bounds_ref(a1, rs["cumsum"], E)
     assert b[0, :2].sum() * 128 <= (1 << 24) and b[0, :3].sum() * 128 > (1 << 24) - (1 << 17)
-    d = moe.dims(M, K, I, E, 1)
+    d = moe.dims(M, K, I, E, 1, layout)
     c1 = empty((M, 2 * I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    _gmm1(d, xq, rs, 1, M, True, dev(b), w1, s1, c1, ws)
+    _gmm1(d, xq, rs, 1, M, True, dev(b), _weights(d, 1, w1, layout), s1, c1, ws)
     assert moe.moe_workspace_status(ws) == 0
     assert_bits_equal(host(c1), c1_ref, "c1")
 
 
+@pytest.mark.parametrize("layout", LAYOUTS, ids=LAYOUT_IDS)
 @pytest.mark.parametrize("gather", [True, False], ids=["gather", "rows"])
-def test_gmm_empty_experts_and_single_rows(gather):
+def test_gmm_empty_experts_and_single_rows(gather, layout):
     """Experts with 0 and 1 rows, and a row tile tail of every length."""
     w = synth.Workload("sparse", 23, 256, 64, 12, 1, "uniform", 61)
     inp, rs, xq, pts1 = _stage_inputs(w)
     inp["expert_idx"][:, 0] = np.array([0, 3, 3, 5, 5, 5] + [7] * 17, np.int32)
     rs = oracle.route_sort(inp["expert_idx"], w.E)
     _, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], inp["expert_idx"], inp["w1"], inp["s1"], w.R)
-    d = _dims(w)
+    d = _dims(w, layout)
     c1 = empty((w.R, 2 * w.I), torch.float16)
     ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
-    _gmm1(d, xq, rs, 1, w.R, gather, None, inp["w1"], inp["s1"], c1, ws)
+    _gmm1(d, xq, rs, 1, w.R, gather, None, _weights(d, 1, inp["w1"], layout), inp["s1"], c1, ws)
     assert_bits_equal(host(c1), c1_ref, "c1")
 
 
