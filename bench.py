@@ -69,7 +69,8 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- algorithmic work
 def algorithmic(w, expert_idx):
-    """Bytes and ops each stage must move / perform for one step."""
+    """Bytes and ops each stage must move / perform for one step: the algorithmic
+    work of each stage of the layer, counted from the shapes and the active experts."""
     R = w.M * w.topK
     active = int(np.unique(expert_idx[(expert_idx >= 0) & (expert_idx < w.E)]).size)
     K, I, M = w.K, w.I, w.M
