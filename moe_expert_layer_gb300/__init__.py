@@ -100,11 +100,16 @@ def load_library(path=None):
 
 
 def _p(t):
-    """Raw pointer of a tensor (device or host), or None."""
+    """Raw pointer of a tensor (device or host), or None.  The ABI takes dense
+    row-major arrays, so a tensor with any other strides (a transpose, a column
+    slice, an expanded view) is refused rather than read with the wrong layout."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError("the C ABI takes dense row-major arrays; got a tensor with shape %s and strides %s"
+                         % (tuple(t.shape), tuple(t.stride())))
     return t.data_ptr()
 
 

@@ -102,3 +102,17 @@ def test_weight_tiles_sizes_and_checks(lib):
     assert lib.moe_pack_weight_tiles(ctypes.byref(small), 3, 4096, 4096, None) == -2
     assert lib.moe_pack_weight_tiles(ctypes.byref(small), 1, None, 4096, None) == -1
     assert lib.moe_pack_weight_tiles(ctypes.byref(small), 1, 4096 + 8, 4096, None) == -3
+
+
+def test_binding_refuses_strided_tensors():
+    """The binding hands the library raw pointers of dense row-major arrays; a view
+    with other strides is refused before anything reaches the library."""
+    import torch
+    import moe_expert_layer_gb300 as moe
+    a = torch.zeros(8, 16, dtype=torch.float16)
+    assert moe._p(a) == a.data_ptr()
+    assert moe._p(a[2:]) == a[2:].data_ptr()          # a row range is still dense
+    assert moe._p(None) is None and moe._p(4096) == 4096
+    for bad in (a.t(), a[:, :8], torch.zeros(16, dtype=torch.float16).expand(8, 16)):
+        with pytest.raises(ValueError):
+            moe._p(bad)
