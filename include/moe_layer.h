@@ -19,8 +19,10 @@
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  No entry point synchronises, except moe_layer_fwd_host and
  *     moe_workspace_status, which say so.
- *   - Arrays are dense row-major with the last index contiguous; every pointer must
- *     be 16-byte aligned.
+ *   - Arrays are dense row-major with the last index contiguous.  Every device
+ *     pointer must be 16-byte aligned (the layer's workspace 256-byte aligned), and
+ *     every entry point checks this for the pointers it is given (MOE_ERR_ALIGN);
+ *     the host buffers of the _host entry points may have any alignment.
  *   - Preconditions checked on the host before anything is launched:
  *       M >= 1, 1 <= topK <= E <= 1023, K % 128 == 0, 128 <= K <= 16384,
  *       I % 64 == 0, 64 <= I <= 8192, M * topK < 2^24, current device sm_103.

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 
 #include <cuda_runtime.h>
 
@@ -22,6 +23,13 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every given (non-null) device pointer 16-byte aligned; optional arguments may be null.
+bool all_aligned16(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p && !aligned16(p)) return false;
+  return true;
+}
 
 // The shape preconditions (d->weight_layout not read).
 int32_t check_shape(const moe_dims_t* d) {
@@ -374,6 +382,8 @@ int32_t moe_route_sort(const moe_dims_t* d, const int32_t* expert_idx, int32_t* 
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!expert_idx || !sorted_src_route || !expanded_row_idx || !tokens_per_expert || !cumsum) return MOE_ERR_NULL;
+  if (!all_aligned16({expert_idx, sorted_src_route, expanded_row_idx, tokens_per_expert, cumsum, workspace}))
+    return MOE_ERR_ALIGN;
   const size_t need = moe::route_sort_workspace_bytes(d->M * d->topK, d->E);
   if (need && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
@@ -387,7 +397,7 @@ int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, const int32_t* 
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!x || !pts1 || (!xq_i8 && !xq_f16) || (a1_bounds && !expert_idx)) return MOE_ERR_NULL;
-  if (!aligned16(x) || (xq_i8 && !aligned16(xq_i8)) || (xq_f16 && !aligned16(xq_f16))) return MOE_ERR_ALIGN;
+  if (!all_aligned16({x, expert_idx, xq_i8, xq_f16, pts1, a1_bounds})) return MOE_ERR_ALIGN;
   if ((rc = check_device()) != MOE_OK) return rc;
   return launch_status(moe::launch_quant_tokens(x, d->M, d->K, xq_i8, xq_f16, pts1, nullptr, d->topK, nullptr,
                                                 expert_idx, d->E, a1_bounds, static_cast<cudaStream_t>(stream)));
@@ -399,7 +409,7 @@ int32_t moe_quant_dispatch(const moe_dims_t* d, const uint16_t* x, const int32_t
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!x || !expanded_row_idx || !a1_f16 || !pts1 || (a1_bounds && !expert_idx)) return MOE_ERR_NULL;
-  if (!aligned16(x) || !aligned16(a1_f16)) return MOE_ERR_ALIGN;
+  if (!all_aligned16({x, expert_idx, expanded_row_idx, a1_f16, pts1, a1_bounds})) return MOE_ERR_ALIGN;
   if ((rc = check_device()) != MOE_OK) return rc;
   return launch_status(moe::launch_quant_tokens(x, d->M, d->K, nullptr, nullptr, pts1, expanded_row_idx, d->topK,
                                                 a1_f16, expert_idx, d->E, a1_bounds,
@@ -415,7 +425,9 @@ int32_t moe_front_reorder(const moe_dims_t* d, const uint16_t* x, const int32_t*
   if (!x || !expert_idx || !sorted_src_route || !expanded_row_idx || !tokens_per_expert || !cumsum || !a1_f16 ||
       !pts1)
     return MOE_ERR_NULL;
-  if (!aligned16(x) || !aligned16(a1_f16)) return MOE_ERR_ALIGN;
+  if (!all_aligned16({x, expert_idx, sorted_src_route, expanded_row_idx, tokens_per_expert, cumsum, a1_f16, pts1,
+                      a1_bounds, workspace}))
+    return MOE_ERR_ALIGN;
   const size_t need = moe::route_sort_workspace_bytes(d->M * d->topK, d->E);
   if (need && (!workspace || workspace_bytes < need)) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
@@ -451,7 +463,7 @@ int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* sor
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!a1_f16 || !cumsum || !w1 || !s1 || !c1 || !workspace) return MOE_ERR_NULL;
-  if (!aligned16(a1_f16) || !aligned16(w1) || !aligned16(c1)) return MOE_ERR_ALIGN;
+  if (!all_aligned16({a1_f16, sorted_src_route, cumsum, a1_bounds, w1, s1, c1, workspace})) return MOE_ERR_ALIGN;
   if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   moe::GroupedGemmProblem g{};
@@ -482,7 +494,8 @@ int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* p
   if (rc != MOE_OK) return rc;
   if (!c1 || !pts1 || !sorted_src_route || !cumsum || !pts2 || (!q2_i8 && !q2_f16) || (q2_bounds && !expert_idx))
     return MOE_ERR_NULL;
-  if (!aligned16(c1) || (q2_i8 && !aligned16(q2_i8)) || (q2_f16 && !aligned16(q2_f16))) return MOE_ERR_ALIGN;
+  if (!all_aligned16({c1, pts1, sorted_src_route, cumsum, expert_idx, q2_i8, q2_f16, pts2, q2_bounds}))
+    return MOE_ERR_ALIGN;
   if ((rc = check_device()) != MOE_OK) return rc;
   return launch_status(moe::launch_swiglu_quant(c1, d->M * d->topK, d->I, d->E, d->topK, pts1, sorted_src_route,
                                                 cumsum, q2_i8, q2_f16, pts2, expert_idx, q2_bounds,
@@ -495,7 +508,7 @@ int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cum
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!q2_f16 || !cumsum || !w2 || !s2 || !c2 || !workspace) return MOE_ERR_NULL;
-  if (!aligned16(q2_f16) || !aligned16(w2) || !aligned16(c2)) return MOE_ERR_ALIGN;
+  if (!all_aligned16({q2_f16, cumsum, q2_bounds, w2, s2, c2, workspace})) return MOE_ERR_ALIGN;
   if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   moe::GroupedGemmProblem g{};
@@ -522,7 +535,7 @@ int32_t moe_combine_unpermute(const moe_dims_t* d, const uint16_t* c2, const flo
   int32_t rc = check_dims(d);
   if (rc != MOE_OK) return rc;
   if (!c2 || !pts2 || !expanded_row_idx || !probs || !out) return MOE_ERR_NULL;
-  if (!aligned16(c2) || !aligned16(out)) return MOE_ERR_ALIGN;
+  if (!all_aligned16({c2, pts2, expanded_row_idx, probs, out})) return MOE_ERR_ALIGN;
   if ((rc = check_device()) != MOE_OK) return rc;
   return launch_status(moe::launch_combine_unpermute(c2, pts2, expanded_row_idx, probs, d->M, d->K, d->topK, out,
                                                      static_cast<cudaStream_t>(stream)));

@@ -116,3 +116,20 @@ def test_binding_refuses_strided_tensors():
     for bad in (a.t(), a[:, :8], torch.zeros(16, dtype=torch.float16).expand(8, 16)):
         with pytest.raises(ValueError):
             moe._p(bad)
+
+
+def test_stage_entry_points_check_every_device_pointer_alignment(lib):
+    """Index, scale and bounds arrays are checked for 16-byte alignment too, before any
+    device call (so this runs without a GPU); optional arguments may be NULL."""
+    import moe_expert_layer_gb300 as moe
+    d = moe.dims(16, 256, 256, 8, 2)
+    A, U = 4096, 4096 + 4  # aligned, 4-byte aligned only (a valid int32/fp32 address)
+    assert lib.moe_route_sort(ctypes.byref(d), A, A, A, A, U, None, 0, None) == -3
+    assert lib.moe_quant_tokens(ctypes.byref(d), A, None, None, A, U, None, None) == -3
+    assert lib.moe_quant_dispatch(ctypes.byref(d), A, A, U, A, A, None, None) == -3
+    assert lib.moe_front_reorder(ctypes.byref(d), A, A, A, A, A, A, A, A, U, None, 0, None) == -3
+    assert lib.moe_gmm1(ctypes.byref(d), A, None, U, None, A, A, A, A, 256, None) == -3
+    assert lib.moe_gmm1(ctypes.byref(d), A, None, A, None, A, U, A, A, 256, None) == -3
+    assert lib.moe_swiglu_quant(ctypes.byref(d), A, A, U, A, None, None, A, A, None, None) == -3
+    assert lib.moe_gmm2(ctypes.byref(d), A, A, U, A, A, A, A, 256, None) == -3
+    assert lib.moe_combine_unpermute(ctypes.byref(d), A, A, A, U, A, None) == -3
