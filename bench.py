@@ -146,6 +146,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- reference arm
+REFERENCE_BUDGET_S = 150.0
 def run_reference(args, rank, world):
     """The CPU oracle, as it stands, on the host cores: each step evaluates a
     bounded sample of the workload's tokens (rank 0 only)."""
@@ -154,10 +155,18 @@ def run_reference(args, rank, world):
     import oracle
     w = synth.CONFIGS[args.workload]
     inp = synth.make_inputs(w)
-    n_tok = min(w.M, 16)
-    toks = np.arange(n_tok, dtype=np.int32)
     cores = os.cpu_count()
-    oracle.layer_tokens(inp, toks[:2])  # warm-up: page in the weights
+    # first call pages in the weights; the second estimates the cost of one token
+    oracle.layer_tokens(inp, np.arange(min(w.M, 2), dtype=np.int32))
+    t0 = time.perf_counter()
+    oracle.layer_tokens(inp, np.arange(min(w.M, 2), dtype=np.int32))
+    t_tok = (time.perf_counter() - t0) / min(w.M, 2)
+    # tokens per step: at most 16, and few enough that the warm-up and timed steps
+    # together stay near REFERENCE_BUDGET_S of host time for any --steps / --warmup
+    n_tok = int(max(1, min(w.M, 16, REFERENCE_BUDGET_S / (max(1, args.steps + args.warmup) * t_tok))))
+    toks = np.arange(n_tok, dtype=np.int32)
+    for _ in range(args.warmup):
+        oracle.layer_tokens(inp, toks)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle.layer_tokens(inp, toks)
