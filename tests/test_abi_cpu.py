@@ -133,3 +133,44 @@ def test_stage_entry_points_check_every_device_pointer_alignment(lib):
     assert lib.moe_swiglu_quant(ctypes.byref(d), A, A, U, A, None, None, A, A, None, None) == -3
     assert lib.moe_gmm2(ctypes.byref(d), A, A, U, A, A, A, A, 256, None) == -3
     assert lib.moe_combine_unpermute(ctypes.byref(d), A, A, A, U, A, None) == -3
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "moe_layer.h"
+
+int main(void) {
+  moe_dims_t ok = {128, 7168, 2048, 256, 8, MOE_WEIGHTS_ROWS};
+  moe_dims_t bad = {16, 100, 256, 8, 2, MOE_WEIGHTS_ROWS};
+  moe_layer_graph_t* g = 0;
+  printf("%zu %zu %zu\n", moe_layer_workspace_size(&ok), moe_layer_workspace_size(&bad),
+         moe_weight_tiles_bytes(&ok, 1));
+  printf("%d %d %d\n", (int)moe_layer_fwd(&bad, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0),
+         (int)moe_layer_fwd(&ok, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0),
+         (int)moe_layer_graph_create(&ok, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, &g));
+  printf("%s|%s\n", moe_status_string(MOE_ERR_SHAPE), moe_status_string(MOE_ERR_TIMEOUT));
+  return g != 0;
+}
+"""
+
+
+def test_plain_c_client_compiles_links_and_runs(lib, tmp_path):
+    """The ABI is consumable from C alone: a C99 program (-pedantic -Werror) includes the
+    header, links against the library and gets the documented host-side results without
+    a GPU (sizes, shape and null-pointer codes, status strings)."""
+    import subprocess
+    from moe_expert_layer_gb300 import build
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(build.LIB_PATH)
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                           "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                           "-L", libdir, "-lmoe_layer", "-Wl,-rpath," + libdir])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    import moe_expert_layer_gb300 as moe
+    ok = moe.dims(128, 7168, 2048, 256, 8)
+    sizes = [int(v) for v in out[0].split()]
+    assert sizes == [moe.moe_layer_workspace_size(ok), 0, 256 * 32 * 56 * 16384]
+    assert out[1].split() == ["-2", "-1", "-1"]
+    assert out[2] == "unsupported dimensions|device-side wait timed out"
