@@ -27,6 +27,11 @@
  *       M >= 1, 1 <= topK <= E <= 1023, K % 128 == 0, 128 <= K <= 16384,
  *       I % 64 == 0, 64 <= I <= 8192, M * topK < 2^24, current device sm_103.
  *     A violated precondition returns an error and launches nothing.
+ *   - The route tables a stage entry point takes (sorted_src_route,
+ *     expanded_row_idx, cumsum) must be what moe_route_sort (or moe_front_reorder)
+ *     wrote for the same expert_idx and dimensions: the kernels use their entries
+ *     as row indices without checking them, so other values read or write out of
+ *     bounds.  moe_layer_fwd produces them itself.
  *   - Routes whose expert id lies outside [0, E) are dropped: sorted after all
  *     valid routes, counted in no expert, expandedRowIdx = -1, and they add
  *     nothing to the output.  Their number is R - cumsum[E-1].
