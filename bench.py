@@ -498,8 +498,10 @@ def main():
                               else "stream launches (moe_layer_fwd)"),
                    "weights": ("16 KiB tiles (MOE_WEIGHTS_TILES), packed once before timing" if args.weights == "tiles"
                                else "[E][N][D] rows (MOE_WEIGHTS_ROWS)"),
-                   "l2": "flushed before every timed step (512 MB write); int8 weights %.2f GB per step"
-                         % ((alg["gmm1"]["bytes"] + alg["gmm2"]["bytes"]) / 1e9),
+                   "l2": "flushed before every timed step (512 MB write); the GEMMs move %.2f GB per "
+                         "step, %.2f GB of them int8 weights"
+                         % ((alg["gmm1"]["bytes"] + alg["gmm2"]["bytes"]) / 1e9,
+                            active * 3 * w.K * w.I / 1e9),
                    "active_experts": active},
         "int8_TOPS": round(layer_ops / (ms * 1e-3) / 1e12, 2),
         "roofline": roofline,
