@@ -147,6 +147,8 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- reference arm
 REFERENCE_BUDGET_S = 150.0
+
+
 def run_reference(args, rank, world):
     """The CPU oracle, as it stands, on the host cores: each step evaluates a
     bounded sample of the workload's tokens (rank 0 only)."""

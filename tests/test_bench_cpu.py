@@ -1,0 +1,59 @@
+"""Host logic of the benchmark that decides whether a measurement is valid or what
+it reports, run on CPU: the clock-sample summary (throttle reasons, the SM clock
+under load) and the ncu traffic record, which is used only while the kernel
+source is unchanged since the capture."""
+import hashlib
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _line(sm, reasons=("Not Active",) * 4, mx=2070):
+    # index, clocks.sm, clocks.max.sm, power.draw, reasons.active, hw_slowdown,
+    # hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+    return ", ".join(["0", str(sm), str(mx), "812.3", "0x0000000000000000"] + list(reasons))
+
+
+def test_clock_summary_median_of_the_busy_half_and_reasons():
+    c = bench.ClockSampler(0)
+    c.lines = [_line(v) for v in (345, 345, 2070, 2055, 2070, 1980)] + ["garbage", ""]
+    s = c.summary()
+    assert s["samples"] == 6 and s["sm_max_mhz"] == 2070.0
+    # the idle edges (345 MHz) fall in the lower half: median of 2055, 2070, 2070
+    assert s["sm_mhz"] == 2070.0
+    assert s["reasons"] == []
+
+
+def test_clock_summary_reports_each_throttle_reason():
+    c = bench.ClockSampler(0)
+    c.lines = [_line(1500, ("Active", "Not Active", "Not Active", "Not Active")),
+               _line(1490, ("Not Active", "Not Active", "Active", "Active")),
+               _line(1510)]
+    s = c.summary()
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+
+
+def test_clock_summary_without_samples():
+    c = bench.ClockSampler(0)
+    c.lines = ["[N/A], [N/A]"]
+    assert c.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_traffic_record_only_for_the_captured_source(tmp_path, monkeypatch):
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel v1\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()
+    (prof / "gmm1_decode_ncu.md").write_text(
+        "summary\n\n    traffic_bytes_per_launch: 123456789\n    source_sha256: %s\n" % digest)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("gmm1", "decode", str(src)) == 123456789
+    assert bench.traffic_record("gmm1", "prefill", str(src)) is None  # no capture of that workload
+    src.write_text("// kernel v2\n")  # the kernel changed since the counters were taken
+    assert bench.traffic_record("gmm1", "decode", str(src)) is None
