@@ -157,7 +157,6 @@ def run_reference(args, rank, world):
     import oracle
     w = synth.CONFIGS[args.workload]
     inp = synth.make_inputs(w)
-    cores = os.cpu_count()
     # first call pages in the weights; the second estimates the cost of one token
     oracle.layer_tokens(inp, np.arange(min(w.M, 2), dtype=np.int32))
     t0 = time.perf_counter()
@@ -167,6 +166,7 @@ def run_reference(args, rank, world):
     # together stay near REFERENCE_BUDGET_S of host time for any --steps / --warmup
     n_tok = int(max(1, min(w.M, 16, REFERENCE_BUDGET_S / (max(1, args.steps + args.warmup) * t_tok))))
     toks = np.arange(n_tok, dtype=np.int32)
+    cores = min(n_tok, oracle.max_threads())  # the per-token loop runs one token per thread
     for _ in range(args.warmup):
         oracle.layer_tokens(inp, toks)
     t0 = time.perf_counter()
@@ -200,7 +200,7 @@ def cpu_baseline(w, inp):
         if time.perf_counter() - t0 > 12.0:
             break
     dt = time.perf_counter() - t0
-    return {"value": n_tok * reps / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": n_tok * reps / dt, "unit": UNIT, "cores": min(n_tok, oracle.max_threads()), "kind": "oracle",
             "sample": "%d x %d tokens of the %s workload (per-token oracle evaluation, %.1f s)" % (
                 reps, n_tok, w.name, dt)}
 

@@ -53,6 +53,7 @@ def _load():
             "oracle_unpermute": ([ci, ci, ci, vp, vp, vp, vp], None),
             "oracle_layer_fwd": ([ci] * 5 + [vp] * 18, ci),
             "oracle_layer_tokens": ([ci] * 5 + [vp] * 7 + [ci, vp, vp], None),
+            "oracle_max_threads": ([], ci),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -239,3 +240,8 @@ def layer_tokens(inp, tokens):
                                 _p(w1), _p(_c(inp["s1"], np.float32)), _p(_c(inp["w2"], np.int8)),
                                 _p(_c(inp["s2"], np.float32)), tok.size, _p(tok), _p(out))
     return out.view(np.float16)
+
+
+def max_threads():
+    """Threads the oracle's OpenMP regions run on (omp_get_max_threads)."""
+    return int(_load().oracle_max_threads())

@@ -46,6 +46,7 @@
 #include <stdlib.h>
 #include <string.h>
 #include <math.h>
+#include <omp.h>
 
 /* ------------------------------------------------------------------ */
 /* binary16 <-> fp32 (compiler _Float16: IEEE conversions, RNE)        */
@@ -368,3 +369,7 @@ void oracle_layer_tokens(int M, int K, int I, int E, int topK, const uint16_t* x
     free(xq); free(c1); free(q2); free(c2); free(y); free(acc);
   }
 }
+
+/* Threads an OpenMP region of this library runs on (diagnostics: the benchmark
+ * reports how many host cores the oracle used).  No arithmetic. */
+int oracle_max_threads(void) { return omp_get_max_threads(); }
