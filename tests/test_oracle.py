@@ -126,6 +126,17 @@ def test_quant_golden_round_half_away():
     assert pts1[0] == np.float32(s[0])
 
 
+def test_quant_golden_divides_by_the_rounded_scale():
+    """Phase 2c divides each element by the binary32 scale (pinned where that
+    differs from multiplying by 127/amax or dividing x*127 by amax)."""
+    rows = read_golden("quant_divide_inexact_scale.txt")
+    for i in range(0, len(rows), 3):
+        x, q, s = rows[i:i + 3]
+        xq, pts1 = oracle.quant_tokens(np.array([x], np.float16))
+        assert list(xq[0]) == [int(v) for v in q], "row with amax %g" % max(abs(v) for v in x)
+        assert pts1[0] == np.float32(s[0])
+
+
 def test_quant_properties():
     x = synth.normal_f16(11, 1, (64, 512))
     x[5] = 0  # all-zero row
@@ -245,6 +256,30 @@ def test_combine_unpermute_closed_form():
     out = oracle.unpermute(dmat, expanded, probs).astype(np.float32)
     assert np.array_equal(out, [[0.25 * 2 + 0.75 * 2, 0.25 * 0.25 - 0.75 * 4, 0.25 * 0.5 + 0.75 * 8],
                                 [0.5 * 1.5, 0.5 * 0.25, -0.5 * 0.5]])
+
+
+def test_unpermute_golden_slot_order_multiply_then_add():
+    """Unpermute: fp32 accumulator from zero, slots in order, a rounded multiply then a
+    rounded add (pinned on cancelling sums where a fused multiply-add, a binary16
+    accumulator or the reverse slot order give other binary16 outputs)."""
+    rows = read_golden("unpermute_slot_order_fp32.txt")
+    n_tok = len(rows) // 3
+    topK = len(rows[0])
+    R = n_tok * topK
+    # expanded rows in an order other than the route order, so the gather is pinned too
+    expanded = np.array([(5 * r + 2) % R for r in range(R)], np.int32)
+    assert sorted(expanded) == list(range(R))
+    dmat = np.zeros((R, 1), np.float16)
+    probs = np.zeros((n_tok, topK), np.float32)
+    want = []
+    for t in range(n_tok):
+        dvals, p, out = rows[3 * t:3 * t + 3]
+        for j in range(topK):
+            dmat[expanded[t * topK + j], 0] = dvals[j]
+        probs[t] = np.array(p, np.float64).astype(np.float32)
+        want.append(out[0])
+    got = oracle.unpermute(dmat, expanded, probs).astype(np.float64)[:, 0]
+    assert list(got) == want
 
 
 def test_combine_saturates():
