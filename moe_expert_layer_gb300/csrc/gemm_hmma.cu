@@ -15,13 +15,17 @@
 // (512 * 127^2 < 2^23); each chunk's fp32 sum is converted to int32 and added in
 // integer registers, which makes the int32 accumulator bit-exact for any K.
 //
-// Data movement.  Weights stay int8 in HBM (they dominate the traffic): a TMA
-// box of 128 channels x 64 k lands in shared memory and each thread converts its
-// fragment to binary16 in registers (byte-permute into the 1024+v encoding, one
-// subtract).  Activations are binary16-coded int8 (produced so by the quant and
-// SwiGLU kernels), loaded by TMA with the 128-byte swizzle; for GMM1 each token
-// row is fetched by its own 1-row TMA box at the token index taken from the sort,
-// so no dispatched copy of the tokens is ever written.
+// Data movement.  Weights stay int8 in HBM (they dominate the traffic): each
+// 256-deep pipeline stage brings two boxes of 128 channels x 128 k into shared
+// memory (two tiled TMA copies in the row layout, one 32 KiB bulk copy in the
+// tile layout) and each thread converts its fragment to binary16 in registers
+// (byte-permute into the 1024+v encoding, one subtract).  Activations are
+// binary16-coded int8 (produced so by the quant-scatter and SwiGLU kernels) in
+// expert-major rows, loaded by tiled TMA boxes with the 128-byte swizzle.  The
+// GATHER instantiation instead reads token-major codes, gathering each tile's
+// token rows by index (tile::gather4, four rows per copy), so that the caller
+// needs no dispatched copy of the tokens; the layer itself keeps the dispatched
+// rows, which measured faster.
 //
 // Tiling.  One CTA computes 128 channels x T rows of one expert.  The work list
 // (expert, row tile) is derived by each CTA from cumsum; CTAs whose index lies
@@ -596,13 +600,13 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
       !encode_tensor_map_2d(&tx8, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.act_rows, 64,
                             gather ? 1 : 8))
     return cudaErrorInvalidValue;
-  static bool attr_set[kMaxDevices] = {};
+  static PerContextOnce attr_set;
   const int dev = current_device();
-  if (!attr_set[dev]) {
+  if (attr_set.needed(dev)) {
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<T, GATHER>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
+    attr_set.done(dev);
   }
   GemmArgs a;
   a.cumsum = p.cumsum;

@@ -855,9 +855,9 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.act, (uint64_t)p.Kd, (uint64_t)p.act_rows, 64,
                             GATHER ? 1 : kHalfRows))
     return cudaErrorInvalidValue;
-  static bool checked[kMaxDevices] = {};
+  static PerContextOnce checked;
   const int dev = current_device();
-  if (!checked[dev]) {
+  if (checked.needed(dev)) {
     // The warpgroups' register split (setmaxnreg) adds up to exactly the registers
     // the CTA is launched with; a build that launches with another count would
     // leave the drains' increase waiting forever, so it is refused here.
@@ -868,7 +868,7 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
     err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemBytes);
     if (err != cudaSuccess) return err;
-    checked[dev] = true;
+    checked.done(dev);
   }
   Args a;
   a.cumsum = p.cumsum;

@@ -5,11 +5,11 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
-#include <initializer_list>
 
 #include <cuda_runtime.h>
 
 #include "../../include/moe_layer.h"
+#include "abi_checks.h"
 #include "kernels.h"
 
 struct moe_layer_graph {
@@ -19,57 +19,20 @@ struct moe_layer_graph {
 
 namespace {
 
+using moe::aligned16;
+using moe::all_aligned16;
+using moe::check_device;
+using moe::check_dims;
+using moe::check_shape;
+using moe::launch_status;
+
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Every given (non-null) device pointer 16-byte aligned; optional arguments may be null.
-bool all_aligned16(std::initializer_list<const void*> ps) {
-  for (const void* p : ps)
-    if (p && !aligned16(p)) return false;
-  return true;
-}
-
-// The shape preconditions (d->weight_layout not read).
-int32_t check_shape(const moe_dims_t* d) {
-  if (!d) return MOE_ERR_NULL;
-  if (d->M < 1 || d->topK < 1 || d->E < d->topK || d->E > 1023) return MOE_ERR_SHAPE;
-  if (d->K < 128 || d->K > 16384 || d->K % 128) return MOE_ERR_SHAPE;
-  if (d->I < 64 || d->I > 8192 || d->I % 64) return MOE_ERR_SHAPE;
-  const int64_t R = (int64_t)d->M * d->topK;
-  if (R >= (int64_t)1 << 24) return MOE_ERR_SHAPE;
-  return MOE_OK;
-}
-
-int32_t check_dims(const moe_dims_t* d) {
-  const int32_t rc = check_shape(d);
-  if (rc != MOE_OK) return rc;
-  if (d->weight_layout != MOE_WEIGHTS_ROWS && d->weight_layout != MOE_WEIGHTS_TILES) return MOE_ERR_SHAPE;
-  return MOE_OK;
-}
 
 // Tiles per 128-channel block of a GEMM's weights in the layout d names (0: rows).
 int weight_kb(const moe_dims_t* d, int D) {
   return d->weight_layout == MOE_WEIGHTS_TILES ? moe::weight_tile_kb(D) : 0;
 }
-
-int32_t check_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_ARCH;
-  static int cached_dev = -2, cached_ok = 0;
-  if (dev != cached_dev) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return MOE_ERR_ARCH;
-    cached_ok = (major == 10 && minor == 3);
-    cached_dev = dev;
-  }
-  return cached_ok ? MOE_OK : MOE_ERR_ARCH;
-}
-
-int32_t launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
 
 // Layout of the layer workspace.
 struct Layout {

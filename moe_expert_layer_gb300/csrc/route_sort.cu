@@ -254,15 +254,15 @@ cudaError_t launch_route_sort(const int32_t* expert_idx, int R, int E, int32_t* 
                               int32_t* expanded_row_idx, int32_t* tokens_per_expert, int32_t* cumsum,
                               void* workspace, cudaStream_t stream, int max_blocks) {
   const size_t smem = sort_smem_bytes(E);  // 74 KB at E = 1023
-  static bool attr_set[kMaxDevices] = {};
+  static PerContextOnce attr_set;
   const int dev = current_device();
-  if (!attr_set[dev]) {
+  if (attr_set.needed(dev)) {
     const int most = (int)sort_smem_bytes(1023);
     cudaError_t e = cudaFuncSetAttribute(route_sort_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set.done(dev);
   }
   if (R <= kSingleBlockMaxRoutes) {
     route_sort_single_kernel<<<1, kSortThreads, smem, stream>>>(expert_idx, R, E, sorted_src_route,

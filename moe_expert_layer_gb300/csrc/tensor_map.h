@@ -46,6 +46,44 @@ inline int current_device() {
   return dev;
 }
 
+// Unique ID (cuCtxGetId) of the CUDA context current on this thread; 0 while the
+// runtime has not yet made one current, or if the driver lacks the query.  Host
+// state cached per device that belongs to a context -- kernel attributes, the
+// address of a __device__ array -- is valid only in the context it was made in: a
+// cudaDeviceReset, or a primary context released and created again, loads the
+// module anew.  Such caches keep this ID beside what they hold and redo the set-up
+// when it changes.
+inline unsigned long long context_id() {
+  typedef CUresult (*PFN_ctxGetCurrent)(CUcontext*);
+  typedef CUresult (*PFN_ctxGetId)(CUcontext, unsigned long long*);
+  static PFN_ctxGetCurrent get_current = nullptr;
+  static PFN_ctxGetId get_id = nullptr;
+  if (!get_current || !get_id) {
+    void* p = nullptr;
+    void* q = nullptr;
+    cudaDriverEntryPointQueryResult r1, r2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r1) != cudaSuccess ||
+        r1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) != cudaSuccess ||
+        r2 != cudaDriverEntryPointSuccess)
+      return 0;
+    get_id = reinterpret_cast<PFN_ctxGetId>(q);
+    get_current = reinterpret_cast<PFN_ctxGetCurrent>(p);
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// A one-time set-up per device and context: needed(dev) is true until done(dev) has
+// been called in the context current now (and again after that context is replaced).
+struct PerContextOnce {
+  unsigned long long ctx[kMaxDevices] = {};
+  bool needed(int dev) const { return ctx[dev] == 0 || ctx[dev] != context_id(); }
+  void done(int dev) { ctx[dev] = context_id(); }
+};
+
 inline int sm_count() {
   static int sms[kMaxDevices] = {};
   const int dev = current_device();

@@ -135,6 +135,30 @@ def test_stage_entry_points_check_every_device_pointer_alignment(lib):
     assert lib.moe_combine_unpermute(ctypes.byref(d), A, A, A, U, A, None) == -3
 
 
+def test_noalloc_sort_host_refusals(lib):
+    """moe_route_sort_noalloc makes moe_route_sort's host checks (shape, NULL, 16-byte
+    alignment of its five device pointers) plus its own size limit, all before any
+    device call (so this runs without a GPU)."""
+    import moe_expert_layer_gb300 as moe
+    d = moe.dims(16, 256, 256, 8, 2)
+    A, U = 4096, 4096 + 4
+    f = lib.moe_route_sort_noalloc
+    assert f(None, A, A, A, A, A, None) == -1
+    for bad in (moe.dims(0, 256, 256, 8, 2), moe.dims(16, 256, 256, 8, 9), moe.dims(16, 256, 256, 1024, 2),
+                moe.dims(16, 100, 256, 8, 2), moe.dims(16, 256, 256, 8, 2, 5)):
+        assert f(ctypes.byref(bad), A, A, A, A, A, None) == -2
+    big = moe.dims(moe.ROUTE_SORT_NOALLOC_MAX_ROUTES // 8 + 1, 256, 256, 16, 8)
+    assert f(ctypes.byref(big), A, A, A, A, A, None) == -2
+    for i in range(5):
+        ptrs = [A] * 5
+        ptrs[i] = None
+        assert f(ctypes.byref(d), *ptrs, None) == -1
+        ptrs[i] = U
+        assert f(ctypes.byref(d), *ptrs, None) == -3
+    # the regular sort refuses the same misaligned pointers the same way
+    assert lib.moe_route_sort(ctypes.byref(d), U, A, A, A, A, None, 0, None) == -3
+
+
 C_CLIENT = r"""
 #include <stdio.h>
 #include "moe_layer.h"
