@@ -1,6 +1,7 @@
 """Benchmark of the W8A8 MoE expert layer on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill] [--also tiny,decode,mid,skewed]
+                    [--impl reference]
 
 One step = one pass of the whole layer (FrontReorder: route sort and token quant
 with the scatter to expert-major rows, GMM1, SwiGLU + requant, GMM2, Combine + Unpermute) over one
@@ -9,9 +10,12 @@ every rank runs an independent replica of the layer on its own batch: the path
 has no exchange step, so there is no collective on the data path (weak scaling).
 
 Prints one JSON line on rank 0.  `value` is tokens/s of the whole job with the
-inputs resident in device memory; `e2e` repeats the measurement through the
-host-buffer entry point (moe_layer_fwd_host), host<->device copies included.
-`--impl reference` times the CPU oracle instead (on the host cores, rank 0 only).
+inputs resident in device memory on the headline workload (prefill, the largest
+configuration); `e2e` repeats the measurement through the host-buffer entry point
+(moe_layer_fwd_host), host<->device copies included; `workloads` carries the same
+step, stage and roofline figures for the other configurations, measured in the
+same run.  `--impl reference` times the CPU oracle instead (on the host cores,
+rank 0 only).
 """
 import argparse
 import hashlib
@@ -39,7 +43,11 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="decode", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", default="prefill", choices=sorted(synth.CONFIGS),
+                    help="the headline workload (the JSON line's value, roofline, e2e)")
+    ap.add_argument("--also", default="tiny,decode,mid,skewed",
+                    help="comma-separated workloads measured in the same run and reported under "
+                         "`workloads` (single GPU only; 'none' for none)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -259,44 +267,97 @@ def job_tokens_per_s(world, M, ms):
 
 
 # ----------------------------------------------------------------------------- GPU arm
-def main():
-    args = parse()
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
-        return run_reference(args, rank, world)
+class Gpu:
+    """What every workload measurement shares: the modules, the launching stream, the
+    L2 flush buffer, the process group."""
 
-    import torch
-    import torch.distributed as dist
-    import moe_expert_layer_gb300 as moe
-
-    torch.cuda.set_device(local_rank)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-
-    def barrier():
+    def __init__(self, world, rank, local_rank):
+        import torch
+        import torch.distributed as dist
+        import moe_expert_layer_gb300 as moe
+        self.torch, self.dist, self.moe = torch, dist, moe
+        self.world, self.rank, self.local_rank = world, rank, local_rank
+        torch.cuda.set_device(local_rank)
         if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        self.stream = torch.cuda.Stream()  # a capturable stream (not the legacy default stream)
+        self.flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # > L2 (126 MB)
 
-    w = synth.CONFIGS[args.workload]
-    inp = replica_inputs(w, rank)  # each rank its own batch, the same weights
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+        self.torch.cuda.synchronize()
+
+
+def step_stats(step_ms):
+    return {"mean": statistics.mean(step_ms), "median": statistics.median(step_ms), "min": min(step_ms)}
+
+
+def roofline_of(w, stage_ms, alg, peaks):
+    """The dominant GEMM stage against its bound: HBM when its bytes take longer at the
+    measured copy rate than its MACs at the measured dense 16-bit tensor rate, tensor
+    otherwise.  Both engines multiply the int8 codes as binary16 (kind::f16 / HMMA
+    f16), whose dense rate equals the bf16 rate the peak was measured with."""
+    dom = max(["gmm1", "gmm2"], key=lambda n: stage_ms[n])
+    src = engine_source(w)
+    kernel = "grouped_gemm_kernel" if src.endswith("gemm_hmma.cu") else \
+        "grouped_gemm_hmma (experts <= 32 rows) + grouped_gemm_pair_kernel (the rest)"
+    t_dom = stage_ms[dom] * 1e-3
+    t_hbm = alg[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg[dom]["ops"] / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        ach = alg[dom]["bytes"] / t_dom / 1e9
+        r = {"kernel": "%s (%s)" % (kernel, dom.upper()), "bound": "hbm", "achieved": round(ach, 1),
+             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 3),
+             "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, a copy's read + write rate)",
+             "algorithmic_bytes_per_launch": alg[dom]["bytes"]}
+    else:
+        ach = alg[dom]["ops"] / t_dom / 1e12
+        r = {"kernel": "%s (%s)" % (kernel, dom.upper()), "bound": "tensor", "achieved": round(ach, 1),
+             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 3),
+             "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst; the int8 "
+                            "codes run on the binary16 tensor path at the same rate)",
+             "algorithmic_ops_per_launch": alg[dom]["ops"]}
+    r["us_per_launch"] = round(stage_ms[dom] * 1e3, 2)
+    r["traffic"] = traffic_record(dom, w.name, src)
+    if r["frac"] > 1.0:
+        # the denominators are a plain copy and cuBLAS: a kernel that streams reads
+        # (no writes) or packed tiles can pass them; far above 1 would mean missing work
+        r["above_peak"] = True
+    return r
+
+
+def launches_per_step(w):
+    """Our kernels per layer call: the sort (fused into the quant kernel up to 4096
+    routes, one kernel up to 8192, three above), the quant, each GEMM (one engine up
+    to 24 rows per expert on average, both above), SwiGLU, combine."""
+    sort_launches = 0 if w.R <= 4096 else (1 if w.R <= 8192 else 3)
+    gemm_launches = 1 if w.R / w.E <= 24.0 else 2
+    return sort_launches + 1 + 2 * gemm_launches + 2
+
+
+def measure_workload(g, w, args, headline, keep_host=False):
+    """One workload: the layer step timed over args.steps steps (L2 flushed before
+    each), the stages timed apart through the stage entry points, and, for the
+    headline workload, the end-to-end host-buffer path.  Returns the report and the
+    host inputs (with the weights only if keep_host)."""
+    torch, moe, stream = g.torch, g.moe, g.stream
+    inp = replica_inputs(w, g.rank)  # each rank its own batch, the same weights
     dev = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in inp.items()}
+    host_inp = inp if keep_host else {k: inp[k] for k in ("x", "expert_idx", "probs")}
+    del inp
     layout = moe.WEIGHTS_TILES if args.weights == "tiles" else moe.WEIGHTS_ROWS
     d = moe.dims(w.M, w.K, w.I, w.E, w.topK, layout)
     if layout == moe.WEIGHTS_TILES:
         # once, at weight-load time (outside every timed region): the row-layout
         # weights rewritten as tiles, which the layer then reads instead
-        for g, k in ((1, "w1"), (2, "w2")):
-            t = torch.empty(moe.moe_weight_tiles_bytes(d, g), dtype=torch.int8, device="cuda")
-            moe.moe_pack_weight_tiles(d, g, dev[k], t)
+        for gi, k in ((1, "w1"), (2, "w2")):
+            t = torch.empty(moe.moe_weight_tiles_bytes(d, gi), dtype=torch.int8, device="cuda")
+            moe.moe_pack_weight_tiles(d, gi, dev[k], t)
             dev[k] = t
         torch.cuda.synchronize()
     ws = torch.empty(moe.moe_layer_workspace_size(d), dtype=torch.uint8, device="cuda")
     out = torch.empty((w.M, w.K), dtype=torch.float16, device="cuda")
-    stream = torch.cuda.Stream()  # a capturable stream (not the legacy default stream)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # > L2 (126 MB)
     graph = None
     if not args.no_graph:  # the layer's launches recorded once, replayed every step
         graph = moe.moe_layer_graph_create(d, dev["x"], dev["expert_idx"], dev["probs"], dev["w1"], dev["s1"],
@@ -311,33 +372,32 @@ def main():
 
     for _ in range(max(3, args.warmup)):
         step()
-    barrier()
+    g.barrier()
     if moe.moe_workspace_status(ws) != 0:
         raise RuntimeError("device status after warm-up: %d" % moe.moe_workspace_status(ws))
 
     # ---- timed region: K layer steps, L2 flushed before each, CUDA events on the stream
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(g.local_rank)
     clocks.start()
     time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    barrier()
+    g.barrier()
     t_wall = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            flush.fill_(i & 0xff)
+            g.flush.fill_(i & 0xff)
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
-    barrier()
+    g.barrier()
     t_wall = time.perf_counter() - t_wall
     clocks.stop()
-    use_graph = graph is not None
-    if use_graph:
+    if graph is not None:
         moe.moe_layer_graph_destroy(graph)
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, "cuda")
-    value = job_tokens_per_s(world, w.M, ms)
+    st = step_stats([a.elapsed_time(b) for a, b in ev])
+    ms = max_over_ranks(st["mean"], g.world, "cuda")
+    st = {k: max_over_ranks(v, g.world, "cuda") for k, v in st.items()}
 
     # ---- per-stage timing through the stage entry points (same kernels), for the roofline
     R = w.R
@@ -360,38 +420,38 @@ def main():
     def stages(evs):
         with torch.cuda.stream(stream):
             bounds.zero_()  # the layer clears them with its status word
-        ev = iter(evs)
-        next(ev).record(stream)
+        it = iter(evs)
+        next(it).record(stream)
         if fused_front:
             moe.moe_front_reorder(d, dev["x"], dev["expert_idx"], sorted_, expanded, tpe, cs, a1, pts1, b1, sws,
                                   stream)
         else:  # what moe_front_reorder launches above 4096 routes, timed apart
             moe.moe_route_sort(d, dev["expert_idx"], sorted_, expanded, tpe, cs, sws, stream)
-            next(ev).record(stream)
+            next(it).record(stream)
             moe.moe_quant_dispatch(d, dev["x"], dev["expert_idx"], expanded, a1, pts1, b1, stream)
-        next(ev).record(stream)
+        next(it).record(stream)
         moe.moe_gmm1(d, a1, None, cs, b1, dev["w1"], dev["s1"], c1, gws, stream)
-        next(ev).record(stream)
+        next(it).record(stream)
         moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, dev["expert_idx"], None, q2, pts2, b2, stream)
-        next(ev).record(stream)
+        next(it).record(stream)
         moe.moe_gmm2(d, q2, cs, b2, dev["w2"], dev["s2"], c2, gws, stream)
-        next(ev).record(stream)
+        next(it).record(stream)
         moe.moe_combine_unpermute(d, c2, pts2, expanded, dev["probs"], out, stream)
-        next(ev).record(stream)
+        next(it).record(stream)
 
     for _ in range(3):
         stages([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
     n_stage_steps = max(3, min(args.steps, 50))
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(n_stage_steps)]
-    barrier()
+    g.barrier()
     with torch.cuda.stream(stream):
         for i in range(n_stage_steps):
-            flush.fill_(i & 0xff)
+            g.flush.fill_(i & 0xff)
             stages(sev[i])
-    barrier()
+    g.barrier()
     stage_ms = {n: statistics.mean(s[j].elapsed_time(s[j + 1]) for s in sev) for j, n in enumerate(names)}
 
-    alg, active = algorithmic(w, inp["expert_idx"])
+    alg, active = algorithmic(w, host_inp["expert_idx"])
     peaks = load_peaks()
     stage_report = {}
     for n in names:
@@ -400,45 +460,29 @@ def main():
                "hbm_frac": round(alg[n]["bytes"] / t / 1e9 / peaks["hbm_gbs"], 3)}
         if "ops" in alg[n]:
             rep["TOPS"] = round(alg[n]["ops"] / t / 1e12, 2)
+            rep["tensor_frac"] = round(alg[n]["ops"] / t / 1e12 / peaks["bf16_tflops"], 3)
         stage_report[n] = rep
-    dom = max(["gmm1", "gmm2"], key=lambda n: stage_ms[n])
-    src = engine_source(w)
-    kernel = ("grouped_gemm_kernel" if src.endswith("gemm_hmma.cu") else "grouped_gemm_pair_kernel")
-    # Bound of the dominant GEMM: HBM when its bytes take longer at the measured copy
-    # rate than its MACs at the measured dense 16-bit tensor rate, tensor otherwise.
-    # Both engines multiply the int8 codes as binary16 (kind::f16 / HMMA f16), whose
-    # dense rate equals the bf16 rate the peak was measured with.
-    t_dom = stage_ms[dom] * 1e-3
-    t_hbm = alg[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = alg[dom]["ops"] / (peaks["bf16_tflops"] * 1e12)
-    if t_hbm >= t_tc:
-        ach = alg[dom]["bytes"] / t_dom / 1e9
-        roofline = {"kernel": "%s (%s)" % (kernel, dom.upper()), "bound": "hbm",
-                    "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(ach / peaks["hbm_gbs"], 3),
-                    "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
-                    "algorithmic_bytes_per_launch": alg[dom]["bytes"],
-                    "traffic": traffic_record(dom, w.name, src)}
-    else:
-        ach = alg[dom]["ops"] / t_dom / 1e12
-        roofline = {"kernel": "%s (%s)" % (kernel, dom.upper()), "bound": "tensor",
-                    "achieved": round(ach, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": round(ach / peaks["bf16_tflops"], 3),
-                    "peak_source": peaks["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst; the int8 "
-                                   "codes run on the binary16 tensor path at the same rate)",
-                    "algorithmic_ops_per_launch": alg[dom]["ops"],
-                    "traffic": traffic_record(dom, w.name, src)}
     layer_ops = alg["gmm1"]["ops"] + alg["gmm2"]["ops"]
+    rep = {
+        "workload": workload_desc(w), "ms_per_step": round(ms, 4),
+        "ms_per_step_median": round(st["median"], 4), "ms_per_step_min": round(st["min"], 4),
+        "value": round(job_tokens_per_s(g.world, w.M, ms), 1), "unit": UNIT,
+        "int8_TOPS": round(layer_ops / (ms * 1e-3) / 1e12, 2),
+        "roofline": roofline_of(w, stage_ms, alg, peaks), "stages": stage_report,
+        "gpu_launches_per_step": launches_per_step(w), "clocks": clocks.summary(),
+        "wall_s_timed_region": round(t_wall, 3), "active_experts": active,
+        "gemm_bytes": alg["gmm1"]["bytes"] + alg["gmm2"]["bytes"], "weight_bytes": active * 3 * w.K * w.I,
+        "launch": ("CUDA graph of the layer's launches (moe_layer_graph_launch)" if not args.no_graph
+                   else "stream launches (moe_layer_fwd)"),
+    }
 
-    # ---- end to end through the host-buffer entry point
-    e2e = None
-    if not args.no_e2e:
+    # ---- end to end through the host-buffer entry point (headline workload)
+    if headline and not args.no_e2e:
         hws = torch.empty(moe.moe_layer_host_workspace_size(d), dtype=torch.uint8, device="cuda")
-        xh = torch.from_numpy(inp["x"]).pin_memory()
-        eih = torch.from_numpy(inp["expert_idx"]).pin_memory()
-        prh = torch.from_numpy(inp["probs"]).pin_memory()
+        xh = torch.from_numpy(host_inp["x"]).pin_memory()
+        eih = torch.from_numpy(host_inp["expert_idx"]).pin_memory()
+        prh = torch.from_numpy(host_inp["probs"]).pin_memory()
         outh = torch.empty((w.M, w.K), dtype=torch.float16).pin_memory()
-
         hgraph = None
         if not args.no_graph:  # copies in, layer, copy out: recorded once
             hgraph = moe.moe_layer_graph_create_host(d, xh, eih, prh, dev["w1"], dev["s1"], dev["w2"], dev["s2"],
@@ -456,68 +500,126 @@ def main():
             host_step()
         n_e2e = max(3, min(args.steps, 100))
         tot = 0.0
-        barrier()
+        g.barrier()
         for i in range(n_e2e):
-            flush.fill_(i & 0xff)
+            g.flush.fill_(i & 0xff)
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             host_step()  # synchronises the stream before returning
             tot += time.perf_counter() - t0
-        barrier()
+        g.barrier()
         e_ms = 1e3 * tot / n_e2e
         if hgraph is not None:
             moe.moe_layer_graph_destroy(hgraph)
-        e_ms = max_over_ranks(e_ms, world, "cuda")
-        e2e = {"value": job_tokens_per_s(world, w.M, e_ms), "unit": UNIT,
-               "h2d_bytes_per_step": int(inp["x"].nbytes + inp["expert_idx"].nbytes + inp["probs"].nbytes),
-               "d2h_bytes_per_step": int(w.M * w.K * 2), "ms_per_step": round(e_ms, 4),
-               "path": ("moe_layer_graph_create_host + moe_layer_graph_launch, then a stream synchronise"
-                        if not args.no_graph else "moe_layer_fwd_host")}
+        e_ms = max_over_ranks(e_ms, g.world, "cuda")
+        rep["e2e"] = {"value": job_tokens_per_s(g.world, w.M, e_ms), "unit": UNIT,
+                      "h2d_bytes_per_step": int(host_inp["x"].nbytes + host_inp["expert_idx"].nbytes
+                                                + host_inp["probs"].nbytes),
+                      "d2h_bytes_per_step": int(w.M * w.K * 2), "ms_per_step": round(e_ms, 4),
+                      "path": ("moe_layer_graph_create_host + moe_layer_graph_launch, then a stream synchronise"
+                               if not args.no_graph else "moe_layer_fwd_host")}
+    return rep, host_inp
+
+
+def single_thread_oracle(inputs):
+    """The oracle on ONE host thread over a few tokens of each workload given
+    ({name: its host inputs}), next to the all-cores figure of cpu_baseline."""
+    import oracle
+    res = {}
+    prev = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        for name, inp in inputs.items():
+            w = synth.CONFIGS[name]
+            oracle.layer_tokens(inp, np.arange(1, dtype=np.int32))  # page in
+            n_tok = min(w.M, 4)
+            toks = np.arange(n_tok, dtype=np.int32)
+            t0 = time.perf_counter()
+            reps = 0
+            while True:
+                oracle.layer_tokens(inp, toks)
+                reps += 1
+                if time.perf_counter() - t0 > 3.0:
+                    break
+            dt = time.perf_counter() - t0
+            res[name] = {"value": n_tok * reps / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d x %d tokens of the %s workload (per-token oracle evaluation, %.1f s)"
+                                   % (reps, n_tok, name, dt)}
+    finally:
+        oracle.set_threads(prev)
+    return res
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    g = Gpu(world, rank, local_rank)
+    w = synth.CONFIGS[args.workload]
+    head, host_inp = measure_workload(g, w, args, headline=True)
+    g.torch.cuda.empty_cache()
+
+    # the other configurations, measured in the same run (one GPU only: under
+    # torchrun every rank would repeat them)
+    others, kept = {}, {}
+    extra = [n for n in args.also.split(",") if n and n != "none" and n != w.name] if world == 1 else []
+    one_thread = [] if args.no_cpu_baseline or world > 1 else ["tiny", "decode"]
+    for name in extra:
+        rep, hinp = measure_workload(g, synth.CONFIGS[name], args, headline=False, keep_host=name in one_thread)
+        rep.pop("launch", None)
+        others[name] = rep
+        if name in one_thread:
+            kept[name] = hinp
+        del hinp
+        g.torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
-            dist.barrier()
-            dist.destroy_process_group()
+            g.dist.barrier()
+            g.dist.destroy_process_group()
         return
 
-    cpu = None
+    cpu = cpu1 = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(w, inp)
+        cpu = cpu_baseline(w, synth.make_inputs(w))
+        for name in one_thread:
+            if name not in kept:
+                kept[name] = synth.make_inputs(name)
+        cpu1 = single_thread_oracle(kept)
 
-    # our kernels per layer call: the sort (fused into the quant kernel up to 4096
-    # routes, one kernel up to 8192, three above), the quant, each GEMM (one engine up
-    # to 24 rows per expert on average, both above), SwiGLU, combine
-    sort_launches = 0 if w.R <= 4096 else (1 if w.R <= 8192 else 3)
-    gemm_launches = 1 if w.R / w.E <= 24.0 else 2
-    launches_per_step = sort_launches + 1 + 2 * gemm_launches + 2
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "ms_per_step_median": head["ms_per_step_median"], "ms_per_step_min": head["ms_per_step_min"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic",
-        "config": {"workload": workload_desc(w), "parallelism": "replicas" if world > 1 else "single GPU",
-                   "launch": ("CUDA graph of the layer's launches (moe_layer_graph_launch)" if use_graph
-                              else "stream launches (moe_layer_fwd)"),
+        "config": {"workload": head["workload"], "parallelism": "replicas" if world > 1 else "single GPU",
+                   "launch": head["launch"],
                    "weights": ("16 KiB tiles (MOE_WEIGHTS_TILES), packed once before timing" if args.weights == "tiles"
                                else "[E][N][D] rows (MOE_WEIGHTS_ROWS)"),
                    "l2": "flushed before every timed step (512 MB write); the GEMMs move %.2f GB per "
                          "step, %.2f GB of them int8 weights"
-                         % ((alg["gmm1"]["bytes"] + alg["gmm2"]["bytes"]) / 1e9,
-                            active * 3 * w.K * w.I / 1e9),
-                   "active_experts": active},
-        "int8_TOPS": round(layer_ops / (ms * 1e-3) / 1e12, 2),
-        "roofline": roofline,
-        "stages": stage_report,
+                         % (head["gemm_bytes"] / 1e9, head["weight_bytes"] / 1e9),
+                   "active_experts": head["active_experts"]},
+        "int8_TOPS": head["int8_TOPS"],
+        "roofline": head["roofline"],
+        "stages": head["stages"],
         "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks.summary(),
-        "wall_s_timed_region": round(t_wall, 3),
+        "cpu_baseline_1thread": cpu1,
+        "e2e": head.get("e2e"),
+        "gpu_launches": head["gpu_launches_per_step"] * args.steps,
+        "clocks": head["clocks"],
+        "wall_s_timed_region": head["wall_s_timed_region"],
+        "workloads": others,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
+        g.dist.barrier()
+        g.dist.destroy_process_group()
 
 
 if __name__ == "__main__":

@@ -54,6 +54,7 @@ def _load():
             "oracle_layer_fwd": ([ci] * 5 + [vp] * 18, ci),
             "oracle_layer_tokens": ([ci] * 5 + [vp] * 7 + [ci, vp, vp], None),
             "oracle_max_threads": ([], ci),
+            "oracle_set_threads": ([ci], None),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -245,3 +246,8 @@ def layer_tokens(inp, tokens):
 def max_threads():
     """Threads the oracle's OpenMP regions run on (omp_get_max_threads)."""
     return int(_load().oracle_max_threads())
+
+
+def set_threads(n):
+    """Threads the oracle's OpenMP regions use from now on (diagnostics; no arithmetic)."""
+    _load().oracle_set_threads(int(n))

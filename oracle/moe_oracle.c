@@ -373,3 +373,7 @@ void oracle_layer_tokens(int M, int K, int I, int E, int topK, const uint16_t* x
 /* Threads an OpenMP region of this library runs on (diagnostics: the benchmark
  * reports how many host cores the oracle used).  No arithmetic. */
 int oracle_max_threads(void) { return omp_get_max_threads(); }
+
+/* Threads the following OpenMP regions of this library use (the benchmark's
+ * single-thread baseline sets 1, then restores the previous count).  No arithmetic. */
+void oracle_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }

@@ -57,3 +57,29 @@ def test_traffic_record_only_for_the_captured_source(tmp_path, monkeypatch):
     assert bench.traffic_record("gmm1", "prefill", str(src)) is None  # no capture of that workload
     src.write_text("// kernel v2\n")  # the kernel changed since the counters were taken
     assert bench.traffic_record("gmm1", "decode", str(src)) is None
+
+
+def test_roofline_picks_the_bound_and_flags_fractions_above_the_peak():
+    import synth
+    w = synth.CONFIGS["prefill"]
+    ei, _ = synth.routing(w.seed, w.M, w.E, w.topK, w.routing)
+    alg, active = bench.algorithmic(w, ei)
+    peaks = {"hbm_gbs": 6785.9, "bf16_tflops": 1833.7, "source": "measured"}
+    t = alg["gmm1"]["ops"] / (0.8 * peaks["bf16_tflops"] * 1e12)  # 80% of the tensor peak
+    r = bench.roofline_of(w, {"gmm1": t * 1e3, "gmm2": t * 0.5e3}, alg, peaks)
+    assert r["bound"] == "tensor" and abs(r["frac"] - 0.8) < 1e-3 and "above_peak" not in r
+    r = bench.roofline_of(w, {"gmm1": t * 0.7e3, "gmm2": t * 0.5e3}, alg, peaks)
+    assert r["frac"] > 1 and r["above_peak"] is True
+    d = synth.CONFIGS["decode"]
+    ei, _ = synth.routing(d.seed, d.M, d.E, d.topK, d.routing)
+    alg, active = bench.algorithmic(d, ei)
+    r = bench.roofline_of(d, {"gmm1": 1.1, "gmm2": 0.6}, alg, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+
+
+def test_single_thread_oracle_baseline():
+    import synth
+    res = bench.single_thread_oracle({"tiny": synth.make_inputs("tiny")})
+    assert res["tiny"]["cores"] == 1 and res["tiny"]["value"] > 0
+    import oracle
+    assert oracle.max_threads() > 1 or os.cpu_count() == 1  # the previous count is restored
