@@ -18,29 +18,36 @@
 //
 // CTA pairs.  One tcgen05.mma of M = 256 costs ~92 cycles for any N <= 128 and
 // 128 cycles at N = 256 (measured on GB300); at N = 256 changing the operand
-// addresses between MMAs is free and a tcgen05.commit costs ~60 cycles of tensor
-// time.  So two CTAs of a cluster issue MMAs of M = 256, N = 256 (cta_group::2),
-// one commit per 128-deep stage: each CTA contributes 128 weight channels
-// (operand A, in its own tensor memory) and half of the N token rows (operand B,
-// in its own shared memory), and receives the 128 x N block of its channels in its
-// tensor memory.  A work item is (expert, 256-channel block, 256-row tile); N is
-// 64, 128 or 256 by the rows the tile holds.
+// addresses between MMAs is free.  The issuing thread, however, is the limit:
+// a tcgen05.commit holds it ~700 cycles while the MMA queue covers only ~500
+// cycles of work, so with one commit per 8 MMAs a stage of 8 N = 256 MMAs took
+// ~1210 cycles instead of 1024, and with one per 16 MMAs the pipe ran at its full
+// 128 cycles per MMA (a one-thread issue loop measured on GB300).  So two CTAs of a
+// cluster issue MMAs of M = 256, N = 256 (cta_group::2), one commit per 256-deep
+// stage (16 MMAs): each CTA contributes 128 weight channels (operand A, in its own
+// tensor memory) and half of the N token rows (operand B, in its own shared
+// memory), and receives the 128 x N block of its channels in its tensor memory.
+// A work item is (expert, 256-channel block, 256-row tile); N is 64, 128 or 256
+// by the rows the tile holds.
 //   - Weights stay int8 in HBM (they are the dominant traffic at small batches).
-//     A TMA box of 128 channels x 128 k lands in shared memory (128-byte swizzle);
-//     converter warps read one channel row per thread, widen 4 int8 to 4 binary16
-//     with a byte permute into the 1024+v encoding and one subtract, and store the
-//     row into the stage's tensor-memory A buffer (tcgen05.st, 32x32b).
+//     They arrive in k-blocks: a TMA box (or one 16 KiB tile) of 128 channels x
+//     128 k in shared memory (128-byte swizzle), two per stage; converter warps read
+//     one channel row per thread, widen 4 int8 to 4 binary16 with a byte permute
+//     into the 1024+v encoding and one subtract, and store the row into the stage's
+//     tensor-memory A buffer (tcgen05.st, 32x32b).
 //   - Activations are binary16-coded int8 in expert-major rows (written so by the
-//     quant-scatter and SwiGLU kernels), loaded by TMA as two [128][64] tiles per
+//     quant-scatter and SwiGLU kernels), loaded by TMA as four [128][64] tiles per
 //     stage in the canonical K-major 128-byte-swizzled layout the MMA reads
 //     through a shared-memory descriptor.
-//   - Tensor memory: the accumulator (256 columns) and four A buffers (64 columns
-//     each).  The token ring and the A buffers have the same four slots, so one
-//     commit per stage frees both.
+//   - Tensor memory: the accumulator (256 columns) and two A buffers (128 columns
+//     each).  The token ring and the A buffers have the same two slots, so one
+//     commit per stage frees both; converters and the token producer refill a slot
+//     while the MMAs of the other one (2048 cycles at N = 256) run.
 //   - The MMA issuer cannot run far ahead of the tensor pipe (a stage completes
 //     ~500 cycles after its last MMA is issued), so its per-stage work is kept to
-//     one barrier wait: the stage's readiness (both CTAs' token halves and A
-//     buffers) is gathered on one barrier in CTA 0.
+//     one barrier wait and one commit: the stage's readiness (both CTAs' token
+//     halves and A buffers) is gathered on one barrier in CTA 0, and the operand
+//     descriptors of the stage's MMAs are one base plus constants.
 //
 // Roles (one persistent pair per two SMs, work items strided over the pairs):
 //   warp 0      TMA producer of the weight ring (freed by the converters as soon
@@ -82,24 +89,28 @@ static_assert(128 * kRegsSingle + 128 * kRegsConv + 512 * kRegsDrain <= kThreads
               "register split exceeds the registers the CTA is launched with");
 constexpr int kBM = 128;            // weight channels per CTA
 constexpr int kPairCh = 256;        // weight channels per pair (MMA M)
-constexpr int kBK = 128;            // reduction depth per stage
+constexpr int kBK = 128;            // reduction depth of a k-block (one weight tile / TMA box pair)
+constexpr int kKBlocks = 2;         // k-blocks per pipeline stage: one commit per 16 MMAs
 constexpr int kTileRows = 256;      // token rows per work item (MMA N <= 256)
 constexpr int kHalfRows = kTileRows / 2;  // token rows per CTA (TMA box height)
-constexpr int kTmemCols = 512;      // accumulator [0, 256), A buffers 256 + 64*slot
+constexpr int kTmemCols = 512;      // accumulator [0, 256), A buffers 256 + 128*slot
 constexpr int kACol0 = 256;
+constexpr int kACols = kKBlocks * kBK / 2;  // binary16 pairs per 32-bit column: 128 columns per stage
 constexpr int kMaxExperts = 1024;
-constexpr int kStages = 4;          // token ring = A buffers, freed by one commit per stage
-constexpr int kWStages = 4;         // weight ring, freed after conversion
+constexpr int kStages = 2;          // token ring = A buffers (256-deep stages), freed by one commit per stage
+constexpr int kWStages = 4;         // weight ring of k-blocks, freed after conversion
 constexpr int kWBytes = kBM * kBK;  // [128][128] int8, 128-B swizzled rows
-constexpr int kXHalfBytes = kHalfRows * 128;  // [128 rows][64] binary16, 128-B swizzled rows
-constexpr int kXBytes = 2 * kXHalfBytes;
+constexpr int kXHalfBytes = kHalfRows * 128;  // one token box: [128 rows][64] binary16, 128-B swizzled rows
+constexpr int kXBlockBytes = 2 * kXHalfBytes;  // a k-block of tokens
+constexpr int kXBytes = kKBlocks * kXBlockBytes;  // a stage of tokens (4 boxes)
 static_assert(kXHalfBytes % 1024 == 0, "1024-B alignment of swizzled tiles");
 static_assert(kBM == kWTileRows && kBK == kWTileDepth && kWBytes == kWTileBytes, "a weight stage is one tile");
 constexpr int kSmemBytes = kWStages * kWBytes + kStages * kXBytes + 1024;
 constexpr int kWProducerWarp = 0, kMmaWarp = 1, kXProducerWarp = 2, kRelayWarp = 3, kConvWarp0 = 4,
               kNumConvWarps = 4, kDrainWarp0 = 8, kNumDrainWarps = 16;
 static_assert(kThreads == 32 * (kDrainWarp0 + kNumDrainWarps), "warp roles");
-static_assert(kSmemBytes + 10 * 1024 <= 227 * 1024, "shared memory");
+static_assert(kSmemBytes + 13 * 1024 <= 227 * 1024, "shared memory (dynamic + ~12.4 KB static)");
+static_assert(kACol0 + kStages * kACols == kTmemCols, "tensor memory: accumulator + A buffers");
 // kind::f16 instruction descriptor: D f32, A/B f16, both K-major, M = 256; N is set per item
 constexpr uint32_t kIdescBase = (1u << 4) | ((uint32_t)(256 >> 4) << 24);
 
@@ -123,14 +134,15 @@ struct Args {
 // Role timing, compiled in only with -DMOE_GEMM_PROFILE: each role sums clock64()
 // intervals (time in a wait, time doing its work) into registers and adds them to
 // a 32-slot device buffer at the end.  Slot bases: weight producer 0, token producer
-// 2, relay 4, MMA issuer 8, converters 16, drains 24, issuer's total 31.
+// 2, relay 4, MMA issuer 8 (8-15: accumulator wait, stage wait, issue, commit, stage
+// body, set-up, item decode, final wait), converters 16, drains 24, issuer's total 31.
 #ifdef MOE_GEMM_PROFILE
-#define PROF_REGS unsigned long long _pf[6] = {0, 0, 0, 0, 0, 0}
+#define PROF_REGS unsigned long long _pf[8] = {0, 0, 0, 0, 0, 0, 0, 0}
 #define PROF_WAIT(i, expr) ([&]() { const long long _t0 = clock64(); const bool _r = (expr); \
                                     _pf[i] += clock64() - _t0; return _r; }())
 #define PROF_T0(v) const long long v = clock64()
 #define PROF_ADD(i, t0) (_pf[i] += clock64() - (t0))
-#define PROF_FLUSH(base) for (int _i = 0; _i < 6; ++_i) if (_pf[_i]) atomicAdd(args.prof + (base) + _i, _pf[_i])
+#define PROF_FLUSH(base) for (int _i = 0; _i < 8; ++_i) if (_pf[_i]) atomicAdd(args.prof + (base) + _i, _pf[_i])
 #define PROF_TOTAL(t0) atomicAdd(args.prof + 31, (unsigned long long)(clock64() - (t0)))
 #else
 #define PROF_REGS
@@ -422,7 +434,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int E = args.E, n_cb = (args.N + kPairCh - 1) / kPairCh;
-  const int nk = (args.Kd + kBK - 1) / kBK;  // a 64-deep tail reads TMA zero fill
+  const int nk = (args.Kd + kBK - 1) / kBK;  // k-blocks; a 64-deep tail reads TMA zero fill
+  const int nst = (nk + kKBlocks - 1) / kKBlocks;  // pipeline stages per work item
   PROF_T0(t_start);
   PROF_REGS;
   volatile int* abort_flag = &s_abort;
@@ -523,7 +536,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
   const uint32_t w_ring = smem_base;                  // SW x [128][128] int8
-  const uint32_t x_ring = smem_base + SW * kWBytes;   // S x 2 x [128][64] binary16
+  const uint32_t x_ring = smem_base + SW * kWBytes;   // S x 4 x [128][64] binary16
 
   if (warp < kConvWarp0) {
     regs_dec<kRegsSingle>();
@@ -562,12 +575,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     } else if (warp == kXProducerWarp) {
       // ======================= token producer =======================
-      // This CTA's half of the item's N rows (hr = N/2), as two [hr][64] boxes per
-      // stage.  Tiled: lane 0 loads two 128-row boxes of the expert-major operand.
-      // Gathered: the half's 4-row groups (G = hr/4 of them) are gathered by token
-      // index, lane l issuing group l % G of both boxes (G = 32) or of box l / G
-      // (G = 8, 16); rows past the item's last real row repeat that row's token
-      // (their outputs are never stored).
+      // This CTA's half of the item's N rows (hr = N/2), as [hr][64] boxes: two per
+      // k-block, up to four per stage.  Tiled: lane 0 loads 128-row boxes of the
+      // expert-major operand.  Gathered: the half's 4-row groups (G = hr/4 of them)
+      // are gathered by token index, lane l issuing group l % G of the boxes
+      // (l / G) mod (32 / G) + 32 / G * i; rows past the item's last real row repeat
+      // that row's token (their outputs are never stored).
       int n = 0;
       if (!GATHER) {
         if (lane == 0) {
@@ -575,14 +588,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int j = pair; j < total; j += npairs) {
             const Item it = decode_item(j, wl, e_hint);
             const int y = it.row0 + (int)rank * (it.n_mma >> 1);
-            for (int kb = 0; kb < nk; ++kb, ++n) {
+            for (int st = 0; st < nst; ++st, ++n) {
               const int slot = n % S;
+              const int nbox = 2 * min(kKBlocks, nk - st * kKBlocks);
               if (!PROF_WAIT(0, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status)))
                 goto x_done;
               uint8_t* xs_g = smem_gen + SW * kWBytes + slot * kXBytes;
-              mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)kXBytes);
-              tma_load_2d(xs_g, &tm_x, kb * kBK, y, &xfull_bar[slot]);
-              tma_load_2d(xs_g + kXHalfBytes, &tm_x, kb * kBK + 64, y, &xfull_bar[slot]);
+              mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)(nbox * kXHalfBytes));
+              for (int b = 0; b < nbox; ++b)
+                tma_load_2d(xs_g + b * kXHalfBytes, &tm_x, st * kKBlocks * kBK + 64 * b, y, &xfull_bar[slot]);
             }
           }
         }
@@ -598,19 +612,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tok.y = __ldg(args.gather_route + min(r0 + 1, last)) / args.topK;
           tok.z = __ldg(args.gather_route + min(r0 + 2, last)) / args.topK;
           tok.w = __ldg(args.gather_route + min(r0 + 3, last)) / args.topK;
-          for (int kb = 0; kb < nk; ++kb, ++n) {
+          for (int st = 0; st < nst; ++st, ++n) {
             const int slot = n % S;
+            const int nbox = 2 * min(kKBlocks, nk - st * kKBlocks);
             bool ok = true;
             if (lane == 0)
               ok = PROF_WAIT(0, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status));
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) goto x_done;
             uint8_t* xs_g = smem_gen + SW * kWBytes + slot * kXBytes;
-            if (lane == 0) mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)hr * 256u);
+            if (lane == 0) mbar_arrive_expect_tx(&xfull_bar[slot], (uint32_t)(hr * 128 * nbox));
             __syncwarp();  // the stage's expected bytes are posted before any gather lands
-            for (int i = lane; i < 2 * G; i += 32) {
+            for (int i = lane; i < nbox * G; i += 32) {
               const int box = i / G;
-              tma_gather4(xs_g + box * kXHalfBytes + (i - box * G) * 512, &tm_x, kb * kBK + 64 * box, tok,
-                          &xfull_bar[slot]);
+              tma_gather4(xs_g + box * kXHalfBytes + (i - box * G) * 512, &tm_x, st * kKBlocks * kBK + 64 * box,
+                          tok, &xfull_bar[slot]);
             }
           }
         }
@@ -627,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int n = 0;
         bool ok = true;
         for (int j = pair; j < total && ok; j += npairs) {
-          for (int kb = 0; kb < nk; ++kb, ++n) {
+          for (int st = 0; st < nst; ++st, ++n) {
             const int slot = n % S;
             ok = PROF_WAIT(0, wait_or_abort(&xfull_bar[slot], (n / S) & 1, abort_flag, args.status));
             if (!ok) break;
@@ -643,14 +658,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool ok = true;
         int e_hint = 0;
         for (int j = pair; j < total && ok; j += npairs) {
+          PROF_T0(t_item);
           const Item it = decode_item(j, wl, e_hint);
           const uint32_t idesc = kIdescBase | ((uint32_t)(it.n_mma >> 3) << 17);
           const int cs = s_chunk[it.e];
-          int kc = 0;  // stage index within the current exact chunk
-          for (int kb = 0; kb < nk && ok; ++kb, ++n) {
+          PROF_ADD(6, t_item);
+          int kc = 0;  // k-blocks done within the current exact chunk (cs is a whole number of stages)
+          for (int st = 0; st < nst && ok; ++st, ++n) {
             PROF_T0(t_body);
             const int slot = n % S;
             const uint32_t ph = (n / S) & 1;
+            const int nkb = min(kKBlocks, nk - st * kKBlocks);  // 1 only in an odd last stage
             if (kc == 0) {
               // a new exact chunk: both CTAs' drains must have read the accumulator
               ok = PROF_WAIT(0, wait_or_abort(&accempty_bar, (c & 1) ^ 1, abort_flag, args.status));
@@ -660,19 +678,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
             PROF_T0(t_issue);
             tc_fence_after();
-            const uint32_t xs = x_ring + slot * kXBytes;
-            const uint32_t a_tmem = tmem + kACol0 + slot * 64;
+            // 16-deep step s of the stage: A columns 8s of the stage's buffer; token box
+            // s/4 at byte 32*(s%4) of its 128-byte rows, i.e. the descriptor's start
+            // address field advanced by that offset / 16 (no carry: shared addresses
+            // stay below 256 KB)
+            const uint64_t bdesc0 = sw128_desc(x_ring + slot * kXBytes);
+            const uint32_t a0 = tmem + kACol0 + slot * kACols;
+            mma_pair(tmem, a0, bdesc0, idesc, kc != 0 ? 1u : 0u);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-              // 16-k step s: A columns 8s.., token tile s/4
-              const uint64_t bdesc = sw128_desc(xs + (s >> 2) * kXHalfBytes + (s & 3) * 32);
-              mma_pair(tmem, a_tmem + s * 8, bdesc, idesc, (kc != 0 || s != 0) ? 1u : 0u);
+            for (int s = 1; s < 8; ++s)
+              mma_pair(tmem, a0 + s * 8, bdesc0 + (uint64_t)(((s >> 2) * kXHalfBytes + (s & 3) * 32) >> 4), idesc, 1u);
+            if (nkb == kKBlocks) {
+#pragma unroll
+              for (int s = 8; s < 16; ++s)
+                mma_pair(tmem, a0 + s * 8, bdesc0 + (uint64_t)(((s >> 2) * kXHalfBytes + (s & 3) * 32) >> 4), idesc,
+                         1u);
             }
             PROF_ADD(2, t_issue);
             PROF_T0(t_commit);
             mma_commit_pair(&sdone_bar[slot]);  // token slot and A buffer free once these MMAs complete
             PROF_ADD(3, t_commit);
-            if (++kc == cs || kb == nk - 1) {
+            kc += nkb;
+            if (kc == cs || st == nst - 1) {
               mma_commit_pair(&accfull_bar);    // chunk accumulated: hand it to the drains
               ++c;
               kc = 0;
@@ -681,8 +708,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         // every MMA issued by this thread has completed once final_bar fires
+        PROF_T0(t_fin);
         mma_commit_local(&final_bar);
         mbar_wait_bounded(&final_bar, 0);
+        PROF_ADD(7, t_fin);
         PROF_FLUSH(8);
         PROF_TOTAL(t_start);
       }
@@ -690,49 +719,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kDrainWarp0) {
     // ======================= converters =======================
-    // A full 128-byte weight row per thread, widened and stored into the stage's
-    // tensor-memory A buffer in two 64-k halves, then handed to the MMA issuer.
+    // A full 128-byte weight row of each k-block per thread, widened and stored into
+    // the stage's tensor-memory A buffer in 64-k halves; once the stage's k-blocks
+    // are stored it is handed to the MMA issuer.
     regs_dec<kRegsConv>();
     const int quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;         // weight channel row of this thread
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t ready_remote0 = cluster_addr(&ready_bar[0], 0);
-    int n = 0;
+    int n = 0, m = 0;  // stages, k-blocks (weight ring positions)
     bool ok = true;
     for (int j = pair; j < total && ok; j += npairs) {
-      for (int kb = 0; kb < nk; ++kb, ++n) {
-        const int slot = n % S, wslot = n % SW;
-        ok = PROF_WAIT(0, wait_or_abort(&wfull_bar[wslot], (n / SW) & 1, abort_flag, args.status)) &&
-             PROF_WAIT(1, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status));
+      for (int st = 0; st < nst; ++st, ++n) {
+        const int slot = n % S;
+        const int nkb = min(kKBlocks, nk - st * kKBlocks);
+        ok = PROF_WAIT(1, wait_or_abort(&sdone_bar[slot], ((n / S) & 1) ^ 1, abort_flag, args.status));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        PROF_T0(t_conv);
         tc_fence_after();
-        const uint32_t wrow = w_ring + wslot * kWBytes + r * kBK;
-        const uint32_t ta = tmem + lane_off + kACol0 + slot * 64;
+        const uint32_t ta0 = tmem + lane_off + kACol0 + slot * kACols;
+        for (int kbi = 0; kbi < nkb; ++kbi, ++m) {
+          const int wslot = m % SW;
+          ok = PROF_WAIT(0, wait_or_abort(&wfull_bar[wslot], (m / SW) & 1, abort_flag, args.status));
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          PROF_T0(t_conv);
+          const uint32_t wrow = w_ring + wslot * kWBytes + r * kBK;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v[32];
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 w4 = lds128(wrow + (((4 * h + q) ^ (r & 7)) << 4));
-            i8x4_to_f16x4(w4.x, v[8 * q + 0], v[8 * q + 1]);
-            i8x4_to_f16x4(w4.y, v[8 * q + 2], v[8 * q + 3]);
-            i8x4_to_f16x4(w4.z, v[8 * q + 4], v[8 * q + 5]);
-            i8x4_to_f16x4(w4.w, v[8 * q + 6], v[8 * q + 7]);
+            for (int q = 0; q < 4; ++q) {
+              const uint4 w4 = lds128(wrow + (((4 * h + q) ^ (r & 7)) << 4));
+              i8x4_to_f16x4(w4.x, v[8 * q + 0], v[8 * q + 1]);
+              i8x4_to_f16x4(w4.y, v[8 * q + 2], v[8 * q + 3]);
+              i8x4_to_f16x4(w4.z, v[8 * q + 4], v[8 * q + 5]);
+              i8x4_to_f16x4(w4.w, v[8 * q + 6], v[8 * q + 7]);
+            }
+            if (h == 1) {
+              // the weight k-block is in registers: hand it back to the producer
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&wempty_bar[wslot]);
+            }
+            tmem_st32(ta0 + kbi * (kBK / 2) + 32 * h, v);
           }
-          if (h == 1) {
-            // the weight stage is in registers: hand it back to the producer
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&wempty_bar[wslot]);
-          }
-          tmem_st32(ta + 32 * h, v);
+          PROF_ADD(2, t_conv);
         }
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(ready_remote0 + slot * (uint32_t)sizeof(uint64_t));
-        PROF_ADD(2, t_conv);
       }
     }
     if (lane == 0) PROF_FLUSH(16);
