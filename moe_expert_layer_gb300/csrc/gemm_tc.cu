@@ -794,13 +794,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // One exact chunk for the whole reduction (activation bounds permitting): its
       // fp32 sums are the exact integers (|sum| <= 2^24), so the raw values are kept,
       // the accumulator is handed back to the MMAs right after the loads, and the
-      // epilogue scales them as they are (float(acc) is the same value).  Otherwise
-      // each chunk is converted to int32 and added before the hand-back.
-      const bool single = nch == 1;
-      int acc[64];  // int32 sums, or (single) the chunk's fp32 bits
+      // epilogue scales them as they are (float(acc) is the same value).  Two exact
+      // chunks: the first is kept raw the same way, and the second is added to it in
+      // fp32 as it is read -- one IEEE addition of two exact integers, i.e. the
+      // correctly rounded float of their exact sum, which is what the epilogue
+      // scales.  Either way the accumulator goes back to the MMAs after its loads
+      // and additions alone.  Otherwise each chunk is converted to int32 and added
+      // before the hand-back.
+      const bool raw = nch <= 2;
+      int acc[64];  // int32 sums, or (raw) the fp32 bits of the float total
 #pragma unroll
       for (int t = 0; t < 64; ++t) acc[t] = 0;
-      if (single) {
+      if (raw) {
         ok = PROF_WAIT(0, wait_or_abort(&accfull_bar, c & 1, abort_flag, args.status));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
@@ -816,6 +821,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(accempty_remote);
+        if (nch == 2) {
+          ok = PROF_WAIT(0, wait_or_abort(&accfull_bar, c & 1, abort_flag, args.status));
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          ++c;
+          PROF_T0(t_drain);
+          tc_fence_after();
+          if (active) {
+#pragma unroll
+            for (int t0 = 0; t0 < 64; t0 += 16) {
+              uint32_t v[16];
+              tmem_ld16(lane_base + t0, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                acc[t0 + i] = __float_as_int(__fadd_rn(__int_as_float(acc[t0 + i]), __uint_as_float(v[i])));
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(accempty_remote);
+          PROF_ADD(1, t_drain);
+        }
       } else {
         for (int ch = 0; ch < nch; ++ch, ++c) {
           ok = PROF_WAIT(0, wait_or_abort(&accfull_bar, c & 1, abort_flag, args.status));
@@ -851,7 +879,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float sc = __ldg(args.scale + (size_t)it.e * args.N + ch);
         const int t_lo = cg * 64;
         __half* dst = args.C + (size_t)(it.row0 + t_lo) * args.N + ch;
-        if (single) {
+        if (raw) {
 #pragma unroll
           for (int t = 0; t < 64; ++t)
             if (t_lo + t < it.rows) dst[(size_t)t * args.N] = f2h_sat(__fmul_rn(__int_as_float(acc[t]), sc));
