@@ -300,8 +300,10 @@ def roofline_of(w, stage_ms, alg, peaks):
     f16), whose dense rate equals the bf16 rate the peak was measured with."""
     dom = max(["gmm1", "gmm2"], key=lambda n: stage_ms[n])
     src = engine_source(w)
-    kernel = "grouped_gemm_kernel" if src.endswith("gemm_hmma.cu") else \
-        "grouped_gemm_hmma (experts <= 32 rows) + grouped_gemm_pair_kernel (the rest)"
+    mean_rows = w.R / w.E
+    kernel = ("grouped_gemm_kernel" if mean_rows <= 24.0 else
+              "grouped_gemm_pair_kernel" if mean_rows >= 256.0 else
+              "grouped_gemm_kernel (experts <= 32 rows) + grouped_gemm_pair_kernel (the rest)")
     t_dom = stage_ms[dom] * 1e-3
     t_hbm = alg[dom]["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_tc = alg[dom]["ops"] / (peaks["bf16_tflops"] * 1e12)
@@ -330,9 +332,9 @@ def roofline_of(w, stage_ms, alg, peaks):
 def launches_per_step(w):
     """Our kernels per layer call: the sort (fused into the quant kernel up to 4096
     routes, one kernel up to 8192, three above), the quant, each GEMM (one engine up
-    to 24 rows per expert on average, both above), SwiGLU, combine."""
+    to 24 rows per expert on average and from 256 on, both between), SwiGLU, combine."""
     sort_launches = 0 if w.R <= 4096 else (1 if w.R <= 8192 else 3)
-    gemm_launches = 1 if w.R / w.E <= 24.0 else 2
+    gemm_launches = 1 if (w.R / w.E <= 24.0 or w.R / w.E >= 256.0) else 2
     return sort_launches + 1 + 2 * gemm_launches + 2
 
 

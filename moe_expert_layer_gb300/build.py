@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libmoe_layer.so")
-SOURCES = ["route_sort.cu", "elementwise.cu", "gemm_hmma.cu", "gemm_tc.cu", "moe_layer.cu",
+SOURCES = ["route_sort.cu", "elementwise.cu", "gemm_hmma.cu", "gemm_tc.cu", "gemm_dispatch.cu", "moe_layer.cu",
            "route_sort_noalloc.cu", "selftest.cu", "weight_tiles.cu"]
 HEADERS = ["abi_checks.h", "common.cuh", "kernels.h", "tensor_map.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")

@@ -964,37 +964,4 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
   return p.gather_route ? launch_pair<true>(p, stream) : launch_pair<false>(p, stream);
 }
 
-// Engine choice.  A tcgen05.mma costs ~90 cycles for any N up to 128 (measured on
-// GB300) and consumes 2 KB of int8 weights per SM in that time: with few rows per
-// expert that caps weight streaming at about the HBM rate before any overhead.
-// Warp-level HMMA (m16n8k16) consumes weights several times faster at N=8.  So
-// batches with at most 24 rows per expert on average run entirely on the warp-MMA
-// engine (GMM1 at K=7168, I=2048, E=256, 16 rows per expert: 1.64 ms with 16-row
-// tiles against 2.92 ms on single-CTA tcgen05).  Larger batches split by expert
-// on the device: experts with at most kSplitRows rows go to the warp-MMA engine
-// (32-row tiles: one work item per expert and channel block), the others to the
-// tcgen05 pairs; both kernels derive their share from cumsum, so the host never
-// reads device counts (a kernel with no share exits at once).  Skewed routing
-// (K=7168, I=2048, E=256, Zipf): GMM1 1.90 ms at 32 rows, 1.97 at 16.
-constexpr int kSplitRows = 32;
-
-// The warp-MMA engine alone (up to 24 rows per expert on average) keeps 512-deep
-// chunks and reads no activation bounds.
-bool grouped_gemm_reads_bounds(int R, int E) { return (double)R / (double)E > 24.0; }
-
-cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream) {
-  GroupedGemmProblem q = p;
-  const double mean_rows = (double)p.R / (double)p.E;
-  if (!grouped_gemm_reads_bounds(p.R, p.E)) {
-    // 16-row tiles up to 8 rows per expert on average (decode); 32-row tiles above,
-    // so that an expert of up to 32 rows streams its weights through one work item
-    q.split_rows = 0x7fffffff;
-    return launch_grouped_gemm_hmma(q, mean_rows <= 8.0 ? 16 : 32, stream);
-  }
-  q.split_rows = kSplitRows;
-  cudaError_t err = launch_grouped_gemm_hmma(q, 32, stream);
-  if (err != cudaSuccess) return err;
-  return launch_grouped_gemm_tc(q, stream);
-}
-
 }  // namespace moe

@@ -325,6 +325,39 @@ def test_gmm2_bit_exact(w, bounded, layout):
     assert_bits_equal(host(c2)[:Rv], c2_ref, "c2")
 
 
+@pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
+def test_gmm_pairs_only_with_small_experts(bounded):
+    """Above 256 rows per expert on average the tcgen05 pairs take every expert, the
+    small ones (here 20, 10 and 0 rows beside 1200 and 70) on their short tiles."""
+    w = synth.Workload("pairs_only", 1300, 512, 192, 5, 1, "uniform", 81)
+    inp = synth.make_inputs(w)
+    ei = np.zeros((w.M, 1), np.int32)
+    ei[1200:1270] = 1
+    ei[1270:1290] = 2
+    ei[1290:] = 3
+    inp["expert_idx"] = ei[np.random.default_rng(81).permutation(w.M)]  # the tokens of each expert spread out
+    rs = oracle.route_sort(inp["expert_idx"], w.E)
+    assert list(rs["tokens_per_expert"]) == [1200, 70, 20, 10, 0] and w.R / w.E >= 256
+    xq, _ = oracle.quant_tokens(inp["x"])
+    _, c1_ref = oracle.gmm1(xq, rs["sorted_src_route"], inp["expert_idx"], inp["w1"], inp["s1"], w.R)
+    d = _dims(w, 1)
+    ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
+    a1 = _a1(xq, rs, 1, w.R)
+    c1 = torch.full((w.R, 2 * w.I), float("nan"), dtype=torch.float16, device="cuda")
+    b1 = dev(_bounds_ref(a1, rs["cumsum"], w.E)) if bounded else None
+    moe.moe_gmm1(d, dev(a1), None, dev(rs["cumsum"]), b1, _weights(d, 1, inp["w1"], 1), dev(inp["s1"]), c1, ws)
+    assert moe.moe_workspace_status(ws) == 0
+    assert_bits_equal(host(c1), c1_ref, "c1")
+    q2 = synth.int8_sym127(w.seed, 77, (w.R, w.I))
+    _, c2_ref = oracle.gmm2(q2, rs["sorted_src_route"], inp["expert_idx"], inp["w2"], inp["s2"])
+    c2 = empty((w.R, w.K), torch.float16)
+    q2f = q2.astype(np.float16)
+    b2 = dev(_bounds_ref(q2f, rs["cumsum"], w.E)) if bounded else None
+    moe.moe_gmm2(d, dev(q2f), dev(rs["cumsum"]), b2, _weights(d, 2, inp["w2"], 1), dev(inp["s2"]), c2, ws)
+    assert moe.moe_workspace_status(ws) == 0
+    assert_bits_equal(host(c2), c2_ref, "c2")
+
+
 @pytest.mark.parametrize("E,N,D", [(3, 128, 128), (2, 384, 192), (2, 256, 64), (1, 128, 1408), (2, 128, 7168),
                                    (3, 256, 320)])
 def test_pack_weight_tiles_layout(E, N, D):
