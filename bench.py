@@ -94,6 +94,8 @@ def algorithmic(w, expert_idx):
     st["swiglu"] = {"bytes": R * 2 * I * 2 + R * I * 2 + 8 * R}
     st["gmm2"] = {"bytes": active * K * I + active * K * 4 + R * I * 2 + R * K * 2,
                   "ops": 2 * R * I * K}
+    # GMM1 with SwiGLU fused in (every expert on the tcgen05 pairs): both stages' bytes
+    st["gmm1_swiglu"] = {"bytes": st["gmm1"]["bytes"] + st["swiglu"]["bytes"], "ops": st["gmm1"]["ops"]}
     st["combine"] = {"bytes": R * K * 2 + 12 * R + M * K * 2}
     return st, active
 
@@ -293,12 +295,18 @@ def step_stats(step_ms):
     return {"mean": statistics.mean(step_ms), "median": statistics.median(step_ms), "min": min(step_ms)}
 
 
+def fused_swiglu(w):
+    """Whether the layer runs SwiGLU inside the GMM1 kernel for this workload: every
+    expert on the tcgen05 pairs (>= 256 routes per expert on average), I <= 1536."""
+    return w.R / w.E >= 256.0 and w.I <= 1536
+
+
 def roofline_of(w, stage_ms, alg, peaks):
     """The dominant GEMM stage against its bound: HBM when its bytes take longer at the
     measured copy rate than its MACs at the measured dense 16-bit tensor rate, tensor
     otherwise.  Both engines multiply the int8 codes as binary16 (kind::f16 / HMMA
     f16), whose dense rate equals the bf16 rate the peak was measured with."""
-    dom = max(["gmm1", "gmm2"], key=lambda n: stage_ms[n])
+    dom = max([n for n in stage_ms if "ops" in alg[n]], key=lambda n: stage_ms[n])
     src = engine_source(w)
     mean_rows = w.R / w.E
     kernel = ("grouped_gemm_kernel" if mean_rows <= 24.0 else
@@ -332,10 +340,11 @@ def roofline_of(w, stage_ms, alg, peaks):
 def launches_per_step(w):
     """Our kernels per layer call: the sort (fused into the quant kernel up to 4096
     routes, one kernel up to 8192, three above), the quant, each GEMM (one engine up
-    to 24 rows per expert on average and from 256 on, both between), SwiGLU, combine."""
+    to 24 rows per expert on average and from 256 on, both between), SwiGLU (inside
+    GMM1 when fused_swiglu), combine."""
     sort_launches = 0 if w.R <= 4096 else (1 if w.R <= 8192 else 3)
     gemm_launches = 1 if (w.R / w.E <= 24.0 or w.R / w.E >= 256.0) else 2
-    return sort_launches + 1 + 2 * gemm_launches + 2
+    return sort_launches + 1 + 2 * gemm_launches + (0 if fused_swiglu(w) else 1) + 1
 
 
 def measure_workload(g, w, args, headline, keep_host=False):
@@ -416,7 +425,9 @@ def measure_workload(g, w, args, headline, keep_host=False):
     # the layer computes them only where its GEMM engine reads them (above 24 rows per expert)
     b1, b2 = (bounds[0], bounds[1]) if w.R / w.E > 24.0 else (None, None)
     fused_front = w.R <= 4096  # the layer's FrontReorder is one kernel
-    names = (["front_reorder"] if fused_front else ["route_sort", "quant"]) + ["gmm1", "swiglu", "gmm2", "combine"]
+    fused_sw = fused_swiglu(w)  # the layer's GMM1 runs SwiGLU too
+    names = ((["front_reorder"] if fused_front else ["route_sort", "quant"]) +
+             (["gmm1_swiglu"] if fused_sw else ["gmm1", "swiglu"]) + ["gmm2", "combine"])
     nev = len(names) + 1
 
     def stages(evs):
@@ -432,9 +443,13 @@ def measure_workload(g, w, args, headline, keep_host=False):
             next(it).record(stream)
             moe.moe_quant_dispatch(d, dev["x"], dev["expert_idx"], expanded, a1, pts1, b1, stream)
         next(it).record(stream)
-        moe.moe_gmm1(d, a1, None, cs, b1, dev["w1"], dev["s1"], c1, gws, stream)
-        next(it).record(stream)
-        moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, dev["expert_idx"], None, q2, pts2, b2, stream)
+        if fused_sw:
+            moe.moe_gmm1_swiglu(d, a1, cs, b1, dev["w1"], dev["s1"], c1, pts1, sorted_, dev["expert_idx"], q2, pts2,
+                                b2, gws, stream)
+        else:
+            moe.moe_gmm1(d, a1, None, cs, b1, dev["w1"], dev["s1"], c1, gws, stream)
+            next(it).record(stream)
+            moe.moe_swiglu_quant(d, c1, pts1, sorted_, cs, dev["expert_idx"], None, q2, pts2, b2, stream)
         next(it).record(stream)
         moe.moe_gmm2(d, q2, cs, b2, dev["w2"], dev["s2"], c2, gws, stream)
         next(it).record(stream)
@@ -466,6 +481,7 @@ def measure_workload(g, w, args, headline, keep_host=False):
         stage_report[n] = rep
     layer_ops = alg["gmm1"]["ops"] + alg["gmm2"]["ops"]
     rep = {
+        "fused_gmm1_swiglu": fused_sw,
         "workload": workload_desc(w), "ms_per_step": round(ms, 4),
         "ms_per_step_median": round(st["median"], 4), "ms_per_step_min": round(st["min"], 4),
         "value": round(job_tokens_per_s(g.world, w.M, ms), 1), "unit": UNIT,

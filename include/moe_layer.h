@@ -305,7 +305,7 @@ int32_t moe_front_reorder(const moe_dims_t* d, const uint16_t* x, const int32_t*
                           int32_t* cumsum, uint16_t* a1_f16, float* pts1, int32_t* a1_bounds, void* workspace,
                           size_t workspace_bytes, void* stream);
 
-/* Workspace bytes of moe_gmm1 / moe_gmm2 (status word). */
+/* Workspace bytes of moe_gmm1 / moe_gmm1_swiglu / moe_gmm2 (status word and E counters). */
 size_t moe_gmm_workspace_size(const moe_dims_t* d);
 
 /*
@@ -360,6 +360,25 @@ int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* sor
 int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* pts1,
                          const int32_t* sorted_src_route, const int32_t* cumsum, const int32_t* expert_idx,
                          int8_t* q2_i8, uint16_t* q2_f16, float* pts2, int32_t* q2_bounds, void* stream);
+
+/*
+ * GMM1 followed by SwiGLU + dynamic requant (page sections "3. GMM1" and "4. SwiGLU"):
+ * c1 exactly as moe_gmm1 writes it (the dispatched operand: a1_f16 [R][K] expert-major),
+ * then q2_f16, pts2 and q2_bounds exactly as moe_swiglu_quant writes them from c1 (q2
+ * only in the binary16-coded form the GMM2 reads; expert_idx is read only for the
+ * bounds).  When every expert runs on the tcgen05 CTA pairs (from 256 routes per expert
+ * on average) and I <= 1536, the SwiGLU runs inside the GMM1 kernel: the pairs'
+ * drain warps requantise the rows of each expert as soon as all of the expert's GMM1
+ * tiles are stored, between the tensor-core work items, so the SwiGLU kernel's pass
+ * over c1 leaves the critical path (the overlap of GMM1 and SwiGLU the page builds
+ * with its per-expert flags).  Otherwise GMM1 and the SwiGLU kernel run one after the
+ * other.  The results are the same bits either way.
+ *   workspace: moe_gmm_workspace_size(d) bytes (status word and per-expert counters).
+ */
+int32_t moe_gmm1_swiglu(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int32_t* a1_bounds,
+                        const int8_t* w1, const float* s1, uint16_t* c1, const float* pts1,
+                        const int32_t* sorted_src_route, const int32_t* expert_idx, uint16_t* q2_f16, float* pts2,
+                        int32_t* q2_bounds, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * GMM2 (page section "5. GMM2"): for each valid expanded row d of expert e,

@@ -25,7 +25,8 @@ EXPORTS = [
     "moe_layer_host_workspace_size", "moe_layer_fwd_host", "moe_workspace_status",
     "moe_workspace_clear_status", "moe_route_sort_workspace_size", "moe_route_sort",
     "moe_quant_tokens", "moe_quant_dispatch", "moe_front_reorder", "moe_gmm_workspace_size", "moe_gmm1",
-    "moe_swiglu_quant", "moe_gmm2", "moe_combine_unpermute", "moe_route_sort_noalloc", "moe_selftest_wait_timeout",
+    "moe_swiglu_quant", "moe_gmm1_swiglu", "moe_gmm2", "moe_combine_unpermute", "moe_route_sort_noalloc",
+    "moe_selftest_wait_timeout",
     "moe_layer_graph_create", "moe_layer_graph_create_host", "moe_layer_graph_launch", "moe_layer_graph_destroy",
     "moe_weight_tiles_bytes", "moe_pack_weight_tiles",
 ]
@@ -84,6 +85,7 @@ def load_library(path=None):
         "moe_front_reorder": ([D] + [vp] * 10 + [sz, vp], i32),
         "moe_gmm1": ([D] + [vp] * 8 + [sz, vp], i32),
         "moe_swiglu_quant": ([D] + [vp] * 10, i32),
+        "moe_gmm1_swiglu": ([D] + [vp] * 13 + [sz, vp], i32),
         "moe_gmm2": ([D] + [vp] * 7 + [sz, vp], i32),
         "moe_combine_unpermute": ([D] + [vp] * 6, i32),
         "moe_route_sort_noalloc": ([D] + [vp] * 6, i32),
@@ -245,6 +247,14 @@ def moe_swiglu_quant(d, c1, pts1, sorted_src_route, cumsum, expert_idx, q2_i8, q
     _check("moe_swiglu_quant", load_library().moe_swiglu_quant(
         ctypes.byref(d), _p(c1), _p(pts1), _p(sorted_src_route), _p(cumsum), _p(expert_idx), _p(q2_i8),
         _p(q2_f16), _p(pts2), _p(q2_bounds), _stream(stream)))
+
+
+def moe_gmm1_swiglu(d, a1_f16, cumsum, a1_bounds, w1, s1, c1, pts1, sorted_src_route, expert_idx, q2_f16, pts2,
+                    q2_bounds, workspace, stream=None):
+    _check("moe_gmm1_swiglu", load_library().moe_gmm1_swiglu(
+        ctypes.byref(d), _p(a1_f16), _p(cumsum), _p(a1_bounds), _p(w1), _p(s1), _p(c1), _p(pts1),
+        _p(sorted_src_route), _p(expert_idx), _p(q2_f16), _p(pts2), _p(q2_bounds), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def moe_gmm2(d, q2_f16, cumsum, q2_bounds, w2, s2, c2, workspace, stream=None):

@@ -13,7 +13,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libmoe_layer.so")
 SOURCES = ["route_sort.cu", "elementwise.cu", "gemm_hmma.cu", "gemm_tc.cu", "gemm_dispatch.cu", "moe_layer.cu",
            "route_sort_noalloc.cu", "selftest.cu", "weight_tiles.cu"]
-HEADERS = ["abi_checks.h", "common.cuh", "kernels.h", "tensor_map.h"]
+HEADERS = ["abi_checks.h", "common.cuh", "kernels.h", "swiglu.cuh", "tensor_map.h"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

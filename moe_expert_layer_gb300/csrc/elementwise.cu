@@ -9,6 +9,7 @@
 // the rounding points the page defines.
 #include "common.cuh"
 #include "kernels.h"
+#include "swiglu.cuh"
 
 namespace moe {
 
@@ -38,20 +39,6 @@ __device__ __forceinline__ void add_segment_l1(int* s_l1, int idx, int l1) {
   const unsigned mask = __activemask();
   const int sum = __reduce_add_sync(mask, l1);
   if ((int)(threadIdx.x & 31) == __ffs(mask) - 1) atomicAdd(&s_l1[(idx * 8) / kBoundSegment], sum);
-}
-
-// Requant codes read off a float: for |v| < 127.5, r = fl(v + kCodeMagic) is
-// kCodeMagic + q with q = v rounded to the nearest integer, ties to even (the float
-// spacing in [2^23, 2^24) is 1 and kCodeMagic is even), and r's bits are 0x4B406480 + q:
-// the low half-word, 0x6480 + q, is the binary16 1152 + q (the mantissa of 1024) and
-// its low byte 0x80 + q is q's two's-complement byte with the top bit flipped.
-constexpr float kCodeMagic = 12608640.0f;  // 1.5 * 2^23 + 0x6480
-
-// Two such code floats -> the binary16 pair (q0, q1): their low half-words, minus 1152.
-__device__ __forceinline__ uint32_t code_bits_to_half2(uint32_t b0, uint32_t b1) {
-  uint32_t r;
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(__byte_perm(b0, b1, 0x5410)), "r"(0x64806480u));
-  return r;
 }
 
 __device__ __forceinline__ uint32_t codes_to_half2(int q0, int q1) {
@@ -301,47 +288,25 @@ __global__ void __launch_bounds__(kRowThreads) swiglu_quant_kernel(
       const Vec8h& u = uv[i];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float hg = __fmul_rn(__half2float(g.h[j]), p1);
-        // exp and the division on the MUFU fast paths (ex2 / rcp, a few ulp): SwiGLU
-        // is instruction-bound, and the requantised codes tolerate it (the pages'
-        // exp is a different library's in any case).  The up half's token scale p1
-        // is left out of y: it scales the whole row, so the codes y * 127 / max|y|
-        // keep their values (to an ulp or two, like the fast exp) and only pts2
-        // takes it back.
-        const float silu = __fdividef(hg, __fadd_rn(1.0f, __expf(-hg)));
-        y[i][j] = __fmul_rn(silu, __half2float(u.h[j]));
+        y[i][j] = swiglu_y(g.h[j], u.h[j], p1);  // swiglu.cuh: fast exp, token scale on the gate only
         amax = fmaxf(amax, fabsf(y[i][j]));
       }
     }
   }
   amax = block_max_nonneg(amax, red);
-  const bool nz = amax > 0.0f;
-  // inv = 0 for an all-zero row: every y * inv is then +-0 and its code 0
-  const float inv = nz ? __fdiv_rn(127.0f, amax) : 0.0f;
-  if (threadIdx.x == 0) pts2[d] = nz ? __fdiv_rn(__fmul_rn(amax, p1), 127.0f) : 0.0f;
+  const float inv = swiglu_inv(amax);
+  if (threadIdx.x == 0) pts2[d] = swiglu_pts2(amax, p1);
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int idx = threadIdx.x + i * (int)blockDim.x;
     if (idx < nvec) {
-      // r = fl(y * inv + kCodeMagic), one rounding of the exact product: its nearest
-      // integer q, ties to even.  |y| <= amax keeps |y * inv| below 127 * (1 + 2^-23)
-      // < 127.5, so q needs no clamp.  (SwiGLU is issue-bound: the codes, their
-      // binary16 form and the segment sums take few instructions.)
+      // the codes as binary16 and their sum of |q| (swiglu.cuh); r keeps the code
+      // floats, whose low bytes are the int8 codes with the top bit flipped
       float r[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) r[j] = __fmaf_rn(y[i][j], inv, kCodeMagic);
-      Vec8h hc;  // the codes as binary16
-#pragma unroll
-      for (int j = 0; j < 4; ++j) hc.u[j] = code_bits_to_half2(__float_as_uint(r[2 * j]), __float_as_uint(r[2 * j + 1]));
-      if (bounds) {
-        // sum of |q| over the 8 codes in binary16 (integers up to 8 * 127 are exact),
-        // read off the bits of s + 1024 = 0x6400 + s
-        __half2 a = __habs2(hc.h2[0]);
-#pragma unroll
-        for (int j = 1; j < 4; ++j) a = __hadd2(a, __habs2(hc.h2[j]));
-        const __half s = __hadd(__hadd(__low2half(a), __high2half(a)), __ushort_as_half(0x6400));
-        add_segment_l1(s_l1, idx, (int)__half_as_ushort(s) - 0x6400);
-      }
+      int l1 = 0;
+      Vec8h hc;
+      hc.v = swiglu_codes8(y[i], inv, bounds ? &l1 : nullptr, r);
+      if (bounds) add_segment_l1(s_l1, idx, l1);
       if (q2_i8) {
         // the low bytes 0x80 + q, top bits flipped back: q's two's-complement bytes
         uint2 packed;

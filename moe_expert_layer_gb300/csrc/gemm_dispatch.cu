@@ -48,4 +48,29 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream
   return launch_grouped_gemm_tc(q, stream);
 }
 
+cudaError_t launch_gemm1_swiglu(const GroupedGemmProblem& g1, int I, int topK, const float* pts1,
+                                const int32_t* sorted_src_route, const int32_t* expert_idx, uint16_t* q2,
+                                float* pts2, int32_t* q2_bounds, int32_t* sw_done, cudaStream_t stream, bool* fused) {
+  const double mean_rows = (double)g1.R / (double)g1.E;
+  const bool fuse = grouped_gemm_reads_bounds(g1.R, g1.E) && mean_rows >= kPairsOnlyRows && !g1.gather_route &&
+                    I <= kFusedSwigluMaxI && pair_grid_coresident();
+  if (fused) *fused = fuse;
+  if (fuse) {
+    GroupedGemmProblem q = g1;
+    q.split_rows = 0;
+    q.topK = topK;  // a row's token is its route / topK
+    q.sw_pts1 = pts1;
+    q.sw_sorted = sorted_src_route;
+    q.sw_q2 = q2;
+    q.sw_pts2 = pts2;
+    q.sw_bounds = q2_bounds;
+    q.sw_done = sw_done;
+    return launch_grouped_gemm_tc(q, stream);
+  }
+  cudaError_t e = launch_grouped_gemm(g1, stream);
+  if (e != cudaSuccess) return e;
+  return launch_swiglu_quant(g1.C, g1.R, I, g1.E, topK, pts1, sorted_src_route, g1.cumsum, nullptr, q2, pts2,
+                             expert_idx, q2_bounds, stream);
+}
+
 }  // namespace moe

@@ -69,6 +69,7 @@
 // is freed) before returning.
 #include "common.cuh"
 #include "kernels.h"
+#include "swiglu.cuh"
 #include "tensor_map.h"
 
 namespace moe {
@@ -126,10 +127,105 @@ struct Args {
   int topK;
   const uint8_t* w_tiles;  // null: weights through the tensor map; else the tile layout
   int w_kb;                // tiles per 128-channel block of the tile layout
+  // SwiGLU fused into GMM1 (sw_q2 null: a plain grouped GEMM); see the drain role
+  const float* sw_pts1;          // [M] token scales
+  const int32_t* sw_sorted;      // [R] route of each expanded row
+  __half* sw_q2;                 // [R][N/2] binary16 codes
+  float* sw_pts2;                // [R]
+  int32_t* sw_bounds;            // [E][kBoundSegments] or null
+  int32_t* sw_done;              // [E] stored-item counters, zero at launch
 #ifdef MOE_GEMM_PROFILE
   unsigned long long* prof;
 #endif
 };
+
+// ------------------------------------------------------------------ SwiGLU fused into GMM1
+// With args.sw_q2 set (GMM1, every expert on the pairs, I <= kSwigluMaxI) the drain
+// warps also run SwiGLU + requant, one expanded row per warp at a time, on the rows of
+// experts all of whose GMM1 items are stored.  Every drain warp counts each item it
+// has finished (its epilogue stores fenced first) on the item's expert; an expert is
+// complete at kSwigluCountPerItem * (its items).  Drain warp gw of the grid owns rows
+// gw, gw + W, ... (W = all drain warps), taken in order: between items, while the next
+// accumulator chunk is not ready, it requantises its next rows as far as their experts
+// are complete; after its last item it finishes its rows, waiting (bounded) for their
+// experts.  No wait ever depends on a CTA that is not already running: the pairs
+// launch only when all of them can be resident at once (the host checks the
+// occupancy).  The arithmetic is swiglu.cuh's, as in the SwiGLU kernel: the same bits.
+constexpr int kSwigluMaxVpl = 6;                     // 16-byte vectors per lane of a row's half
+constexpr int kSwigluMaxI = kSwigluMaxVpl * 32 * 8;  // 1536
+constexpr int kSwigluCountPerItem = 2 * 16;          // drain warps of a pair
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// SwiGLU + requant of expanded row d (expert e) by one warp: the row's gate and up
+// halves (C1, written by other CTAs: read through L2) in registers, max |y| across
+// the warp, then the codes, pts2 and the row's segment sums of |q|.  y is computed
+// twice from the loaded halves (for the max, then for the codes) rather than kept:
+// the same instructions on the same inputs give the same values, and the drain warps'
+// registers hold the row only once.
+__device__ __forceinline__ void swiglu_row_warp(const Args& a, int d, int e, int lane) {
+  const int I = a.N >> 1, nvec = I >> 3;
+  const int4* gate = reinterpret_cast<const int4*>(a.C + (size_t)d * a.N);
+  const int4* up = gate + nvec;
+  const float p1 = __ldg(a.sw_pts1 + __ldg(a.sw_sorted + d) / a.topK);
+  union V {
+    int4 v;
+    __half h[8];
+  };
+  V g[kSwigluMaxVpl], u[kSwigluMaxVpl];
+#pragma unroll
+  for (int i = 0; i < kSwigluMaxVpl; ++i) {
+    const int v = lane + 32 * i;
+    g[i].v = v < nvec ? __ldcg(gate + v) : make_int4(0, 0, 0, 0);
+    u[i].v = v < nvec ? __ldcg(up + v) : make_int4(0, 0, 0, 0);
+  }
+  float amax = 0.0f;  // zero vectors past the row give y = 0
+#pragma unroll
+  for (int i = 0; i < kSwigluMaxVpl; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(swiglu_y(g[i].h[j], u[i].h[j], p1)));
+  amax = warp_max(amax);
+  const float inv = swiglu_inv(amax);
+  if (lane == 0) a.sw_pts2[d] = swiglu_pts2(amax, p1);
+  int4* q2 = reinterpret_cast<int4*>(a.sw_q2 + (size_t)d * I);
+  int seg0 = 0, seg1 = 0;  // sums of |q| of the two 1024-deep segments I <= 1536 spans
+#pragma unroll
+  for (int i = 0; i < kSwigluMaxVpl; ++i) {
+    const int v = lane + 32 * i;
+    if (v < nvec) {
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) y[j] = swiglu_y(g[i].h[j], u[i].h[j], p1);
+      int l1 = 0;
+      q2[v] = swiglu_codes8(y, inv, &l1);
+      if (v * 8 < kBoundSegment) seg0 += l1; else seg1 += l1;
+    }
+  }
+  if (a.sw_bounds) {
+    const int s0 = __reduce_add_sync(0xffffffffu, seg0), s1 = __reduce_add_sync(0xffffffffu, seg1);
+    if (lane == 0) {
+      atomicMax(a.sw_bounds + (size_t)e * kBoundSegments, s0);
+      if (I > kBoundSegment) atomicMax(a.sw_bounds + (size_t)e * kBoundSegments + 1, s1);
+    }
+  }
+}
 
 // Role timing, compiled in only with -DMOE_GEMM_PROFILE: each role sums clock64()
 // intervals (time in a wait, time doing its work) into registers and adds them to
@@ -312,15 +408,26 @@ __device__ __forceinline__ int chunk_stages(const int32_t* bounds, int e, int nk
 // busiest pair had up to 11% more MMA time than the mean under skewed routing.  In
 // the first stretch pairs working at the same time still share weight blocks
 // through L2.
-__device__ __forceinline__ int full_tiles(int cnt, int split_rows) {
+//
+// With SwiGLU fused (inl), an expert's short last tile instead runs right after its
+// other tiles, in the first stretch (MMA N by the rows it holds): the rows' SwiGLU
+// needs all of the expert's tiles, and in three stretches every expert with a short
+// tile would complete only at the very end.
+__device__ __forceinline__ int full_tiles(int cnt, int split_rows, bool inl) {
   if (cnt <= split_rows) return 0;
+  if (inl) return (cnt + kTileRows - 1) / kTileRows;
   return cnt / kTileRows + (cnt % kTileRows > kTileRows / 2 ? 1 : 0);
 }
 // the kind of the expert's short last tile: 1 for N = 128, 2 for N = 64, 0 for none
-__device__ __forceinline__ int short_tile(int cnt, int split_rows) {
+__device__ __forceinline__ int short_tile(int cnt, int split_rows, bool inl) {
   const int r = cnt % kTileRows;
-  if (cnt <= split_rows || r == 0 || r > kTileRows / 2) return 0;
+  if (inl || cnt <= split_rows || r == 0 || r > kTileRows / 2) return 0;
   return r > kTileRows / 4 ? 1 : 2;
+}
+
+// Items of an expert with cnt rows on the pairs (all channel blocks).
+__device__ __forceinline__ int expert_items(int cnt, int split_rows, int n_cb, bool inl) {
+  return n_cb * (full_tiles(cnt, split_rows, inl) + (short_tile(cnt, split_rows, inl) ? 1 : 0));
 }
 
 struct WorkList {
@@ -328,6 +435,7 @@ struct WorkList {
   const int* end;       // cumsum
   const short* shorts;  // experts with a short last tile: the N = 128 ones, then the N = 64 ones
   int n_full, n128, n_cb, E;
+  bool inl;             // short tiles inline in the first stretch (fused SwiGLU)
 };
 
 // Work item j -> (expert, channel block, first row, rows, MMA N).  In the first
@@ -352,14 +460,14 @@ __device__ __forceinline__ Item decode_item(int j, const WorkList& wl, int& e_hi
     e_hint = lo;
     const int start = lo ? wl.end[lo - 1] : 0;
     const int cnt = wl.end[lo] - start;
-    const int n_rt = cnt / kTileRows + (cnt % kTileRows > kTileRows / 2 ? 1 : 0);
+    const int n_rt = full_tiles(cnt, -1, wl.inl);
     const int local = j - wl.pref[lo];
     const int cb = local / n_rt, rt = local - cb * n_rt;
     it.e = lo;
     it.cb = cb;
     it.row0 = start + rt * kTileRows;
     it.rows = min(kTileRows, cnt - rt * kTileRows);
-    it.n_mma = kTileRows;
+    it.n_mma = !wl.inl || it.rows > kTileRows / 2 ? kTileRows : (it.rows > kTileRows / 4 ? kTileRows / 2 : kTileRows / 4);
   } else {
     const int k = j - wl.n_full, idx = k / wl.n_cb;
     const int e = wl.shorts[idx];
@@ -436,6 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int E = args.E, n_cb = (args.N + kPairCh - 1) / kPairCh;
   const int nk = (args.Kd + kBK - 1) / kBK;  // k-blocks; a 64-deep tail reads TMA zero fill
   const int nst = (nk + kKBlocks - 1) / kKBlocks;  // pipeline stages per work item
+  const bool inl = args.sw_q2 != nullptr;           // short tiles inline (fused SwiGLU)
   PROF_T0(t_start);
   PROF_REGS;
   volatile int* abort_flag = &s_abort;
@@ -449,8 +558,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int hi = __ldg(args.cumsum + e), lo = e ? __ldg(args.cumsum + e - 1) : 0;
       s_end[e] = hi;
       s_chunk[e] = (short)chunk_stages(args.bounds, e, nk);
-      local += full_tiles(hi - lo, args.split_rows) * n_cb;
-      const int st = short_tile(hi - lo, args.split_rows);
+      local += full_tiles(hi - lo, args.split_rows, inl) * n_cb;
+      const int st = short_tile(hi - lo, args.split_rows, inl);
       local2 += st == 1 ? 1 : (st == 2 ? 1 << 16 : 0);
     }
     int incl = local, incl2 = local2;
@@ -509,8 +618,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int e = e0; e < e1; ++e) {
       s_pref[e] = run;
       const int lo = e ? s_end[e - 1] : 0;
-      run += full_tiles(s_end[e] - lo, args.split_rows) * n_cb;
-      const int st = short_tile(s_end[e] - lo, args.split_rows);
+      run += full_tiles(s_end[e] - lo, args.split_rows, inl) * n_cb;
+      const int st = short_tile(s_end[e] - lo, args.split_rows, inl);
       if (st == 1) s_short[run2 & 0xffff] = (short)e;
       if (st == 2) s_short[n128 + (run2 >> 16)] = (short)e;
       run2 += st == 1 ? 1 : (st == 2 ? 1 << 16 : 0);
@@ -530,6 +639,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   wl.n128 = s_nshort & 0xffff;
   wl.n_cb = n_cb;
   wl.E = E;
+  wl.inl = inl;
   const int total = wl.n_full + n_cb * ((s_nshort & 0xffff) + (s_nshort >> 16));
   const uint32_t tmem = s_tmem;
 
@@ -784,6 +894,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + cg * 64;
     const uint32_t accempty_remote = cluster_addr(&accempty_bar, 0);
     int c = 0;
+    // fused SwiGLU: this warp's rows gw, gw + stride, ... of the valid ones, and the
+    // expert of the next one (rows only move forward)
+    const int sw_stride = (int)gridDim.x * kNumDrainWarps;
+    int sw_row = (int)blockIdx.x * kNumDrainWarps + (warp - kDrainWarp0);
+    const int sw_valid = s_end[E - 1];
+    int sw_e = 0;
     bool ok = true;
     int e_hint = 0;
     for (int j = pair; j < total && ok; j += npairs) {
@@ -871,11 +987,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (!active) continue;
       PROF_T0(t_epi);
       // epilogue: channel r of rows row0 + 64*cg + t (a warp writes 64 contiguous bytes per row)
       const int ch = it.cb * kPairCh + (int)rank * kBM + r;
-      if (ch < args.N) {
+      if (active && ch < args.N) {
         const float sc = __ldg(args.scale + (size_t)it.e * args.N + ch);
         const int t_lo = cg * 64;
         __half* dst = args.C + (size_t)(it.row0 + t_lo) * args.N + ch;
@@ -890,6 +1005,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       PROF_ADD(2, t_epi);
+      if (args.sw_q2) {
+        // count this item on its expert once the warp's stores are visible GPU-wide, then
+        // requantise own rows of complete experts while the next chunk is not ready
+        __syncwarp();
+        __threadfence();
+        if (lane == 0) atomicAdd(args.sw_done + it.e, 1);
+        while (sw_row < sw_valid && !mbar_test(&accfull_bar, c & 1)) {
+          while (s_end[sw_e] <= sw_row) ++sw_e;
+          const int lo = sw_e ? s_end[sw_e - 1] : 0;
+          const int target = kSwigluCountPerItem * expert_items(s_end[sw_e] - lo, args.split_rows, n_cb, inl);
+          if (__shfl_sync(0xffffffffu, lane == 0 ? ld_acquire(args.sw_done + sw_e) : 0, 0) < target) break;
+          swiglu_row_warp(args, sw_row, sw_e, lane);
+          sw_row += sw_stride;
+        }
+      }
+    }
+    if (args.sw_q2 && ok) {
+      // the rest of this warp's rows, each once its expert is complete (bounded wait)
+      const uint64_t t0 = globaltimer_ns();
+      while (sw_row < sw_valid) {
+        while (s_end[sw_e] <= sw_row) ++sw_e;
+        const int lo = sw_e ? s_end[sw_e - 1] : 0;
+        const int target = kSwigluCountPerItem * expert_items(s_end[sw_e] - lo, args.split_rows, n_cb, inl);
+        if (__shfl_sync(0xffffffffu, lane == 0 ? ld_acquire(args.sw_done + sw_e) : 0, 0) < target) {
+          if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            record_status(args.status, MOE_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(256);
+          continue;
+        }
+        swiglu_row_warp(args, sw_row, sw_e, lane);
+        sw_row += sw_stride;
+      }
     }
     if (lane == 0) PROF_FLUSH(24);
   }
@@ -949,6 +1099,15 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.topK = p.topK;
   a.w_tiles = p.w_kb ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;
   a.w_kb = p.w_kb;
+  a.sw_pts1 = p.sw_pts1;
+  a.sw_sorted = p.sw_sorted;
+  a.sw_q2 = reinterpret_cast<__half*>(p.sw_q2);
+  a.sw_pts2 = p.sw_pts2;
+  a.sw_bounds = p.sw_bounds;
+  a.sw_done = p.sw_done;
+  if (a.sw_q2 && (GATHER || p.split_rows != 0 || p.N / 2 > kSwigluMaxI || p.topK < 1 || !a.sw_pts1 || !a.sw_sorted ||
+                  !a.sw_pts2 || !a.sw_done))
+    return cudaErrorInvalidValue;  // the fused SwiGLU needs every expert of a tiled GMM1 on the pairs
 #ifdef MOE_GEMM_PROFILE
   a.prof = g_gemm_prof;
   if (!a.prof) return cudaErrorInvalidValue;
@@ -959,6 +1118,33 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+static_assert(kSwigluMaxI == kFusedSwigluMaxI, "fused SwiGLU row size");
+
+bool pair_grid_coresident() {
+  static PerContextOnce queried;
+  static bool ok[kMaxDevices] = {};
+  const int dev = current_device();
+  if (queried.needed(dev)) {
+    // the kernel's attributes (dynamic shared memory) are set by its first launch; set
+    // them here too so the query sees the launch's configuration
+    if (cudaFuncSetAttribute(grouped_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return false;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<false>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      clusters = 0;
+    }
+    ok[dev] = 2 * clusters >= (sm_count() & ~1);
+    queried.done(dev);
+  }
+  return ok[dev];
+}
 
 cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream) {
   return p.gather_route ? launch_pair<true>(p, stream) : launch_pair<false>(p, stream);

@@ -55,11 +55,33 @@ struct GroupedGemmProblem {
   int split_rows;                   // experts with <= split_rows rows run on the warp-MMA engine,
                                     // the others on the tcgen05 pairs (set by launch_grouped_gemm)
   const int32_t* bounds;            // [E][kBoundSegments] activation bounds, or null
+  // GMM1 only, set by launch_gemm1_swiglu: SwiGLU + requant fused into the tcgen05 pairs
+  const float* sw_pts1;             // [M] token scales (null: a plain GEMM)
+  const int32_t* sw_sorted;         // [R] route of each expanded row
+  uint16_t* sw_q2;                  // [R][N/2] binary16-coded codes
+  float* sw_pts2;                   // [R]
+  int32_t* sw_bounds;               // [E][kBoundSegments] or null
+  int32_t* sw_done;                 // [E] int32, zero at launch
 };
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream);     // picks an engine
 bool grouped_gemm_reads_bounds(int R, int E);  // whether the engine it picks uses activation bounds
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream);  // gemm_hmma.cu
 cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream);  // gemm_tc.cu
+// Whether every CTA pair of the tcgen05 kernel's grid can be resident at once on the
+// current device (the fused SwiGLU's waits rely on it).
+bool pair_grid_coresident();
+// The largest I the tcgen05 pairs fuse SwiGLU for (a row's half: 6 vectors per lane).
+constexpr int kFusedSwigluMaxI = 1536;
+// GMM1 (g1: c1 written as usual) followed by SwiGLU + requant of its rows (q2 as
+// binary16 codes, pts2, q2_bounds if not null), as launch_grouped_gemm then
+// launch_swiglu_quant would compute them.  When every expert runs on the tcgen05 pairs,
+// I <= kFusedSwigluMaxI and the pairs can all be resident, the SwiGLU runs inside the
+// GMM1 kernel (sw_done: [E] int32 the caller has zeroed); otherwise the two kernels
+// run one after the other.  Returns in *fused which of the two happened.
+cudaError_t launch_gemm1_swiglu(const GroupedGemmProblem& g1, int I, int topK, const float* pts1,
+                                const int32_t* sorted_src_route, const int32_t* expert_idx, uint16_t* q2,
+                                float* pts2, int32_t* q2_bounds, int32_t* sw_done, cudaStream_t stream,
+                                bool* fused = nullptr);
 
 // weight_tiles.cu: the MOE_WEIGHTS_TILES layout (include/moe_layer.h) of a weight
 // [E][N][D]: 16 KiB tiles of 128 channels x 128 reduction bytes, 128-byte swizzled,

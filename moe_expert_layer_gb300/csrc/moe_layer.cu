@@ -36,7 +36,8 @@ int weight_kb(const moe_dims_t* d, int D) {
 
 // Layout of the layer workspace.
 struct Layout {
-  size_t status, bounds1, bounds2, sorted, expanded, tpe, cumsum, sort_ws, a1, pts1, c1, q2, pts2, c2, total;
+  size_t status, bounds1, bounds2, sw_done, zeroed, sorted, expanded, tpe, cumsum, sort_ws, a1, pts1, c1, q2, pts2, c2,
+      total;
   // host-variant staging
   size_t hx, hei, hprobs, hout, host_total;
 };
@@ -50,11 +51,14 @@ Layout layout_of(const moe_dims_t* d) {
     off = align_up(off + bytes);
     return at;
   };
-  // status word and both bounds arrays are contiguous: one memset clears them
+  // status word, both bounds arrays and the fused SwiGLU's per-expert counters are
+  // contiguous: one memset clears them
   L.status = 0;
   L.bounds1 = 16;
   L.bounds2 = L.bounds1 + E * moe::kBoundSegments * 4;
-  take(L.bounds2 + E * moe::kBoundSegments * 4);
+  L.sw_done = L.bounds2 + E * moe::kBoundSegments * 4;
+  L.zeroed = L.sw_done + E * 4;
+  take(L.zeroed);
   L.sorted = take(R * 4);
   L.expanded = take(R * 4);
   L.tpe = take(E * 4);
@@ -101,8 +105,7 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   int32_t* bounds1 = use_bounds ? at<int32_t>(ws, L.bounds1) : nullptr;
   int32_t* bounds2 = use_bounds ? at<int32_t>(ws, L.bounds2) : nullptr;
   cudaError_t e;
-  if ((e = cudaMemsetAsync(status, 0, L.bounds2 + (size_t)E * moe::kBoundSegments * 4, st)) != cudaSuccess)
-    return launch_status(e);
+  if ((e = cudaMemsetAsync(status, 0, L.zeroed, st)) != cudaSuccess) return launch_status(e);
   // FrontReorder: sort the routes, quantise each token once and scatter its codes to
   // its expert-major rows (a TMA gather of token rows inside GMM1 measured 1.2-3.2x
   // slower GMM1 on GB300: one gather4 moves 512 B, a tiled box up to 16 KB)
@@ -112,6 +115,7 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
 
   moe::GroupedGemmProblem g1{};
   g1.act = a1;
+  g1.topK = topK;
   g1.act_rows = R;
   g1.cumsum = cumsum;
   g1.w = w1;
@@ -124,10 +128,9 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   g1.Kd = K;
   g1.status = status;
   g1.bounds = bounds1;
-  if ((e = moe::launch_grouped_gemm(g1, st)) != cudaSuccess) return launch_status(e);
-
-  if ((e = moe::launch_swiglu_quant(c1, R, I, E, topK, pts1, sorted, cumsum, nullptr, q2, pts2, expert_idx, bounds2,
-                                    st)) != cudaSuccess)
+  // GMM1 and SwiGLU: fused into one kernel when every expert runs on the tcgen05 pairs
+  if ((e = moe::launch_gemm1_swiglu(g1, I, topK, pts1, sorted, expert_idx, q2, pts2, bounds2,
+                                    at<int32_t>(ws, L.sw_done), st)) != cudaSuccess)
     return launch_status(e);
 
   moe::GroupedGemmProblem g2{};
@@ -399,9 +402,11 @@ int32_t moe_front_reorder(const moe_dims_t* d, const uint16_t* x, const int32_t*
                                                  workspace, static_cast<cudaStream_t>(stream)));
 }
 
+// GEMM stage workspace: the status word, then (moe_gmm1_swiglu) E int32 counters.
+constexpr size_t kGmmCounters = 16;
 size_t moe_gmm_workspace_size(const moe_dims_t* d) {
   if (check_dims(d) != MOE_OK) return 0;
-  return kAlign;
+  return align_up(kGmmCounters + (size_t)d->E * 4);
 }
 
 size_t moe_weight_tiles_bytes(const moe_dims_t* d, int32_t gemm) {
@@ -427,7 +432,7 @@ int32_t moe_gmm1(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* sor
   if (rc != MOE_OK) return rc;
   if (!a1_f16 || !cumsum || !w1 || !s1 || !c1 || !workspace) return MOE_ERR_NULL;
   if (!all_aligned16({a1_f16, sorted_src_route, cumsum, a1_bounds, w1, s1, c1, workspace})) return MOE_ERR_ALIGN;
-  if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE;
+  if (workspace_bytes < moe_gmm_workspace_size(d)) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   moe::GroupedGemmProblem g{};
   g.act = a1_f16;
@@ -465,6 +470,42 @@ int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* p
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+int32_t moe_gmm1_swiglu(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int32_t* a1_bounds,
+                        const int8_t* w1, const float* s1, uint16_t* c1, const float* pts1,
+                        const int32_t* sorted_src_route, const int32_t* expert_idx, uint16_t* q2_f16, float* pts2,
+                        int32_t* q2_bounds, void* workspace, size_t workspace_bytes, void* stream) {
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (!a1_f16 || !cumsum || !w1 || !s1 || !c1 || !pts1 || !sorted_src_route || !q2_f16 || !pts2 || !workspace ||
+      (q2_bounds && !expert_idx))
+    return MOE_ERR_NULL;
+  if (!all_aligned16({a1_f16, cumsum, a1_bounds, w1, s1, c1, pts1, sorted_src_route, expert_idx, q2_f16, pts2,
+                      q2_bounds, workspace}))
+    return MOE_ERR_ALIGN;
+  if (workspace_bytes < moe_gmm_workspace_size(d)) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  moe::GroupedGemmProblem g{};
+  g.act = a1_f16;
+  g.topK = d->topK;
+  g.act_rows = d->M * d->topK;
+  g.cumsum = cumsum;
+  g.w = w1;
+  g.w_kb = weight_kb(d, d->K);
+  g.scale = s1;
+  g.C = c1;
+  g.R = d->M * d->topK;
+  g.E = d->E;
+  g.N = 2 * d->I;
+  g.Kd = d->K;
+  g.status = static_cast<int32_t*>(workspace);
+  g.bounds = a1_bounds;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, kGmmCounters + (size_t)d->E * 4, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  int32_t* counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kGmmCounters);
+  return launch_status(moe::launch_gemm1_swiglu(g, d->I, d->topK, pts1, sorted_src_route, expert_idx, q2_f16, pts2,
+                                                q2_bounds, counters, st));
+}
+
 int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cumsum, const int32_t* q2_bounds,
                  const int8_t* w2, const float* s2, uint16_t* c2, void* workspace, size_t workspace_bytes,
                  void* stream) {
@@ -472,7 +513,7 @@ int32_t moe_gmm2(const moe_dims_t* d, const uint16_t* q2_f16, const int32_t* cum
   if (rc != MOE_OK) return rc;
   if (!q2_f16 || !cumsum || !w2 || !s2 || !c2 || !workspace) return MOE_ERR_NULL;
   if (!all_aligned16({q2_f16, cumsum, q2_bounds, w2, s2, c2, workspace})) return MOE_ERR_ALIGN;
-  if (workspace_bytes < kAlign) return MOE_ERR_WORKSPACE;
+  if (workspace_bytes < moe_gmm_workspace_size(d)) return MOE_ERR_WORKSPACE;
   if ((rc = check_device()) != MOE_OK) return rc;
   moe::GroupedGemmProblem g{};
   g.act = q2_f16;

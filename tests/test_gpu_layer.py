@@ -56,6 +56,7 @@ SMALL = [
     synth.Workload("zipf_small", 200, 512, 128, 16, 4, "zipf", 103),
     synth.Workload("one_token", 1, 1024, 256, 8, 8, "uniform", 104),
     synth.Workload("wide_tile", 700, 256, 64, 4, 2, "uniform", 105),
+    synth.Workload("fused_i1408", 1024, 512, 1408, 4, 1, "uniform", 106),   # SwiGLU fused into GMM1
 ]
 
 
@@ -107,6 +108,24 @@ def test_layer_invalid_routes_and_zero_tokens():
     got = host(out)
     assert_out_close(got, ref)
     assert not got[10].astype(np.float32).any() and not got[20].astype(np.float32).any()
+
+
+def test_layer_fused_swiglu_invalid_routes_and_zero_tokens():
+    """The layer with SwiGLU fused into the tcgen05 GMM1 (>= 256 routes per expert):
+    invalid routes are left out of the fused rows, zero tokens give zeros."""
+    w = synth.Workload("fused_edge", 1100, 256, 192, 4, 1, "uniform", 114)
+    inp = synth.make_inputs(w)
+    inp["expert_idx"][[3, 500, 1099], 0] = -1
+    inp["expert_idx"][7, 0] = 77
+    inp["x"][20] = 0
+    ref = oracle.layer_fwd(inp)
+    out, ws = run_layer(w, upload_inputs(inp), layout=1)
+    got = host(out)
+    assert moe.moe_workspace_status(ws) == 0
+    assert_out_close(got, ref)
+    assert not got[[3, 7, 20, 500, 1099]].astype(np.float32).any()
+    same = (got.view(np.uint16) == ref.view(np.uint16)).mean()
+    assert same > 0.99, "only %.4f of outputs bit-identical" % same
 
 
 def test_layer_repeated_calls_identical():
@@ -259,9 +278,9 @@ def test_layer_full_size_sampled(cfg, layout):
     R = w.R
     ref_rs = oracle.route_sort(inp["expert_idx"], w.E)
     wsb = host(ws)
-    # the workspace starts with the status word and the two activation-bound arrays,
-    # then (256-byte aligned) the sorted route table
-    off = (16 + 2 * w.E * moe.BOUND_SEGMENTS * 4 + 255) // 256 * 256
+    # the workspace starts with the status word, the two activation-bound arrays and
+    # the fused SwiGLU's per-expert counters, then (256-byte aligned) the sorted route table
+    off = (16 + 2 * w.E * moe.BOUND_SEGMENTS * 4 + 4 * w.E + 255) // 256 * 256
     sorted_dev = wsb[off:off + 4 * R].view(np.int32)
     assert_bits_equal(sorted_dev, ref_rs["sorted_src_route"], "sorted_src_route")
     toks = _sample_tokens(w.M, 24, w.seed)

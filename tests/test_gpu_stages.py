@@ -358,6 +358,53 @@ def test_gmm_pairs_only_with_small_experts(bounded):
     assert_bits_equal(host(c2), c2_ref, "c2")
 
 
+FUSED_CASES = [
+    # every expert on the tcgen05 pairs (>= 256 routes per expert): SwiGLU inside GMM1
+    synth.Workload("f_prefill_i", 2048, 512, 1408, 8, 1, "uniform", 91),   # the prefill I, 6 vectors per lane
+    synth.Workload("f_i64", 1024, 1024, 64, 2, 2, "biased", 92),           # a row half of one vector
+    synth.Workload("f_i1536", 600, 256, 1536, 2, 1, "zipf", 93),            # the largest fused I
+    synth.Workload("f_tiles", 1800, 256, 320, 6, 1, "zipf", 94),            # short tiles, uneven experts
+    # not fused: both engines (25 routes per expert), or I beyond the fused rows
+    synth.Workload("f_hybrid", 400, 512, 192, 32, 2, "zipf", 95),
+    synth.Workload("f_i2048", 600, 256, 2048, 2, 1, "uniform", 96),
+]
+
+
+@pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
+@pytest.mark.parametrize("w", FUSED_CASES, ids=[w.name for w in FUSED_CASES])
+def test_gmm1_swiglu_matches_the_separate_kernels(w, bounded):
+    """moe_gmm1_swiglu (SwiGLU fused into the tcgen05 GMM1 where it applies) writes the
+    same c1, q2, pts2 and q2 bounds as moe_gmm1 followed by moe_swiglu_quant, bit for
+    bit, on two calls in a row."""
+    inp, rs, xq, pts1 = _stage_inputs(w)
+    d = _dims(w, 1)
+    a1 = dev(_a1(xq, rs, w.topK, w.R))
+    cs, srt, ei = dev(rs["cumsum"]), dev(rs["sorted_src_route"]), dev(inp["expert_idx"])
+    w1, s1, p1 = _weights(d, 1, inp["w1"], 1), dev(inp["s1"]), dev(pts1)
+    b1 = dev(_bounds_ref(_a1(xq, rs, w.topK, w.R), rs["cumsum"], w.E)) if bounded else None
+    ws = empty(moe.moe_gmm_workspace_size(d), torch.uint8)
+    Rv = w.R - rs["invalid"]
+
+    def run(fused):
+        c1 = torch.full((w.R, 2 * w.I), float("nan"), dtype=torch.float16, device="cuda")
+        q2 = torch.full((w.R, w.I), float("nan"), dtype=torch.float16, device="cuda")
+        pts2 = torch.full((w.R,), float("nan"), dtype=torch.float32, device="cuda")
+        b2 = torch.zeros((w.E, moe.BOUND_SEGMENTS), dtype=torch.int32, device="cuda")
+        if fused:
+            moe.moe_gmm1_swiglu(d, a1, cs, b1, w1, s1, c1, p1, srt, ei, q2, pts2, b2, ws)
+        else:
+            moe.moe_gmm1(d, a1, None, cs, b1, w1, s1, c1, ws)
+            moe.moe_swiglu_quant(d, c1, p1, srt, cs, ei, None, q2, pts2, b2)
+        assert moe.moe_workspace_status(ws) == 0
+        return [host(t) for t in (c1[:Rv], q2[:Rv], pts2[:Rv], b2)]
+
+    ref = run(False)
+    for call in range(2):
+        got = run(True)
+        for n, g, r in zip(["c1", "q2", "pts2", "q2 bounds"], got, ref):
+            assert_bits_equal(g, r, "%s (%s, call %d)" % (n, w.name, call))
+
+
 @pytest.mark.parametrize("E,N,D", [(3, 128, 128), (2, 384, 192), (2, 256, 64), (1, 128, 1408), (2, 128, 7168),
                                    (3, 256, 320)])
 def test_pack_weight_tiles_layout(E, N, D):
