@@ -413,6 +413,15 @@ int32_t moe_combine_unpermute(const moe_dims_t* d, const uint16_t* c2, const flo
  */
 int32_t moe_selftest_wait_timeout(int32_t* status, uint32_t limit_us, void* stream);
 
+/*
+ * The same for the bounded wait on a count raised by other CTAs (the per-expert item
+ * counters the SwiGLU fused into GMM1 waits on, see moe_gmm1_swiglu): a one-warp kernel
+ * clears *count (device int32), waits for it to reach 1, which nothing does, gives up
+ * after limit_us microseconds (1 .. 2,000,000) and writes MOE_ERR_TIMEOUT to *status
+ * (device memory, cleared first).  Asynchronous on `stream`.
+ */
+int32_t moe_selftest_count_timeout(int32_t* status, int32_t* count, uint32_t limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

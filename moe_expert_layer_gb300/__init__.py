@@ -26,7 +26,7 @@ EXPORTS = [
     "moe_workspace_clear_status", "moe_route_sort_workspace_size", "moe_route_sort",
     "moe_quant_tokens", "moe_quant_dispatch", "moe_front_reorder", "moe_gmm_workspace_size", "moe_gmm1",
     "moe_swiglu_quant", "moe_gmm1_swiglu", "moe_gmm2", "moe_combine_unpermute", "moe_route_sort_noalloc",
-    "moe_selftest_wait_timeout",
+    "moe_selftest_wait_timeout", "moe_selftest_count_timeout",
     "moe_layer_graph_create", "moe_layer_graph_create_host", "moe_layer_graph_launch", "moe_layer_graph_destroy",
     "moe_weight_tiles_bytes", "moe_pack_weight_tiles",
 ]
@@ -90,6 +90,7 @@ def load_library(path=None):
         "moe_combine_unpermute": ([D] + [vp] * 6, i32),
         "moe_route_sort_noalloc": ([D] + [vp] * 6, i32),
         "moe_selftest_wait_timeout": ([vp, ctypes.c_uint32, vp], i32),
+        "moe_selftest_count_timeout": ([vp, vp, ctypes.c_uint32, vp], i32),
         "moe_weight_tiles_bytes": ([D, i32], sz),
         "moe_pack_weight_tiles": ([D, i32, vp, vp, vp], i32),
     }
@@ -273,6 +274,12 @@ def moe_selftest_wait_timeout(status, limit_us, stream=None):
     """Runs the bounded-wait self-test; status (int32 device tensor) receives the code."""
     _check("moe_selftest_wait_timeout", load_library().moe_selftest_wait_timeout(
         _p(status), limit_us, _stream(stream)))
+
+
+def moe_selftest_count_timeout(status, count, limit_us, stream=None):
+    """Runs the bounded count-wait self-test; status and count are int32 device tensors."""
+    _check("moe_selftest_count_timeout", load_library().moe_selftest_count_timeout(
+        _p(status), _p(count), limit_us, _stream(stream)))
 
 
 # Largest route count (M * topK) moe_route_sort_noalloc accepts (its fixed scratch).

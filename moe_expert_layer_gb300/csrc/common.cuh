@@ -113,6 +113,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *count >= target, a count that other CTAs of the same grid raise
+// (the fused SwiGLU's per-expert item counters): acquire loads between short sleeps;
+// gives up (returns false) after limit_ns of wall time.
+__device__ __forceinline__ bool count_wait_bounded(const int32_t* count, int target,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
+  if (ld_acquire(count) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(256);
+    if (ld_acquire(count) >= target) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // 2-D tiled TMA load of box {x: inner, y: outer} at coordinates (x, y) into smem,
 // completing `bar`'s transaction count.
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32_t y,

@@ -155,12 +155,6 @@ constexpr int kSwigluMaxVpl = 6;                     // 16-byte vectors per lane
 constexpr int kSwigluMaxI = kSwigluMaxVpl * 32 * 8;  // 1536
 constexpr int kSwigluCountPerItem = 2 * 16;          // drain warps of a pair
 
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -1023,19 +1017,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (args.sw_q2 && ok) {
       // the rest of this warp's rows, each once its expert is complete (bounded wait)
-      const uint64_t t0 = globaltimer_ns();
       while (sw_row < sw_valid) {
         while (s_end[sw_e] <= sw_row) ++sw_e;
         const int lo = sw_e ? s_end[sw_e - 1] : 0;
         const int target = kSwigluCountPerItem * expert_items(s_end[sw_e] - lo, args.split_rows, n_cb, inl);
-        if (__shfl_sync(0xffffffffu, lane == 0 ? ld_acquire(args.sw_done + sw_e) : 0, 0) < target) {
-          if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            record_status(args.status, MOE_ERR_TIMEOUT);
-            break;
-          }
-          __nanosleep(256);
-          continue;
+        const int done = lane == 0 ? (count_wait_bounded(args.sw_done + sw_e, target) ? 1 : 0) : 0;
+        if (!__shfl_sync(0xffffffffu, done, 0)) {
+          *abort_flag = 1;
+          record_status(args.status, MOE_ERR_TIMEOUT);
+          break;
         }
         swiglu_row_warp(args, sw_row, sw_e, lane);
         sw_row += sw_stride;
