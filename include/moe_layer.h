@@ -17,8 +17,8 @@
  *     memory; scratch space comes from the caller's `workspace` (moe_route_sort_noalloc
  *     alone uses a fixed scratch array inside the library instead).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the legacy
- *     default stream).  No entry point synchronises, except moe_layer_fwd_host and
- *     moe_workspace_status, which say so.
+ *     default stream).  No entry point synchronises, except moe_layer_fwd_host,
+ *     moe_workspace_status and the pipeline's calls, which say so.
  *   - Arrays are dense row-major with the last index contiguous.  Every device
  *     pointer must be 16-byte aligned (the layer's workspace 256-byte aligned), and
  *     every entry point checks this for the pointers it is given (MOE_ERR_ALIGN);
@@ -180,6 +180,48 @@ int32_t moe_layer_fwd_host(const moe_dims_t* d, const uint16_t* x_host,
                            const int8_t* w1, const float* s1, const int8_t* w2, const float* s2,
                            uint16_t* out_host, void* workspace, size_t workspace_bytes,
                            void* stream);
+
+/*
+ * A pipelined executor for a serving loop whose batches arrive and leave in HOST
+ * memory: consecutive batches overlap their host->device copies, the layer and the
+ * device->host copy of the result, on three streams the pipeline owns (the copies
+ * of batch n+1 and n-1 run while the layer computes batch n).  Up to `depth` batches
+ * (1..8) are in flight; each has its own staging buffers in the workspace, the
+ * layer's own buffers are shared (the layer runs one batch at a time, as a CUDA
+ * graph per staging slot).
+ *   moe_layer_pipeline_workspace_size: device bytes for `depth` slots (0 for bad
+ *     dimensions or depth).
+ *   moe_layer_pipeline_create: checks as moe_layer_fwd (plus 1 <= depth <= 8:
+ *     MOE_ERR_SHAPE), creates the streams, events and graphs (host objects; the
+ *     only host memory it allocates is one page-locked status word per slot) on the
+ *     current device; nothing runs yet.  Weights and workspace must stay allocated
+ *     until moe_layer_pipeline_destroy.
+ *   moe_layer_pipeline_submit: enqueues one batch (x_host [M][K], expert_idx_host
+ *     [M][topK], probs_host [M][topK] in; out_host [M][K] out) and returns its ticket
+ *     (0, 1, 2, ... in submission order).  When `depth` batches are in flight it
+ *     first waits (host) until the oldest has completed.  The host buffers belong to
+ *     the pipeline until their batch has completed: inputs must not change, out_host
+ *     must not be read before then.  Page-locked host buffers (cudaHostAlloc,
+ *     cudaHostRegister) let the copies overlap the layer; pageable ones work but
+ *     serialise them.
+ *   moe_layer_pipeline_wait: blocks until batch `ticket` and every earlier one have
+ *     completed (out_host written).  Returns MOE_ERR_TIMEOUT if a device-side wait of
+ *     any batch up to `ticket` gave up (that batch's output is then undefined),
+ *     MOE_ERR_SHAPE for a ticket not yet submitted, MOE_ERR_LAUNCH if a copy or launch
+ *     failed.
+ *   moe_layer_pipeline_destroy: waits for every batch in flight, then releases the
+ *     pipeline (NULL is a no-op).
+ */
+typedef struct moe_layer_pipeline moe_layer_pipeline_t;
+size_t moe_layer_pipeline_workspace_size(const moe_dims_t* d, int32_t depth);
+int32_t moe_layer_pipeline_create(const moe_dims_t* d, const int8_t* w1, const float* s1, const int8_t* w2,
+                                  const float* s2, void* workspace, size_t workspace_bytes, int32_t depth,
+                                  moe_layer_pipeline_t** pipeline);
+int32_t moe_layer_pipeline_submit(moe_layer_pipeline_t* pipeline, const uint16_t* x_host,
+                                  const int32_t* expert_idx_host, const float* probs_host, uint16_t* out_host,
+                                  uint64_t* ticket);
+int32_t moe_layer_pipeline_wait(moe_layer_pipeline_t* pipeline, uint64_t ticket);
+int32_t moe_layer_pipeline_destroy(moe_layer_pipeline_t* pipeline);
 
 /* Reads the status word that kernels running on `workspace` (the layer's, or a
  * GEMM stage's) set when a device-side wait gives up.  Synchronises `stream`.
@@ -366,13 +408,14 @@ int32_t moe_swiglu_quant(const moe_dims_t* d, const uint16_t* c1, const float* p
  * c1 exactly as moe_gmm1 writes it (the dispatched operand: a1_f16 [R][K] expert-major),
  * then q2_f16, pts2 and q2_bounds exactly as moe_swiglu_quant writes them from c1 (q2
  * only in the binary16-coded form the GMM2 reads; expert_idx is read only for the
- * bounds).  When every expert runs on the tcgen05 CTA pairs (from 256 routes per expert
- * on average) and I <= 1536, the SwiGLU runs inside the GMM1 kernel: the pairs'
- * drain warps requantise the rows of each expert as soon as all of the expert's GMM1
- * tiles are stored, between the tensor-core work items, so the SwiGLU kernel's pass
- * over c1 leaves the critical path (the overlap of GMM1 and SwiGLU the page builds
- * with its per-expert flags).  Otherwise GMM1 and the SwiGLU kernel run one after the
- * other.  The results are the same bits either way.
+ * bounds).  When the tcgen05 CTA pairs run (more than 24 routes per expert on
+ * average; below 256 the warp-MMA engine first takes the experts of at most 32 rows),
+ * the SwiGLU runs inside the pairs' GMM1 kernel: their drain warps requantise the rows
+ * of each expert as soon as all of the expert's GMM1 tiles are stored, between the
+ * tensor-core work items, so the SwiGLU kernel's pass over c1 leaves the critical path
+ * (the overlap of GMM1 and SwiGLU the page builds with its per-expert flags).
+ * Otherwise GMM1 and the SwiGLU kernel run one after the other.  The results are the
+ * same bits either way.
  *   workspace: moe_gmm_workspace_size(d) bytes (status word and per-expert counters).
  */
 int32_t moe_gmm1_swiglu(const moe_dims_t* d, const uint16_t* a1_f16, const int32_t* cumsum, const int32_t* a1_bounds,

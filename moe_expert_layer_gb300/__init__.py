@@ -28,6 +28,8 @@ EXPORTS = [
     "moe_swiglu_quant", "moe_gmm1_swiglu", "moe_gmm2", "moe_combine_unpermute", "moe_route_sort_noalloc",
     "moe_selftest_wait_timeout", "moe_selftest_count_timeout",
     "moe_layer_graph_create", "moe_layer_graph_create_host", "moe_layer_graph_launch", "moe_layer_graph_destroy",
+    "moe_layer_pipeline_workspace_size", "moe_layer_pipeline_create", "moe_layer_pipeline_submit",
+    "moe_layer_pipeline_wait", "moe_layer_pipeline_destroy",
     "moe_weight_tiles_bytes", "moe_pack_weight_tiles",
 ]
 
@@ -75,6 +77,11 @@ def load_library(path=None):
         "moe_layer_graph_create_host": ([D] + [vp] * 9 + [sz, vp, ctypes.POINTER(vp)], i32),
         "moe_layer_graph_launch": ([vp, vp], i32),
         "moe_layer_graph_destroy": ([vp], i32),
+        "moe_layer_pipeline_workspace_size": ([D, i32], sz),
+        "moe_layer_pipeline_create": ([D] + [vp] * 5 + [sz, i32, ctypes.POINTER(vp)], i32),
+        "moe_layer_pipeline_submit": ([vp] * 5 + [ctypes.POINTER(ctypes.c_uint64)], i32),
+        "moe_layer_pipeline_wait": ([vp, ctypes.c_uint64], i32),
+        "moe_layer_pipeline_destroy": ([vp], i32),
         "moe_workspace_status": ([vp, ctypes.POINTER(i32), vp], i32),
         "moe_workspace_clear_status": ([vp, vp], i32),
         "moe_route_sort_workspace_size": ([D], sz),
@@ -187,6 +194,35 @@ def moe_layer_graph_launch(graph, stream=None):
 
 def moe_layer_graph_destroy(graph):
     _check("moe_layer_graph_destroy", load_library().moe_layer_graph_destroy(graph))
+
+
+def moe_layer_pipeline_workspace_size(d, depth):
+    return load_library().moe_layer_pipeline_workspace_size(ctypes.byref(d), depth)
+
+
+def moe_layer_pipeline_create(d, w1, s1, w2, s2, workspace, depth=2):
+    """The pipelined host-memory executor; returns its handle."""
+    h = ctypes.c_void_p()
+    _check("moe_layer_pipeline_create", load_library().moe_layer_pipeline_create(
+        ctypes.byref(d), _p(w1), _p(s1), _p(w2), _p(s2), _p(workspace),
+        workspace.numel() * workspace.element_size(), depth, ctypes.byref(h)))
+    return h
+
+
+def moe_layer_pipeline_submit(pipeline, x_host, expert_idx_host, probs_host, out_host):
+    """Enqueues one batch (host tensors); returns its ticket."""
+    t = ctypes.c_uint64()
+    _check("moe_layer_pipeline_submit", load_library().moe_layer_pipeline_submit(
+        pipeline, _p(x_host), _p(expert_idx_host), _p(probs_host), _p(out_host), ctypes.byref(t)))
+    return t.value
+
+
+def moe_layer_pipeline_wait(pipeline, ticket):
+    _check("moe_layer_pipeline_wait", load_library().moe_layer_pipeline_wait(pipeline, ticket))
+
+
+def moe_layer_pipeline_destroy(pipeline):
+    _check("moe_layer_pipeline_destroy", load_library().moe_layer_pipeline_destroy(pipeline))
 
 
 def moe_layer_fwd_host(d, x_host, expert_idx_host, probs_host, w1, s1, w2, s2, out_host, workspace,

@@ -52,12 +52,18 @@ cudaError_t launch_gemm1_swiglu(const GroupedGemmProblem& g1, int I, int topK, c
                                 const int32_t* sorted_src_route, const int32_t* expert_idx, uint16_t* q2,
                                 float* pts2, int32_t* q2_bounds, int32_t* sw_done, cudaStream_t stream, bool* fused) {
   const double mean_rows = (double)g1.R / (double)g1.E;
-  const bool fuse = grouped_gemm_reads_bounds(g1.R, g1.E) && mean_rows >= kPairsOnlyRows && !g1.gather_route &&
-                    I <= kFusedSwigluMaxI && pair_grid_coresident();
+  const bool fuse = grouped_gemm_reads_bounds(g1.R, g1.E) && !g1.gather_route && I <= kFusedSwigluMaxI &&
+                    pair_grid_coresident();
   if (fused) *fused = fuse;
   if (fuse) {
     GroupedGemmProblem q = g1;
     q.split_rows = 0;
+    if (mean_rows < kPairsOnlyRows) {
+      // the small experts' GMM1 first: their rows are complete when the pairs start
+      q.split_rows = kSplitRows;
+      cudaError_t e = launch_grouped_gemm_hmma(q, 32, stream);
+      if (e != cudaSuccess) return e;
+    }
     q.topK = topK;  // a row's token is its route / topK
     q.sw_pts1 = pts1;
     q.sw_sorted = sorted_src_route;

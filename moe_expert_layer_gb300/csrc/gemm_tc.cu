@@ -110,6 +110,7 @@ constexpr int kSmemBytes = kWStages * kWBytes + kStages * kXBytes + 1024;
 constexpr int kWProducerWarp = 0, kMmaWarp = 1, kXProducerWarp = 2, kRelayWarp = 3, kConvWarp0 = 4,
               kNumConvWarps = 4, kDrainWarp0 = 8, kNumDrainWarps = 16;
 static_assert(kThreads == 32 * (kDrainWarp0 + kNumDrainWarps), "warp roles");
+static_assert(kDrainWarp0 % 4 == 0 && kNumDrainWarps % 4 == 0, "drain warps: whole sets of the 4 SM sub-partitions");
 static_assert(kSmemBytes + 13 * 1024 <= 227 * 1024, "shared memory (dynamic + ~12.4 KB static)");
 static_assert(kACol0 + kStages * kACols == kTmemCols, "tensor memory: accumulator + A buffers");
 // kind::f16 instruction descriptor: D f32, A/B f16, both K-major, M = 256; N is set per item
@@ -140,19 +141,21 @@ struct Args {
 };
 
 // ------------------------------------------------------------------ SwiGLU fused into GMM1
-// With args.sw_q2 set (GMM1, every expert on the pairs, I <= kSwigluMaxI) the drain
-// warps also run SwiGLU + requant, one expanded row per warp at a time, on the rows of
-// experts all of whose GMM1 items are stored.  Every drain warp counts each item it
-// has finished (its epilogue stores fenced first) on the item's expert; an expert is
-// complete at kSwigluCountPerItem * (its items).  Drain warp gw of the grid owns rows
-// gw, gw + W, ... (W = all drain warps), taken in order: between items, while the next
-// accumulator chunk is not ready, it requantises its next rows as far as their experts
-// are complete; after its last item it finishes its rows, waiting (bounded) for their
-// experts.  No wait ever depends on a CTA that is not already running: the pairs
-// launch only when all of them can be resident at once (the host checks the
-// occupancy).  The arithmetic is swiglu.cuh's, as in the SwiGLU kernel: the same bits.
+// With args.sw_q2 set (GMM1 of a tiled operand) the drain warps also run SwiGLU +
+// requant, one expanded row per warp at a time, on the rows of experts all of whose
+// GMM1 items are stored.  Every drain warp counts each item it has finished (its
+// epilogue stores fenced first) on the item's expert; an expert is complete at
+// kSwigluCountPerItem * (its items), so the experts the warp-MMA engine served before
+// this launch (no items here) are complete from the start.  Row warp gw of the grid
+// owns rows gw, gw + W, ... (W = all row warps), taken in order: between items, while
+// the next accumulator chunk is not ready, it requantises its next rows as far as
+// their experts are complete; after its last item it finishes its rows, waiting
+// (bounded) for their experts.  No wait ever depends on a CTA that is not already
+// running: the pairs launch only when all of them can be resident at once (the host
+// checks the occupancy).  The arithmetic is swiglu.cuh's, as in the SwiGLU kernel:
+// the same bits.
 constexpr int kSwigluMaxVpl = 6;                     // 16-byte vectors per lane of a row's half
-constexpr int kSwigluMaxI = kSwigluMaxVpl * 32 * 8;  // 1536
+constexpr int kSwigluRegI = kSwigluMaxVpl * 32 * 8;  // I <= 1536: the row stays in registers
 constexpr int kSwigluCountPerItem = 2 * 16;          // drain warps of a pair
 
 // Non-blocking test of an mbarrier phase.
@@ -174,15 +177,76 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // twice from the loaded halves (for the max, then for the codes) rather than kept:
 // the same instructions on the same inputs give the same values, and the drain warps'
 // registers hold the row only once.
+union SwVec {
+  int4 v;
+  __half h[8];
+};
+
+// Rows longer than the registers hold (I > 1536): the row is read twice (the second
+// time from L2), 128 vectors at a time, one 1024-deep bound segment per pass.
+__device__ __noinline__ void swiglu_long_row_warp(const Args& a, int d, int e, int lane, float p1) {
+  const int I = a.N >> 1, nvec = I >> 3;
+  const int4* gate = reinterpret_cast<const int4*>(a.C + (size_t)d * a.N);
+  const int4* up = gate + nvec;
+  constexpr int kVpl = kBoundSegment / 8 / 32;  // 4 vectors per lane: one segment
+  float amax = 0.0f;
+#pragma unroll 1
+  for (int v0 = 0; v0 < nvec; v0 += 32 * kVpl) {
+    SwVec g[kVpl], u[kVpl];
+#pragma unroll
+    for (int i = 0; i < kVpl; ++i) {
+      const int v = v0 + lane + 32 * i;
+      g[i].v = v < nvec ? __ldcg(gate + v) : make_int4(0, 0, 0, 0);
+      u[i].v = v < nvec ? __ldcg(up + v) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kVpl; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(swiglu_y(g[i].h[j], u[i].h[j], p1)));
+  }
+  amax = warp_max(amax);
+  const float inv = swiglu_inv(amax);
+  if (lane == 0) a.sw_pts2[d] = swiglu_pts2(amax, p1);
+  int4* q2 = reinterpret_cast<int4*>(a.sw_q2 + (size_t)d * I);
+#pragma unroll 1
+  for (int v0 = 0, seg = 0; v0 < nvec; v0 += 32 * kVpl, ++seg) {
+    SwVec g[kVpl], u[kVpl];
+#pragma unroll
+    for (int i = 0; i < kVpl; ++i) {
+      const int v = v0 + lane + 32 * i;
+      g[i].v = v < nvec ? __ldcg(gate + v) : make_int4(0, 0, 0, 0);
+      u[i].v = v < nvec ? __ldcg(up + v) : make_int4(0, 0, 0, 0);
+    }
+    int l1 = 0;
+#pragma unroll
+    for (int i = 0; i < kVpl; ++i) {
+      const int v = v0 + lane + 32 * i;
+      if (v < nvec) {
+        float y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) y[j] = swiglu_y(g[i].h[j], u[i].h[j], p1);
+        int l = 0;
+        q2[v] = swiglu_codes8(y, inv, &l);
+        l1 += l;
+      }
+    }
+    if (a.sw_bounds) {
+      const int sum = __reduce_add_sync(0xffffffffu, l1);
+      if (lane == 0) atomicMax(a.sw_bounds + (size_t)e * kBoundSegments + seg, sum);
+    }
+  }
+}
+
 __device__ __forceinline__ void swiglu_row_warp(const Args& a, int d, int e, int lane) {
   const int I = a.N >> 1, nvec = I >> 3;
   const int4* gate = reinterpret_cast<const int4*>(a.C + (size_t)d * a.N);
   const int4* up = gate + nvec;
   const float p1 = __ldg(a.sw_pts1 + __ldg(a.sw_sorted + d) / a.topK);
-  union V {
-    int4 v;
-    __half h[8];
-  };
+  if (I > kSwigluRegI) {
+    swiglu_long_row_warp(a, d, e, lane, p1);
+    return;
+  }
+  using V = SwVec;
   V g[kSwigluMaxVpl], u[kSwigluMaxVpl];
 #pragma unroll
   for (int i = 0; i < kSwigluMaxVpl; ++i) {
@@ -889,10 +953,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t accempty_remote = cluster_addr(&accempty_bar, 0);
     int c = 0;
     // fused SwiGLU: this warp's rows gw, gw + stride, ... of the valid ones, and the
-    // expert of the next one (rows only move forward)
-    const int sw_stride = (int)gridDim.x * kNumDrainWarps;
-    int sw_row = (int)blockIdx.x * kNumDrainWarps + (warp - kDrainWarp0);
+    // expert of the next one (rows only move forward).  The rows go to the drain warps
+    // of the three SM sub-partitions (warp % 4) other than the MMA-issuing warp's: the
+    // one thread that issues the MMAs sets the kernel's pace, and SwiGLU work beside it
+    // slows its issue (prefill GMM1 + SwiGLU: 713 us with every drain warp on rows,
+    // 696 us without the issuer's sub-partition; fewer sub-partitions lengthen the tail).
+    constexpr int kRowWarps = kNumDrainWarps - kNumDrainWarps / 4;
+    const bool row_warp = quarter != (kMmaWarp & 3);
+    int row_rank = 0;
+    for (int w = kDrainWarp0; w < warp; ++w) row_rank += (w & 3) != (kMmaWarp & 3) ? 1 : 0;
+    const int sw_stride = (int)gridDim.x * kRowWarps;
     const int sw_valid = s_end[E - 1];
+    int sw_row = row_warp ? (int)blockIdx.x * kRowWarps + row_rank : sw_valid;
     int sw_e = 0;
     bool ok = true;
     int e_hint = 0;
@@ -1095,9 +1167,9 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.sw_pts2 = p.sw_pts2;
   a.sw_bounds = p.sw_bounds;
   a.sw_done = p.sw_done;
-  if (a.sw_q2 && (GATHER || p.split_rows != 0 || p.N / 2 > kSwigluMaxI || p.topK < 1 || !a.sw_pts1 || !a.sw_sorted ||
-                  !a.sw_pts2 || !a.sw_done))
-    return cudaErrorInvalidValue;  // the fused SwiGLU needs every expert of a tiled GMM1 on the pairs
+  if (a.sw_q2 && (GATHER || p.N / 2 > kFusedSwigluMaxI || p.topK < 1 || !a.sw_pts1 || !a.sw_sorted || !a.sw_pts2 ||
+                  !a.sw_done))
+    return cudaErrorInvalidValue;  // the fused SwiGLU runs on a tiled GMM1
 #ifdef MOE_GEMM_PROFILE
   a.prof = g_gemm_prof;
   if (!a.prof) return cudaErrorInvalidValue;
@@ -1109,7 +1181,7 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
 
 }  // namespace
 
-static_assert(kSwigluMaxI == kFusedSwigluMaxI, "fused SwiGLU row size");
+static_assert(kFusedSwigluMaxI <= kBoundSegments * kBoundSegment, "fused SwiGLU: a bound segment per pass");
 
 bool pair_grid_coresident() {
   static PerContextOnce queried;

@@ -70,14 +70,15 @@ cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t str
 // Whether every CTA pair of the tcgen05 kernel's grid can be resident at once on the
 // current device (the fused SwiGLU's waits rely on it).
 bool pair_grid_coresident();
-// The largest I the tcgen05 pairs fuse SwiGLU for (a row's half: 6 vectors per lane).
-constexpr int kFusedSwigluMaxI = 1536;
+// The largest I the tcgen05 pairs fuse SwiGLU for (the ABI's largest I).
+constexpr int kFusedSwigluMaxI = 8192;
 // GMM1 (g1: c1 written as usual) followed by SwiGLU + requant of its rows (q2 as
 // binary16 codes, pts2, q2_bounds if not null), as launch_grouped_gemm then
-// launch_swiglu_quant would compute them.  When every expert runs on the tcgen05 pairs,
-// I <= kFusedSwigluMaxI and the pairs can all be resident, the SwiGLU runs inside the
-// GMM1 kernel (sw_done: [E] int32 the caller has zeroed); otherwise the two kernels
-// run one after the other.  Returns in *fused which of the two happened.
+// launch_swiglu_quant would compute them.  When the tcgen05 pairs run (more than 24
+// rows per expert on average; the warp-MMA engine's share, if any, first), the
+// operand is tiled and the pairs can all be resident, the SwiGLU runs inside the
+// pairs' GMM1 kernel (sw_done: [E] int32 the caller has zeroed); otherwise GMM1 and
+// the SwiGLU kernel run one after the other.  Returns in *fused which happened.
 cudaError_t launch_gemm1_swiglu(const GroupedGemmProblem& g1, int I, int topK, const float* pts1,
                                 const int32_t* sorted_src_route, const int32_t* expert_idx, uint16_t* q2,
                                 float* pts2, int32_t* q2_bounds, int32_t* sw_done, cudaStream_t stream,

@@ -17,6 +17,26 @@ struct moe_layer_graph {
   cudaGraphExec_t exec;
 };
 
+// The pipelined executor (include/moe_layer.h): per staging slot the inputs and
+// output of one batch, its layer graph, and the events that order the three streams.
+constexpr int kPipeMaxDepth = 8;
+struct moe_layer_pipeline {
+  int depth, device;
+  size_t x_bytes, ei_bytes, pr_bytes, out_bytes;
+  cudaStream_t copy_in, run, copy_out;
+  cudaEvent_t in_done[kPipeMaxDepth], run_done[kPipeMaxDepth], out_done[kPipeMaxDepth];
+  moe_layer_graph* graph[kPipeMaxDepth];
+  uint16_t* x[kPipeMaxDepth];
+  int32_t* ei[kPipeMaxDepth];
+  float* pr[kPipeMaxDepth];
+  uint16_t* out[kPipeMaxDepth];
+  int32_t* status_dev[kPipeMaxDepth];  // the layer's status word, copied after each batch
+  int32_t* status_host;                // page-locked, one word per slot
+  uint64_t submitted, completed;       // batches submitted; batches known complete
+  int32_t error;                       // first failure seen, and its batch
+  uint64_t error_ticket;
+};
+
 namespace {
 
 using moe::aligned16;
@@ -84,6 +104,13 @@ P* at(void* base, size_t off) {
   return reinterpret_cast<P*>(static_cast<uint8_t*>(base) + off);
 }
 
+// The pipeline's workspace: the layer's, then `depth` staging slots (x, expert_idx,
+// probs, out, status word), each part 256-byte aligned.
+size_t pipeline_slot_bytes(const moe_dims_t* d) {
+  const size_t M = d->M, K = d->K, R = M * d->topK;
+  return align_up(M * K * 2) + align_up(R * 4) + align_up(R * 4) + align_up(M * K * 2) + align_up(16);
+}
+
 int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_idx, const float* probs,
                   const int8_t* w1, const float* s1, const int8_t* w2, const float* s2, uint16_t* out,
                   void* ws, const Layout& L, cudaStream_t st) {
@@ -128,7 +155,7 @@ int32_t run_layer(const moe_dims_t* d, const uint16_t* x, const int32_t* expert_
   g1.Kd = K;
   g1.status = status;
   g1.bounds = bounds1;
-  // GMM1 and SwiGLU: fused into one kernel when every expert runs on the tcgen05 pairs
+  // GMM1 and SwiGLU: the SwiGLU inside the GMM1 kernel when the tcgen05 pairs run
   if ((e = moe::launch_gemm1_swiglu(g1, I, topK, pts1, sorted, expert_idx, q2, pts2, bounds2,
                                     at<int32_t>(ws, L.sw_done), st)) != cudaSuccess)
     return launch_status(e);
@@ -319,6 +346,160 @@ int32_t moe_layer_graph_create_host(const moe_dims_t* d, const uint16_t* x_host,
     return enqueue_layer_host(d, x_host, expert_idx_host, probs_host, w1, s1, w2, s2, out_host, workspace,
                               workspace_bytes, st);
   }, graph);
+}
+
+size_t moe_layer_pipeline_workspace_size(const moe_dims_t* d, int32_t depth) {
+  if (check_dims(d) != MOE_OK || depth < 1 || depth > kPipeMaxDepth) return 0;
+  return layout_of(d).total + (size_t)depth * pipeline_slot_bytes(d);
+}
+
+namespace {
+
+// Waits for batch t (the oldest not yet known complete) and folds in its status.
+int32_t pipeline_retire(moe_layer_pipeline_t* p, uint64_t t) {
+  const int s = (int)(t % (uint64_t)p->depth);
+  int32_t rc = MOE_OK;
+  if (cudaEventSynchronize(p->out_done[s]) != cudaSuccess)
+    rc = MOE_ERR_LAUNCH;
+  else if (p->status_host[s] != MOE_OK)
+    rc = p->status_host[s];
+  if (rc != MOE_OK && p->error == MOE_OK) {
+    p->error = rc;
+    p->error_ticket = t;
+  }
+  p->completed = t + 1;
+  return rc;
+}
+
+void pipeline_release(moe_layer_pipeline_t* p) {
+  if (p->run) {
+    cudaStreamSynchronize(p->copy_in);
+    cudaStreamSynchronize(p->run);
+    cudaStreamSynchronize(p->copy_out);
+  }
+  for (int s = 0; s < kPipeMaxDepth; ++s) {
+    moe_layer_graph_destroy(p->graph[s]);
+    if (p->in_done[s]) cudaEventDestroy(p->in_done[s]);
+    if (p->run_done[s]) cudaEventDestroy(p->run_done[s]);
+    if (p->out_done[s]) cudaEventDestroy(p->out_done[s]);
+  }
+  if (p->copy_in) cudaStreamDestroy(p->copy_in);
+  if (p->run) cudaStreamDestroy(p->run);
+  if (p->copy_out) cudaStreamDestroy(p->copy_out);
+  if (p->status_host) cudaFreeHost(p->status_host);
+  std::free(p);
+}
+
+}  // namespace
+
+int32_t moe_layer_pipeline_create(const moe_dims_t* d, const int8_t* w1, const float* s1, const int8_t* w2,
+                                  const float* s2, void* workspace, size_t workspace_bytes, int32_t depth,
+                                  moe_layer_pipeline_t** pipeline) {
+  if (!pipeline) return MOE_ERR_NULL;
+  *pipeline = nullptr;
+  int32_t rc = check_dims(d);
+  if (rc != MOE_OK) return rc;
+  if (depth < 1 || depth > kPipeMaxDepth) return MOE_ERR_SHAPE;
+  if (!w1 || !s1 || !w2 || !s2 || !workspace) return MOE_ERR_NULL;
+  if (!aligned16(w1) || !aligned16(s1) || !aligned16(w2) || !aligned16(s2) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return MOE_ERR_ALIGN;
+  const Layout L = layout_of(d);
+  if (workspace_bytes < L.total + (size_t)depth * pipeline_slot_bytes(d)) return MOE_ERR_WORKSPACE;
+  if ((rc = check_device()) != MOE_OK) return rc;
+  moe_layer_pipeline_t* p = static_cast<moe_layer_pipeline_t*>(std::calloc(1, sizeof(moe_layer_pipeline_t)));
+  if (!p) return MOE_ERR_LAUNCH;
+  const size_t M = d->M, K = d->K, R = M * d->topK;
+  p->depth = depth;
+  p->x_bytes = M * K * 2;
+  p->ei_bytes = R * 4;
+  p->pr_bytes = R * 4;
+  p->out_bytes = M * K * 2;
+  bool ok = cudaGetDevice(&p->device) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->copy_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->run, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p->copy_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaHostAlloc(reinterpret_cast<void**>(&p->status_host), kPipeMaxDepth * sizeof(int32_t),
+                          cudaHostAllocDefault) == cudaSuccess;
+  size_t off = L.total;
+  for (int s = 0; ok && s < depth; ++s) {
+    p->x[s] = at<uint16_t>(workspace, off);
+    off += align_up(p->x_bytes);
+    p->ei[s] = at<int32_t>(workspace, off);
+    off += align_up(p->ei_bytes);
+    p->pr[s] = at<float>(workspace, off);
+    off += align_up(p->pr_bytes);
+    p->out[s] = at<uint16_t>(workspace, off);
+    off += align_up(p->out_bytes);
+    p->status_dev[s] = at<int32_t>(workspace, off);
+    off += align_up(16);
+    p->status_host[s] = MOE_OK;
+    ok = cudaEventCreateWithFlags(&p->in_done[s], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->run_done[s], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p->out_done[s], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) break;
+    // the slot's layer graph: the layer on the slot's buffers, then its status word
+    // copied out of the shared layer workspace
+    const int32_t* ws_status = at<int32_t>(workspace, L.status);
+    rc = capture_graph(p->run, [&]() {
+      const int32_t r = run_layer(d, p->x[s], p->ei[s], p->pr[s], w1, s1, w2, s2, p->out[s], workspace, L, p->run);
+      if (r != MOE_OK) return r;
+      return launch_status(cudaMemcpyAsync(p->status_dev[s], ws_status, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                           p->run));
+    }, &p->graph[s]);
+    ok = rc == MOE_OK;
+  }
+  if (!ok) {
+    pipeline_release(p);
+    return rc != MOE_OK ? rc : MOE_ERR_LAUNCH;
+  }
+  *pipeline = p;
+  return MOE_OK;
+}
+
+int32_t moe_layer_pipeline_submit(moe_layer_pipeline_t* p, const uint16_t* x_host, const int32_t* expert_idx_host,
+                                  const float* probs_host, uint16_t* out_host, uint64_t* ticket) {
+  if (!p || !x_host || !expert_idx_host || !probs_host || !out_host || !ticket) return MOE_ERR_NULL;
+  if (cudaSetDevice(p->device) != cudaSuccess) return MOE_ERR_LAUNCH;
+  const uint64_t n = p->submitted;
+  const int s = (int)(n % (uint64_t)p->depth);
+  // the slot's previous batch must be complete before its buffers and events are reused
+  while (p->completed + (uint64_t)p->depth <= n) pipeline_retire(p, p->completed);
+  bool ok = cudaMemcpyAsync(p->x[s], x_host, p->x_bytes, cudaMemcpyHostToDevice, p->copy_in) == cudaSuccess &&
+            cudaMemcpyAsync(p->ei[s], expert_idx_host, p->ei_bytes, cudaMemcpyHostToDevice, p->copy_in) ==
+                cudaSuccess &&
+            cudaMemcpyAsync(p->pr[s], probs_host, p->pr_bytes, cudaMemcpyHostToDevice, p->copy_in) == cudaSuccess &&
+            cudaEventRecord(p->in_done[s], p->copy_in) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(p->run, p->in_done[s], 0) == cudaSuccess &&
+       cudaGraphLaunch(p->graph[s]->exec, p->run) == cudaSuccess &&
+       cudaEventRecord(p->run_done[s], p->run) == cudaSuccess;
+  ok = ok && cudaStreamWaitEvent(p->copy_out, p->run_done[s], 0) == cudaSuccess &&
+       cudaMemcpyAsync(out_host, p->out[s], p->out_bytes, cudaMemcpyDeviceToHost, p->copy_out) == cudaSuccess &&
+       cudaMemcpyAsync(p->status_host + s, p->status_dev[s], sizeof(int32_t), cudaMemcpyDeviceToHost,
+                       p->copy_out) == cudaSuccess &&
+       cudaEventRecord(p->out_done[s], p->copy_out) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return MOE_ERR_LAUNCH;
+  }
+  p->submitted = n + 1;
+  *ticket = n;
+  return MOE_OK;
+}
+
+int32_t moe_layer_pipeline_wait(moe_layer_pipeline_t* p, uint64_t ticket) {
+  if (!p) return MOE_ERR_NULL;
+  if (ticket >= p->submitted) return MOE_ERR_SHAPE;
+  if (cudaSetDevice(p->device) != cudaSuccess) return MOE_ERR_LAUNCH;
+  while (p->completed <= ticket) pipeline_retire(p, p->completed);
+  return (p->error != MOE_OK && p->error_ticket <= ticket) ? p->error : MOE_OK;
+}
+
+int32_t moe_layer_pipeline_destroy(moe_layer_pipeline_t* p) {
+  if (!p) return MOE_OK;
+  cudaSetDevice(p->device);
+  pipeline_release(p);
+  return MOE_OK;
 }
 
 int32_t moe_workspace_status(const void* workspace, int32_t* host_status, void* stream) {

@@ -73,6 +73,24 @@ def test_entry_points_reject_before_touching_the_device(lib):
     assert lib.moe_layer_graph_create_host(ctypes.byref(d), *([None] * 9), 0, None, ctypes.byref(h)) == -1
     assert lib.moe_layer_graph_launch(None, None) == -1
     assert lib.moe_layer_graph_destroy(None) == 0
+    # the pipelined executor: size, depth, NULL and alignment checks before any CUDA call
+    assert lib.moe_layer_pipeline_workspace_size(ctypes.byref(d), 2) > lib.moe_layer_workspace_size(ctypes.byref(d))
+    assert lib.moe_layer_pipeline_workspace_size(ctypes.byref(d), 0) == 0
+    assert lib.moe_layer_pipeline_workspace_size(ctypes.byref(d), 9) == 0
+    assert lib.moe_layer_pipeline_workspace_size(ctypes.byref(bad), 2) == 0
+    assert lib.moe_layer_pipeline_create(ctypes.byref(d), *([None] * 5), 0, 2, None) == -1
+    assert lib.moe_layer_pipeline_create(ctypes.byref(d), *([None] * 5), 0, 2, ctypes.byref(h)) == -1
+    assert h.value is None
+    assert lib.moe_layer_pipeline_create(ctypes.byref(bad), *([None] * 5), 0, 2, ctypes.byref(h)) == -2
+    assert lib.moe_layer_pipeline_create(ctypes.byref(d), *([4096] * 5), 1 << 30, 0, ctypes.byref(h)) == -2
+    assert lib.moe_layer_pipeline_create(ctypes.byref(d), *([4096] * 5), 1 << 30, 9, ctypes.byref(h)) == -2
+    assert lib.moe_layer_pipeline_create(ctypes.byref(d), 4096 + 4, *([4096] * 4), 1 << 30, 2, ctypes.byref(h)) == -3
+    assert lib.moe_layer_pipeline_create(ctypes.byref(d), *([4096] * 4), 4096 + 16, 1 << 30, 2, ctypes.byref(h)) == -3
+    assert lib.moe_layer_pipeline_create(ctypes.byref(d), *([4096] * 5), 1024, 2, ctypes.byref(h)) == -5
+    t = ctypes.c_uint64()
+    assert lib.moe_layer_pipeline_submit(None, 1, 1, 1, 1, ctypes.byref(t)) == -1
+    assert lib.moe_layer_pipeline_wait(None, 0) == -1
+    assert lib.moe_layer_pipeline_destroy(None) == 0
     # misaligned pointers -> MOE_ERR_ALIGN
     p = 4096 + 2
     assert lib.moe_layer_fwd(ctypes.byref(d), p, p, p, p, p, p, p, p, 4096, 1 << 30, None) == -3

@@ -212,6 +212,47 @@ def test_layer_host_graph_matches_host_entry_point(layout):
         moe.moe_layer_graph_destroy(g)
 
 
+@pytest.mark.parametrize("name,depth", [("ragged", 2), ("wide_tile", 1), ("wide_tile", 3)])
+def test_layer_pipeline_matches_the_layer(name, depth):
+    """The pipelined host-memory executor: five consecutive batches (other tokens and
+    routes each) through `depth` staging slots give moe_layer_fwd's outputs bit for
+    bit; tickets count from 0, a ticket not yet submitted is refused, and waiting on
+    a completed batch returns at once."""
+    w = next(c for c in SMALL if c.name == name)
+    dv = upload_inputs(synth.make_inputs(w))
+    d = moe.dims(w.M, w.K, w.I, w.E, w.topK, moe.WEIGHTS_TILES)
+    wt1, wt2 = layer_weights(d, dv, moe.WEIGHTS_TILES)
+    batches = []
+    for b in range(5):
+        wb = synth.Workload(w.name, w.M, w.K, w.I, w.E, w.topK, w.routing, w.seed + 3000 + b)
+        inp = synth.make_inputs(wb, with_weights=False)
+        batches.append({k: torch.from_numpy(inp[k]).pin_memory() for k in ("x", "expert_idx", "probs")})
+    ws = empty(moe.moe_layer_workspace_size(d), torch.uint8)
+    refs = []
+    for b in batches:
+        out = empty((w.M, w.K), torch.float16)
+        moe.moe_layer_fwd(d, b["x"].cuda(), b["expert_idx"].cuda(), b["probs"].cuda(), wt1, dv["s1"], wt2,
+                          dv["s2"], out, ws)
+        refs.append(out.cpu())
+    pws = torch.full((moe.moe_layer_pipeline_workspace_size(d, depth),), 0x7f, dtype=torch.uint8, device="cuda")
+    p = moe.moe_layer_pipeline_create(d, wt1, dv["s1"], wt2, dv["s2"], pws, depth)
+    try:
+        outs = [torch.full((w.M, w.K), float("nan"), dtype=torch.float16).pin_memory() for _ in batches]
+        tickets = [moe.moe_layer_pipeline_submit(p, b["x"], b["expert_idx"], b["probs"], o)
+                   for b, o in zip(batches, outs)]
+        assert tickets == list(range(len(batches)))
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_layer_pipeline_wait(p, len(batches))
+        assert e.value.code == -2
+        moe.moe_layer_pipeline_wait(p, tickets[-1])
+        for i, (o, r) in enumerate(zip(outs, refs)):
+            assert torch.equal(o, r), "batch %d" % i
+        moe.moe_layer_pipeline_wait(p, 0)
+        assert moe.moe_workspace_status(pws) == 0
+    finally:
+        moe.moe_layer_pipeline_destroy(p)
+
+
 def test_layer_graph_rejects_the_legacy_stream():
     w = SMALL[0]
     d = moe.dims(w.M, w.K, w.I, w.E, w.topK)

@@ -362,21 +362,26 @@ FUSED_CASES = [
     # every expert on the tcgen05 pairs (>= 256 routes per expert): SwiGLU inside GMM1
     synth.Workload("f_prefill_i", 2048, 512, 1408, 8, 1, "uniform", 91),   # the prefill I, 6 vectors per lane
     synth.Workload("f_i64", 1024, 1024, 64, 2, 2, "biased", 92),           # a row half of one vector
-    synth.Workload("f_i1536", 600, 256, 1536, 2, 1, "zipf", 93),            # the largest fused I
+    synth.Workload("f_i1536", 600, 256, 1536, 2, 1, "zipf", 93),            # the largest row held in registers
     synth.Workload("f_tiles", 1800, 256, 320, 6, 1, "zipf", 94),            # short tiles, uneven experts
-    # not fused: both engines (25 routes per expert), or I beyond the fused rows
+    synth.Workload("f_i2048", 600, 256, 2048, 2, 1, "uniform", 96),         # rows read twice, 1024 deep at a time
+    synth.Workload("f_i2496", 512, 256, 2496, 2, 1, "biased", 99),          # ... with a partial last pass
+    # both engines (25-255 routes per expert): experts of <= 32 rows on the warp-MMA
+    # engine first, the rest on the pairs with the SwiGLU of every row inside
     synth.Workload("f_hybrid", 400, 512, 192, 32, 2, "zipf", 95),
-    synth.Workload("f_i2048", 600, 256, 2048, 2, 1, "uniform", 96),
+    synth.Workload("f_hybrid_long", 400, 256, 2048, 16, 2, "zipf", 97),
+    # not fused: the warp-MMA engine alone (<= 24 routes per expert)
+    synth.Workload("f_warp_only", 128, 256, 192, 16, 2, "uniform", 98),
 ]
 
 
-@pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
-@pytest.mark.parametrize("w", FUSED_CASES, ids=[w.name for w in FUSED_CASES])
-def test_gmm1_swiglu_matches_the_separate_kernels(w, bounded):
-    """moe_gmm1_swiglu (SwiGLU fused into the tcgen05 GMM1 where it applies) writes the
-    same c1, q2, pts2 and q2 bounds as moe_gmm1 followed by moe_swiglu_quant, bit for
-    bit, on two calls in a row."""
-    inp, rs, xq, pts1 = _stage_inputs(w)
+def _fused_vs_separate(w, bounded, inp=None):
+    """moe_gmm1_swiglu against moe_gmm1 then moe_swiglu_quant on w's inputs (or the
+    given ones), bit for bit, on two calls in a row."""
+    if inp is None:
+        inp = synth.make_inputs(w)
+    rs = oracle.route_sort(inp["expert_idx"], w.E)
+    xq, pts1 = oracle.quant_tokens(inp["x"])
     d = _dims(w, 1)
     a1 = dev(_a1(xq, rs, w.topK, w.R))
     cs, srt, ei = dev(rs["cumsum"]), dev(rs["sorted_src_route"]), dev(inp["expert_idx"])
@@ -403,6 +408,25 @@ def test_gmm1_swiglu_matches_the_separate_kernels(w, bounded):
         got = run(True)
         for n, g, r in zip(["c1", "q2", "pts2", "q2 bounds"], got, ref):
             assert_bits_equal(g, r, "%s (%s, call %d)" % (n, w.name, call))
+
+
+@pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
+@pytest.mark.parametrize("w", FUSED_CASES, ids=[w.name for w in FUSED_CASES])
+def test_gmm1_swiglu_matches_the_separate_kernels(w, bounded):
+    """moe_gmm1_swiglu (SwiGLU fused into the tcgen05 GMM1 where it applies) writes the
+    same c1, q2, pts2 and q2 bounds as moe_gmm1 followed by moe_swiglu_quant, bit for
+    bit, on two calls in a row."""
+    _fused_vs_separate(w, bounded)
+
+
+def test_gmm1_swiglu_no_expert_on_the_pairs():
+    """28 routes per expert, none above 32: the warp-MMA engine serves every expert,
+    the pairs launch with no work item and their drain warps requantise every row
+    (each expert complete from the start)."""
+    w = synth.Workload("f_none_on_pairs", 56, 256, 320, 2, 1, "uniform", 90)
+    inp = synth.make_inputs(w)
+    inp["expert_idx"] = (np.arange(w.M, dtype=np.int32) % w.E).reshape(w.M, 1)
+    _fused_vs_separate(w, True, inp)
 
 
 @pytest.mark.parametrize("E,N,D", [(3, 128, 128), (2, 384, 192), (2, 256, 64), (1, 128, 1408), (2, 128, 7168),
