@@ -235,10 +235,11 @@ __global__ void __launch_bounds__(kSortThreads) route_scatter_kernel(
 constexpr int kSingleBlockMaxRoutes = kSortThreads * kMaxGroups;
 
 // Routes per block of the multi-block path: one pass of kSortThreads while that
-// needs at most max_blocks blocks, more passes per block beyond.
+// needs at most max_blocks blocks, more passes per block beyond (up to kMaxGroups),
+// and more blocks only past max_blocks * kSingleBlockMaxRoutes routes.
 int sort_chunk(int R, int max_blocks) {
   const int passes = (R + kSortThreads * max_blocks - 1) / (kSortThreads * max_blocks);
-  return kSortThreads * (passes < 1 ? 1 : passes);
+  return kSortThreads * (passes < 1 ? 1 : passes > kMaxGroups ? kMaxGroups : passes);
 }
 
 }  // namespace
@@ -270,7 +271,6 @@ cudaError_t launch_route_sort(const int32_t* expert_idx, int R, int E, int32_t* 
     return cudaGetLastError();
   }
   const int chunk = sort_chunk(R, max_blocks);
-  if (chunk > kSingleBlockMaxRoutes) return cudaErrorInvalidValue;  // R >= 2^24 or too few blocks
   const int nb = (R + chunk - 1) / chunk;
   int32_t* block_hist = static_cast<int32_t*>(workspace);
   int32_t* block_off = block_hist + (size_t)nb * (E + 1);

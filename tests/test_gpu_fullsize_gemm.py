@@ -13,7 +13,10 @@ isolates each GEMM:
   - SwiGLU's codes on those rows are within 1 LSB on at most 0.1% of elements of
     the oracle's, its scales within 1e-6 relative;
   - GMM2, given the same int8 codes on both sides, equals the oracle bit for bit
-    on the same rows.
+    on the same rows;
+  - above 24 rows per expert (skewed, prefill), the fused GMM1 + SwiGLU stage the
+    layer runs there writes the same c1, q2, pts2 and q2 bounds as the two kernels,
+    bit for bit, on every row.
 The reference rows are evaluated one at a time by the oracle (its GEMM over a
 list of expanded rows), so the CPU cost stays bounded at full size.
 """
@@ -151,6 +154,22 @@ def test_gemm_stages_bit_exact_at_full_size(cfg):
     np.testing.assert_allclose(pts2_h[rows], ref_pts2, rtol=1e-6)
     if use_bounds:
         assert_bits_equal(host(b2_gpu), segment_bounds(q2_h, cumsum, E, I), "q2 activation bounds")
+
+    if use_bounds:
+        # the layer's path above 24 rows per expert: SwiGLU inside the pairs' GMM1
+        # kernel; the same bits as the two kernels above, on every row
+        c1f = torch.full_like(c1, float("nan"))
+        q2f = torch.full_like(q2_f16, float("nan"))
+        pts2f = torch.full_like(pts2, float("nan"))
+        b2f = torch.zeros_like(b2_gpu)
+        moe.moe_gmm1_swiglu(d, dev(a1.astype(np.float16)), cs_dev, dev(b1), w_t["w1"], s1, c1f, dev(pts1),
+                            sorted_dev, ei_dev, q2f, pts2f, b2f, gws)
+        assert moe.moe_workspace_status(gws) == 0
+        Rv = int(cumsum[-1])
+        assert_bits_equal(host(c1f)[:Rv], c1_h[:Rv], "%s fused c1" % cfg)
+        assert_bits_equal(host(q2f)[:Rv], host(q2_f16)[:Rv], "%s fused q2" % cfg)
+        assert_bits_equal(host(pts2f)[:Rv], pts2_h[:Rv], "%s fused pts2" % cfg)
+        assert_bits_equal(host(b2f), host(b2_gpu), "%s fused q2 bounds" % cfg)
 
     # GMM2 on the same int8 codes on both sides (the GPU's q2)
     c2 = empty((R, K), torch.float16)

@@ -69,6 +69,8 @@ SORT_CASES = [
     ("E1", synth.Workload("E1", 100, 128, 64, 1, 1, "uniform", 23)),
     ("E1023", synth.Workload("E1023", 3000, 128, 64, 1023, 8, "zipf", 24)),
     ("bigR", synth.Workload("bigR", 20000, 128, 64, 300, 5, "biased", 25)),
+    # past 64 blocks of 8192 routes: blocks of 8192, as many as it takes
+    ("R600k", synth.Workload("R600k", 75000, 128, 64, 1023, 8, "uniform", 26)),
 ]
 
 
