@@ -579,10 +579,16 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 // GATHER: token rows gathered by index (args.gather_route) instead of tiled boxes of
 // expert-major rows; a separate instantiation, so the tiled kernel carries none of it.
-template <bool GATHER>
+// FUSE: kFuseNone, or kFuseSwiglu (GMM1 with SwiGLU: args.sw_*), each its own
+// instantiation, so the plain kernel's drains carry none of the SwiGLU state (its
+// register spills went from 28 to 4 bytes).
+enum { kFuseNone = 0, kFuseSwiglu = 1 };
+template <bool GATHER, int FUSE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                              const Args args) {
+  constexpr bool kSw = FUSE == kFuseSwiglu;
+  static_assert(!(GATHER && FUSE != kFuseNone), "fusion runs on the tiled operand");
   constexpr int S = kStages, SW = kWStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t wfull_bar[SW], wempty_bar[SW], xfull_bar[S], ready_bar[S], sdone_bar[S];
@@ -602,7 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int E = args.E, n_cb = (args.N + kPairCh - 1) / kPairCh;
   const int nk = (args.Kd + kBK - 1) / kBK;  // k-blocks; a 64-deep tail reads TMA zero fill
   const int nst = (nk + kKBlocks - 1) / kKBlocks;  // pipeline stages per work item
-  const bool inl = args.sw_q2 != nullptr;           // short tiles inline (fused SwiGLU)
+  constexpr bool inl = kSw;                         // short tiles inline (fused SwiGLU)
   PROF_T0(t_start);
   PROF_REGS;
   volatile int* abort_flag = &s_abort;
@@ -1071,7 +1077,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       PROF_ADD(2, t_epi);
-      if (args.sw_q2) {
+      if (kSw) {
         // count this item on its expert once the warp's stores are visible GPU-wide, then
         // requantise own rows of complete experts while the next chunk is not ready
         __syncwarp();
@@ -1087,7 +1093,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (args.sw_q2 && ok) {
+    if (kSw && ok) {
       // the rest of this warp's rows, each once its expert is complete (bounded wait)
       while (sw_row < sw_valid) {
         while (s_end[sw_e] <= sw_row) ++sw_e;
@@ -1122,7 +1128,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool GATHER>
+template <bool GATHER, int FUSE>
 cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   CUtensorMap tw, tx;
   if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kBK,
@@ -1139,10 +1145,10 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
     // the CTA is launched with; a build that launches with another count would
     // leave the drains' increase waiting forever, so it is refused here.
     cudaFuncAttributes fa;
-    cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_pair_kernel<GATHER>);
+    cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_pair_kernel<GATHER, FUSE>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<GATHER, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemBytes);
     if (err != cudaSuccess) return err;
     checked.done(dev);
@@ -1167,15 +1173,15 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.sw_pts2 = p.sw_pts2;
   a.sw_bounds = p.sw_bounds;
   a.sw_done = p.sw_done;
-  if (a.sw_q2 && (GATHER || p.N / 2 > kFusedSwigluMaxI || p.topK < 1 || !a.sw_pts1 || !a.sw_sorted || !a.sw_pts2 ||
-                  !a.sw_done))
+  if (FUSE == kFuseSwiglu && (p.N / 2 > kFusedSwigluMaxI || p.topK < 1 || !a.sw_q2 || !a.sw_pts1 || !a.sw_sorted ||
+                               !a.sw_pts2 || !a.sw_done))
     return cudaErrorInvalidValue;  // the fused SwiGLU runs on a tiled GMM1
 #ifdef MOE_GEMM_PROFILE
   a.prof = g_gemm_prof;
   if (!a.prof) return cudaErrorInvalidValue;
 #endif
   const int grid = sm_count() & ~1;  // whole pairs, one CTA per SM
-  grouped_gemm_pair_kernel<GATHER><<<grid, kThreads, kSmemBytes, stream>>>(tw, tx, a);
+  grouped_gemm_pair_kernel<GATHER, FUSE><<<grid, kThreads, kSmemBytes, stream>>>(tw, tx, a);
   return cudaGetLastError();
 }
 
@@ -1190,7 +1196,7 @@ bool pair_grid_coresident() {
   if (queried.needed(dev)) {
     // the kernel's attributes (dynamic shared memory) are set by its first launch; set
     // them here too so the query sees the launch's configuration
-    if (cudaFuncSetAttribute(grouped_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(grouped_gemm_pair_kernel<false, kFuseSwiglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return false;
     cudaLaunchConfig_t cfg = {};
@@ -1198,7 +1204,7 @@ bool pair_grid_coresident() {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<false>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<false, kFuseSwiglu>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       clusters = 0;
     }
@@ -1209,7 +1215,11 @@ bool pair_grid_coresident() {
 }
 
 cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream) {
-  return p.gather_route ? launch_pair<true>(p, stream) : launch_pair<false>(p, stream);
+  if (p.gather_route) {
+    if (p.sw_q2) return cudaErrorInvalidValue;  // the fused SwiGLU runs on the tiled operand
+    return launch_pair<true, kFuseNone>(p, stream);
+  }
+  return p.sw_q2 ? launch_pair<false, kFuseSwiglu>(p, stream) : launch_pair<false, kFuseNone>(p, stream);
 }
 
 }  // namespace moe
