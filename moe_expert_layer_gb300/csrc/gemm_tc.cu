@@ -111,7 +111,7 @@ constexpr int kWProducerWarp = 0, kMmaWarp = 1, kXProducerWarp = 2, kRelayWarp =
               kNumConvWarps = 4, kDrainWarp0 = 8, kNumDrainWarps = 16;
 static_assert(kThreads == 32 * (kDrainWarp0 + kNumDrainWarps), "warp roles");
 static_assert(kDrainWarp0 % 4 == 0 && kNumDrainWarps % 4 == 0, "drain warps: whole sets of the 4 SM sub-partitions");
-static_assert(kSmemBytes + 13 * 1024 <= 227 * 1024, "shared memory (dynamic + ~12.4 KB static)");
+static_assert(kSmemBytes + 15 * 1024 <= 227 * 1024, "shared memory (dynamic + ~14.3 KB static)");
 static_assert(kACol0 + kStages * kACols == kTmemCols, "tensor memory: accumulator + A buffers");
 // kind::f16 instruction descriptor: D f32, A/B f16, both K-major, M = 256; N is set per item
 constexpr uint32_t kIdescBase = (1u << 4) | ((uint32_t)(256 >> 4) << 24);
@@ -457,87 +457,76 @@ __device__ __forceinline__ int chunk_stages(const int32_t* bounds, int e, int nk
 }
 
 // Work items on the pairs: (expert, channel block, row tile), for the experts with
-// more than split_rows rows (the warp-MMA engine takes the others).  They run in
-// three stretches, each expert-major, then channel block, then row tile: first the
-// tiles that take N = 256 (an expert's whole 256-row tiles, and a last tile of more
-// than 128 rows), then the experts whose last tile takes N = 128 (65-128 rows), then
-// those whose last tile takes N = 64.  Dealt round-robin over the pairs, this gives
-// every pair a similar mix of long and short items: in plain expert-major order the
-// busiest pair had up to 11% more MMA time than the mean under skewed routing.  In
-// the first stretch pairs working at the same time still share weight blocks
-// through L2.
-//
-// With SwiGLU fused (inl), an expert's short last tile instead runs right after its
-// other tiles, in the first stretch (MMA N by the rows it holds): the rows' SwiGLU
-// needs all of the expert's tiles, and in three stretches every expert with a short
-// tile would complete only at the very end.
-__device__ __forceinline__ int full_tiles(int cnt, int split_rows, bool inl) {
-  if (cnt <= split_rows) return 0;
-  if (inl) return (cnt + kTileRows - 1) / kTileRows;
-  return cnt / kTileRows + (cnt % kTileRows > kTileRows / 2 ? 1 : 0);
-}
-// the kind of the expert's short last tile: 1 for N = 128, 2 for N = 64, 0 for none
-__device__ __forceinline__ int short_tile(int cnt, int split_rows, bool inl) {
-  const int r = cnt % kTileRows;
-  if (inl || cnt <= split_rows || r == 0 || r > kTileRows / 2) return 0;
-  return r > kTileRows / 4 ? 1 : 2;
+// more than split_rows rows (the warp-MMA engine takes the others), expert-major,
+// then channel block, then row tile, so that pairs working at the same time share
+// each weight block through L2 and experts complete in order (the fused SwiGLU
+// needs all of an expert's tiles).  An expert of cnt rows is cut into
+// t = ceil(cnt / 256) row tiles of two sizes that are multiples of 32 rows, a and
+// a + 32 (the larger ones first, as few as cover cnt), each run with MMA N = its rows
+// rounded up to 32.  A tcgen05.mma costs about the same for any N up to 128 and grows
+// with N above (96 cycles at N = 192, 128 at 256), so 795 rows as 224 + 192 + 192 +
+// 187 take ~16% less tensor time than 256 + 256 + 256 + 27 (whose short tile costs
+// nearly a full one); over the prefill and skewed routings, 6-7% less.
+__device__ __forceinline__ int row_tiles(int cnt, int split_rows) {
+  return cnt <= split_rows ? 0 : (cnt + kTileRows - 1) / kTileRows;
 }
 
 // Items of an expert with cnt rows on the pairs (all channel blocks).
-__device__ __forceinline__ int expert_items(int cnt, int split_rows, int n_cb, bool inl) {
-  return n_cb * (full_tiles(cnt, split_rows, inl) + (short_tile(cnt, split_rows, inl) ? 1 : 0));
+__device__ __forceinline__ int expert_items(int cnt, int split_rows, int n_cb) {
+  return n_cb * row_tiles(cnt, split_rows);
 }
 
 struct WorkList {
-  const int* pref;      // first N = 256 item of each expert; pref[E] = their number
-  const int* end;       // cumsum
-  const short* shorts;  // experts with a short last tile: the N = 128 ones, then the N = 64 ones
-  int n_full, n128, n_cb, E;
-  bool inl;             // short tiles inline in the first stretch (fused SwiGLU)
+  const int* pref;  // first work item of each expert; pref[E] = their number
+  const int* end;   // cumsum
+  const int* tile;  // row tiles of each expert: a | k << 16 (k tiles of a + 32 rows, then a rows)
+  int n_cb, E;
+  bool pow2_n;      // MMA N a power of two (the gathering token producer deals 4-row groups
+                    // of a half tile over the 32 lanes, which needs N / 8 to divide 32)
 };
 
-// Work item j -> (expert, channel block, first row, rows, MMA N).  In the first
-// stretch, the last expert whose first item is <= j (experts without N = 256 tiles
-// leave the prefix flat and are skipped).  A role's items only move forward, so the
-// search starts at its previous item's expert (e_hint): the next four prefixes are
-// read at once, and a binary search covers longer jumps.
+// The row tiling of an expert with cnt rows: t = row_tiles(cnt) tiles, a = 32 *
+// floor(cnt / (32 t)) rows each, the first k of them 32 rows more (k < t unless a
+// tile of a rows would leave rows out; the last tile holds what is left).
+__device__ __forceinline__ int tile_plan(int cnt, int t) {
+  if (t == 0) return 0;
+  const int a = 32 * (cnt / (32 * t));
+  const int k = (cnt - t * a + 31) / 32;
+  return a | (k << 16);
+}
+
+// Work item j -> (expert, channel block, first row, rows, MMA N): the last expert
+// whose first item is <= j (experts without items leave the prefix flat and are
+// skipped).  A role's items only move forward, so the search starts at its previous
+// item's expert (e_hint): the next four prefixes are read at once, and a binary
+// search covers longer jumps.
 __device__ __forceinline__ Item decode_item(int j, const WorkList& wl, int& e_hint) {
   Item it;
-  if (j < wl.n_full) {
-    int lo = e_hint, c = 0;
+  int lo = e_hint, c = 0;
 #pragma unroll
-    for (int step = 1; step <= 4; ++step) c += wl.pref[min(lo + step, wl.E)] <= j ? 1 : 0;  // pref[E] > j
-    lo += c;
-    if (c == 4) {
-      int hi = wl.E;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (wl.pref[mid] <= j) lo = mid; else hi = mid;
-      }
+  for (int step = 1; step <= 4; ++step) c += wl.pref[min(lo + step, wl.E)] <= j ? 1 : 0;  // pref[E] > j
+  lo += c;
+  if (c == 4) {
+    int hi = wl.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (wl.pref[mid] <= j) lo = mid; else hi = mid;
     }
-    e_hint = lo;
-    const int start = lo ? wl.end[lo - 1] : 0;
-    const int cnt = wl.end[lo] - start;
-    const int n_rt = full_tiles(cnt, -1, wl.inl);
-    const int local = j - wl.pref[lo];
-    const int cb = local / n_rt, rt = local - cb * n_rt;
-    it.e = lo;
-    it.cb = cb;
-    it.row0 = start + rt * kTileRows;
-    it.rows = min(kTileRows, cnt - rt * kTileRows);
-    it.n_mma = !wl.inl || it.rows > kTileRows / 2 ? kTileRows : (it.rows > kTileRows / 4 ? kTileRows / 2 : kTileRows / 4);
-  } else {
-    const int k = j - wl.n_full, idx = k / wl.n_cb;
-    const int e = wl.shorts[idx];
-    const int start = e ? wl.end[e - 1] : 0;
-    const int cnt = wl.end[e] - start;
-    const int nfull = cnt / kTileRows;
-    it.e = e;
-    it.cb = k - idx * wl.n_cb;
-    it.row0 = start + nfull * kTileRows;
-    it.rows = cnt - nfull * kTileRows;
-    it.n_mma = idx < wl.n128 ? kTileRows / 2 : kTileRows / 4;
   }
+  e_hint = lo;
+  const int start = lo ? wl.end[lo - 1] : 0;
+  const int cnt = wl.end[lo] - start;
+  const int n_rt = row_tiles(cnt, -1);
+  const int a = wl.tile[lo] & 0xffff, k = wl.tile[lo] >> 16;
+  const int local = j - wl.pref[lo];
+  const int cb = local / n_rt, rt = local - cb * n_rt;
+  const int row = rt < k ? rt * (a + 32) : k * (a + 32) + (rt - k) * a;
+  it.e = lo;
+  it.cb = cb;
+  it.row0 = start + row;
+  it.rows = min(rt < k ? a + 32 : a, cnt - row);
+  it.n_mma = wl.pow2_n ? (it.rows <= 32 ? 32 : 1 << (32 - __clz(it.rows - 1)))  // 32, 64, 128 or 256
+                      : (it.rows + 31) & ~31;                                  // N in steps of 32
   return it;
 }
 
@@ -596,9 +585,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __shared__ int s_pref[kMaxExperts + 1];
   __shared__ int s_end[kMaxExperts];
   __shared__ short s_chunk[kMaxExperts];  // stages per exact chunk of each expert
-  __shared__ short s_short[kMaxExperts];  // experts with a short last tile (WorkList::shorts)
-  __shared__ int s_wsum[kThreads / 32], s_wsum2[kThreads / 32];
-  __shared__ int s_nshort;                // (N = 128 experts) | (N = 64 experts) << 16
+  __shared__ int s_tile[kMaxExperts];     // row tiling of each expert (WorkList::tile)
+  __shared__ int s_wsum[kThreads / 32];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_w_issued, s_x_issued;
 
@@ -608,7 +596,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int E = args.E, n_cb = (args.N + kPairCh - 1) / kPairCh;
   const int nk = (args.Kd + kBK - 1) / kBK;  // k-blocks; a 64-deep tail reads TMA zero fill
   const int nst = (nk + kKBlocks - 1) / kKBlocks;  // pipeline stages per work item
-  constexpr bool inl = kSw;                         // short tiles inline (fused SwiGLU)
   PROF_T0(t_start);
   PROF_REGS;
   volatile int* abort_flag = &s_abort;
@@ -617,29 +604,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   {
     const int per = (E + kThreads - 1) / kThreads;
     const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
-    int local = 0, local2 = 0;  // N = 256 items; short tiles packed (N = 128) | (N = 64) << 16
+    int local = 0;  // work items of this thread's experts
     for (int e = e0; e < e1; ++e) {
       const int hi = __ldg(args.cumsum + e), lo = e ? __ldg(args.cumsum + e - 1) : 0;
       s_end[e] = hi;
       s_chunk[e] = (short)chunk_stages(args.bounds, e, nk);
-      local += full_tiles(hi - lo, args.split_rows, inl) * n_cb;
-      const int st = short_tile(hi - lo, args.split_rows, inl);
-      local2 += st == 1 ? 1 : (st == 2 ? 1 << 16 : 0);
+      const int nt = row_tiles(hi - lo, args.split_rows);
+      s_tile[e] = tile_plan(hi - lo, nt);
+      local += nt * n_cb;
     }
-    int incl = local, incl2 = local2;
+    int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      const int n2 = __shfl_up_sync(0xffffffffu, incl2, o);
-      if (lane >= o) {
-        incl += n;
-        incl2 += n2;
-      }
+      if (lane >= o) incl += n;
     }
-    if (lane == 31) {
-      s_wsum[warp] = incl;
-      s_wsum2[warp] = incl2;
-    }
+    if (lane == 31) s_wsum[warp] = incl;
     if (threadIdx.x == 0) {
       s_abort = 0;
       s_w_issued = 0;
@@ -672,24 +652,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
     }
     __syncthreads();
-    int run = incl - local, run2 = incl2 - local2, tot2 = 0;
+    int run = incl - local;
     for (int w = 0; w < warp; ++w) run += s_wsum[w];
-    for (int w = 0; w < kThreads / 32; ++w) {
-      if (w < warp) run2 += s_wsum2[w];
-      tot2 += s_wsum2[w];
-    }
-    const int n128 = tot2 & 0xffff;
     for (int e = e0; e < e1; ++e) {
       s_pref[e] = run;
       const int lo = e ? s_end[e - 1] : 0;
-      run += full_tiles(s_end[e] - lo, args.split_rows, inl) * n_cb;
-      const int st = short_tile(s_end[e] - lo, args.split_rows, inl);
-      if (st == 1) s_short[run2 & 0xffff] = (short)e;
-      if (st == 2) s_short[n128 + (run2 >> 16)] = (short)e;
-      run2 += st == 1 ? 1 : (st == 2 ? 1 << 16 : 0);
+      run += row_tiles(s_end[e] - lo, args.split_rows) * n_cb;
     }
     if (e0 < E && e1 == E) s_pref[E] = run;
-    if (threadIdx.x == 0) s_nshort = tot2;
   }
   __syncthreads();
   cluster_sync_all();  // the peer's barriers and tensor memory are ready
@@ -698,13 +668,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   WorkList wl;
   wl.pref = s_pref;
   wl.end = s_end;
-  wl.shorts = s_short;
-  wl.n_full = s_pref[E];
-  wl.n128 = s_nshort & 0xffff;
+  wl.tile = s_tile;
   wl.n_cb = n_cb;
   wl.E = E;
-  wl.inl = inl;
-  const int total = wl.n_full + n_cb * ((s_nshort & 0xffff) + (s_nshort >> 16));
+  wl.pow2_n = GATHER;
+  const int total = s_pref[E];
   const uint32_t tmem = s_tmem;
 
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -1086,7 +1054,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         while (sw_row < sw_valid && !mbar_test(&accfull_bar, c & 1)) {
           while (s_end[sw_e] <= sw_row) ++sw_e;
           const int lo = sw_e ? s_end[sw_e - 1] : 0;
-          const int target = kSwigluCountPerItem * expert_items(s_end[sw_e] - lo, args.split_rows, n_cb, inl);
+          const int target = kSwigluCountPerItem * expert_items(s_end[sw_e] - lo, args.split_rows, n_cb);
           if (__shfl_sync(0xffffffffu, lane == 0 ? ld_acquire(args.sw_done + sw_e) : 0, 0) < target) break;
           swiglu_row_warp(args, sw_row, sw_e, lane);
           sw_row += sw_stride;
@@ -1098,7 +1066,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       while (sw_row < sw_valid) {
         while (s_end[sw_e] <= sw_row) ++sw_e;
         const int lo = sw_e ? s_end[sw_e - 1] : 0;
-        const int target = kSwigluCountPerItem * expert_items(s_end[sw_e] - lo, args.split_rows, n_cb, inl);
+        const int target = kSwigluCountPerItem * expert_items(s_end[sw_e] - lo, args.split_rows, n_cb);
         const int done = lane == 0 ? (count_wait_bounded(args.sw_done + sw_e, target) ? 1 : 0) : 0;
         if (!__shfl_sync(0xffffffffu, done, 0)) {
           *abort_flag = 1;

@@ -8,8 +8,9 @@ rest).  The stages are fed the oracle's own quantised tokens, so the comparison
 isolates each GEMM:
 
   - GMM1's binary16 outputs equal the oracle's bit for bit on: a middle row of
-    every active expert, the first and last row of every work tile (256-row pair
-    tiles, 16/32-row warp-MMA tiles), and every row of the most loaded expert;
+    every active expert, the first and last row of every work tile (the pairs'
+    balanced row tiles of up to 256 rows, 16/32-row warp-MMA tiles), and every row
+    of the most loaded expert;
   - SwiGLU's codes on those rows are within 1 LSB on at most 0.1% of elements of
     the oracle's, its scales within 1e-6 relative;
   - GMM2, given the same int8 codes on both sides, equals the oracle bit for bit
@@ -37,12 +38,28 @@ SPLIT_ROWS = 32    # experts with at most this many rows run on the warp-MMA eng
 PAIR_ROWS = 256    # token rows per tcgen05 pair tile
 
 
+def pair_row_tiles(cnt):
+    """Row tiles of an expert on the tcgen05 pairs: t = ceil(cnt / 256) tiles of
+    a = 32 * floor(cnt / (32 t)) rows, the first k of them a + 32 rows (k the fewest
+    that cover cnt), the last holding what is left; (first, rows) each."""
+    t = (cnt + PAIR_ROWS - 1) // PAIR_ROWS
+    a = 32 * (cnt // (32 * t))
+    k = (cnt - t * a + 31) // 32
+    out, row = [], 0
+    for rt in range(t):
+        n = min(a + 32 if rt < k else a, cnt - row)
+        out.append((row, n))
+        row += n
+    assert row == cnt and all(0 < n <= PAIR_ROWS for _, n in out)
+    return out
+
+
 def work_tiles(cumsum, R, E):
     """(first row, last row) of every work tile of the grouped GEMM, as the engines
     cut them: everything on warp-MMA tiles of 16 (up to 8 rows per expert on
     average) or 32 rows up to 24 rows per expert; above, experts of at most 32 rows
-    on 32-row warp-MMA tiles and the others on 256-row pair tiles (a last tile of
-    at most 128 rows is a short tile of its own)."""
+    on 32-row warp-MMA tiles (all experts on the pairs from 256 rows per expert on
+    average) and the others on the pairs' balanced row tiles."""
     mean = R / E
     tiles = []
     lo = 0
@@ -52,10 +69,11 @@ def work_tiles(cumsum, R, E):
         if cnt:
             if mean <= 24.0:
                 step = 16 if mean <= 8.0 else 32
+                tiles += [(t0, min(hi, t0 + step) - 1) for t0 in range(lo, hi, step)]
+            elif cnt <= SPLIT_ROWS and mean < 256.0:
+                tiles += [(lo, hi - 1)]
             else:
-                step = 32 if cnt <= SPLIT_ROWS else PAIR_ROWS
-            for t0 in range(lo, hi, step):
-                tiles.append((t0, min(hi, t0 + step) - 1))
+                tiles += [(lo + r0, lo + r0 + n - 1) for r0, n in pair_row_tiles(cnt)]
         lo = hi
     return tiles
 
