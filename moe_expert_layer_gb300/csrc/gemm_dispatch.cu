@@ -20,7 +20,7 @@ namespace moe {
 constexpr int kSplitRows = 32;
 
 // Above kPairsOnlyRows rows per expert on average (prefill-sized batches) the pairs
-// take every expert, small ones on their N = 64 / 128 tiles: an expert of at most
+// take every expert, small ones as single short tiles (small MMA N): an expert of at most
 // kSplitRows rows is then rare, while the warp-MMA kernel's launch, work-list set-up
 // and exit (~4 us per GEMM at M = 8192, E = 64, measured) would be paid on every call.
 constexpr double kPairsOnlyRows = 256.0;

@@ -27,8 +27,8 @@
 // stage (16 MMAs): each CTA contributes 128 weight channels (operand A, in its own
 // tensor memory) and half of the N token rows (operand B, in its own shared
 // memory), and receives the 128 x N block of its channels in its tensor memory.
-// A work item is (expert, 256-channel block, 256-row tile); N is 64, 128 or 256
-// by the rows the tile holds.
+// A work item is (expert, 256-channel block, row tile of up to 256 rows); N is the
+// tile's rows rounded up to 32 (the experts' rows are cut into balanced tiles).
 //   - Weights stay int8 in HBM (they are the dominant traffic at small batches).
 //     They arrive in k-blocks: a TMA box (or one 16 KiB tile) of 128 channels x
 //     128 k in shared memory (128-byte swizzle), two per stage; converter warps read

@@ -267,10 +267,10 @@ GEMM_CASES = [
     synth.Workload("g_dec", 60, 512, 128, 16, 2, "uniform", 59),            # warp-MMA engine, 16-row tiles
     synth.Workload("g_small", 40, 256, 128, 8, 2, "uniform", 51),           # warp-MMA engine, 32-row tiles
     synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # warp-MMA engine, 32-row tiles, ragged
-    synth.Workload("g_mid_tc", 320, 512, 192, 16, 2, "biased", 57),         # tcgen05 pairs, N=64/128 tiles, 128-channel tail
+    synth.Workload("g_mid_tc", 320, 512, 192, 16, 2, "biased", 57),         # tcgen05 pairs, small N tiles, 128-channel tail
     synth.Workload("g_big", 384, 1024, 256, 4, 2, "zipf", 53),              # tcgen05 pairs, N=256 tiles, hot expert
     synth.Workload("g_kchunks", 64, 2560, 64, 2, 1, "uniform", 54),         # tcgen05 pairs, three 1024-deep chunks
-    synth.Workload("g_tiles", 700, 512, 192, 3, 2, "zipf", 55),             # 256-row tiles + tails, 64-deep tail
+    synth.Workload("g_tiles", 700, 512, 192, 3, 2, "zipf", 55),             # several balanced row tiles per expert, 64-deep tail
     synth.Workload("g_odd", 48, 384, 192, 8, 2, "uniform", 56),             # warp-MMA engine, 3 stages per item
     synth.Workload("g_hybrid", 400, 512, 192, 32, 2, "zipf", 58),           # both engines: small experts on warp MMA
 ]
@@ -330,7 +330,7 @@ def test_gmm2_bit_exact(w, bounded, layout):
 @pytest.mark.parametrize("bounded", [False, True], ids=["chunk1024", "bounds"])
 def test_gmm_pairs_only_with_small_experts(bounded):
     """Above 256 rows per expert on average the tcgen05 pairs take every expert, the
-    small ones (here 20, 10 and 0 rows beside 1200 and 70) on their short tiles."""
+    small ones (here 20, 10 and 0 rows beside 1200 and 70) as single small-N tiles."""
     w = synth.Workload("pairs_only", 1300, 512, 192, 5, 1, "uniform", 81)
     inp = synth.make_inputs(w)
     ei = np.zeros((w.M, 1), np.int32)
@@ -365,7 +365,7 @@ FUSED_CASES = [
     synth.Workload("f_prefill_i", 2048, 512, 1408, 8, 1, "uniform", 91),   # the prefill I, 6 vectors per lane
     synth.Workload("f_i64", 1024, 1024, 64, 2, 2, "biased", 92),           # a row half of one vector
     synth.Workload("f_i1536", 600, 256, 1536, 2, 1, "zipf", 93),            # the largest row held in registers
-    synth.Workload("f_tiles", 1800, 256, 320, 6, 1, "zipf", 94),            # short tiles, uneven experts
+    synth.Workload("f_tiles", 1800, 256, 320, 6, 1, "zipf", 94),            # uneven experts, small and balanced tiles
     synth.Workload("f_i2048", 600, 256, 2048, 2, 1, "uniform", 96),         # rows read twice, 1024 deep at a time
     synth.Workload("f_i2496", 512, 256, 2496, 2, 1, "biased", 99),          # ... with a partial last pass
     # both engines (25-255 routes per expert): experts of <= 32 rows on the warp-MMA
