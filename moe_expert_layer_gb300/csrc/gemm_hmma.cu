@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[S];
   __shared__ __align__(8) uint64_t empty_bar[S];
-  __shared__ __align__(8) uint64_t part_full_bar;  // partials hand-off to the epilogue group
+  __shared__ __align__(8) uint64_t part_full_bar;   // partials hand-off to the epilogue group
+  __shared__ __align__(8) uint64_t part_empty_bar;  // the epilogue group has read them
   __shared__ int s_pref[kMaxExperts + 1];  // first work item of each expert
   __shared__ int s_end[kMaxExperts];       // cumsum
   __shared__ int s_wsum[kConsumerWarps];
@@ -335,6 +336,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       mbar_init(&empty_bar[s], kGroupWarps);  // one group consumes each stage
     }
     mbar_init(&part_full_bar, kGroupWarps);
+    mbar_init(&part_empty_bar, kGroupWarps);
     s_abort = 0;
     s_issued = 0;
     fence_barrier_init();
@@ -506,14 +508,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       // partials over through shared memory (part_full) and moves on to the next
       // item; the epilogue group adds them, scales, converts, stages [T][128]
       // binary16 and stores it coalesced.
-      // The groups take turns (item n: group n % 2), so that one item's epilogue
-      // overlaps the other group's MMAs of the next.  Each warp owns one slice of the
-      // partials buffer, and the sender of item n is the group that read item n-1's
-      // partials, so a warp rewrites its slice only after it has read it; item n's
-      // epilogue ends (its staging-tile reads included) before the same group sends
-      // item n+1's partials, so the two groups' epilogues never overlap.
-      const int epi_grp = n_items & 1;
+      // The epilogue group is the one that computes the item's last stage: the other
+      // group's partials are then ready when it gets there, so neither group idles
+      // at the hand-off (with the groups taking turns instead, every other item's
+      // epilogue group waited a stage for the other's partials while its next
+      // stages, and behind them the in-order producer, stalled: mid GMM2 745 -> 725 us).
+      // Each warp owns one slice of the partials buffer; a sender rewrites its slice
+      // only after the epilogue group has read the previous item's (part_empty).
+      // Item n's epilogue ends (its staging-tile reads included) before the next
+      // epilogue starts: with an even stage count per item the same group runs every
+      // epilogue, with an odd one the groups alternate and the sender of item n + 1
+      // is item n's epilogue group, which sends only after that epilogue.
+      const int epi_grp = ((n_items * nk + nk - 1) % S) % kGroups;
       if (grp != epi_grp) {
+        if (n_items > 0) {
+          bool free = lane == 0 ? wait_part(&part_empty_bar, (n_items - 1) & 1, args.status) : true;
+          free = __shfl_sync(0xffffffffu, free ? 1 : 0, 0) != 0;
+          ok = ok && free;
+        }
         if (ok) {
 #pragma unroll
           for (int mt = 0; mt < Cfg::MT; ++mt)
@@ -540,6 +552,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 sum += got ? spart_base[(q - 1) * kGroupWarps * kPartWarp + ((mt * Cfg::NT + nt) * 4 + i) * 32] : 0;
               v[mt][nt][i] = sum;
             }
+        __syncwarp();  // the slice is read (the sums above use every loaded value)
+        if (lane == 0) mbar_arrive(&part_empty_bar);
         ok = ok && got;
         epilogue_bar();  // the previous epilogue's staging-tile reads are done
         if (ok) {
