@@ -211,6 +211,8 @@ int32_t moe_layer_fwd_host(const moe_dims_t* d, const uint16_t* x_host,
  *     failed.
  *   moe_layer_pipeline_destroy: waits for every batch in flight, then releases the
  *     pipeline (NULL is a no-op).
+ * A pipeline's calls must come from one host thread at a time (it keeps its ticket
+ * counters without locks); separate pipelines are independent.
  */
 typedef struct moe_layer_pipeline moe_layer_pipeline_t;
 size_t moe_layer_pipeline_workspace_size(const moe_dims_t* d, int32_t depth);
