@@ -128,29 +128,51 @@ __global__ void __launch_bounds__(kRowThreads) quant_tokens_kernel(const __half*
   }
   if constexpr (SORT) {
     // the row loads above are in flight while the routes are counted
-    __shared__ int s_cnt[1024], s_before[1024], s_ws[32];
+    __shared__ int s_after[1024], s_before[1024], s_ws[32];
     const int nb = E + 1;
     for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-      s_cnt[b] = 0;
+      s_after[b] = 0;
       s_before[b] = 0;
     }
     __syncthreads();
+    // each route counted once, in its bucket's count before or from this token's
+    // routes; the ids come in 16-byte loads, several per thread in flight at once
     const int first = t * topK;
-    for (int r = threadIdx.x; r < R; r += blockDim.x) {
-      const int e = __ldg(expert_idx + r);
+    auto count = [&](int r, int e) {
       const int b = (e >= 0 && e < E) ? e : E;
-      atomicAdd(&s_cnt[b], 1);
-      if (r < first) atomicAdd(&s_before[b], 1);
+      atomicAdd(r < first ? &s_before[b] : &s_after[b], 1);
+    };
+    const int nq = R >> 2;  // whole groups of four routes
+    const int4* ids4 = reinterpret_cast<const int4*>(expert_idx);
+    constexpr int kBatch = 4;
+    for (int q0 = threadIdx.x; q0 < nq; q0 += kBatch * (int)blockDim.x) {
+      int4 v4[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int q = q0 + u * (int)blockDim.x;
+        if (q < nq) v4[u] = __ldg(ids4 + q);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int q = q0 + u * (int)blockDim.x;
+        if (q < nq) {
+          count(4 * q, v4[u].x);
+          count(4 * q + 1, v4[u].y);
+          count(4 * q + 2, v4[u].z);
+          count(4 * q + 3, v4[u].w);
+        }
+      }
     }
+    for (int r = 4 * nq + threadIdx.x; r < R; r += blockDim.x) count(r, __ldg(expert_idx + r));
     __syncthreads();
     // exclusive scan of the bucket counts: thread i owns buckets [i*per, i*per + per)
     const int per = (nb + blockDim.x - 1) / blockDim.x;
     const int b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
     int local = 0;
-    for (int b = b0; b < b1; ++b) local += s_cnt[b];
+    for (int b = b0; b < b1; ++b) local += s_before[b] + s_after[b];
     int run = block_scan_excl(local, s_ws);
     for (int b = b0; b < b1; ++b) {
-      const int c = s_cnt[b];
+      const int c = s_before[b] + s_after[b];
       if (t == 0 && b < E) {
         tokens_per_expert[b] = c;
         cumsum[b] = run + c;
