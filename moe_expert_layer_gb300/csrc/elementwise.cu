@@ -504,9 +504,10 @@ cudaError_t launch_swiglu_quant(const uint16_t* c1, int R, int I, int E, int top
   // a block-wide max and the stores, so throughput comes from rows in flight: short
   // rows per thread-block (64 threads, up to 4 vectors each) once there are rows
   // enough to fill the GPU (I = 1408: 97 us instead of 115 at 49152 rows), 128
-  // threads below that (1024 rows: 64-thread blocks were 24% slower).
+  // threads below 8192 rows (1024 rows: 64-thread blocks were 24% slower; 4096 rows
+  // of I = 2048: 17.3 us with 128 threads, 19.2 with 64 or 256).
   const int nvec = I / 8;
-  const int row_cap = R >= 4096 ? 64 : 128;
+  const int row_cap = R >= 8192 ? 64 : 128;
   const int vpt = min(8, (nvec + row_cap - 1) / row_cap);  // I <= 8192: at most 128 threads
   const int threads = row_threads(nvec, vpt);
   const __half* ch = reinterpret_cast<const __half*>(c1);
