@@ -29,12 +29,35 @@ constexpr double kPairsOnlyRows = 256.0;
 // chunks and reads no activation bounds.
 bool grouped_gemm_reads_bounds(int R, int E) { return (double)R / (double)E > 24.0; }
 
+// The warp-MMA engine's share of experts with more than lo and at most hi rows: 16-row
+// tiles for the experts of up to 16 rows, 32-row tiles for the larger ones (one launch
+// each).  An expert of 9-16 rows streams its weights once either way, and the 16-row
+// tiles' kernel (a 16-row token box, four partial accumulators per fragment) runs its
+// stages faster; an expert of 17-32 rows would stream them twice on 16-row tiles.
+// Skewed routing (181 experts of <= 32 rows, 125 of them <= 16): GMM1 1609 -> 1591 us,
+// GMM2 889 -> 880 us against 32-row tiles for all.
+constexpr int kWarpTile16Rows = 16;
+cudaError_t launch_warp_share(const GroupedGemmProblem& p, int lo, int hi, cudaStream_t stream) {
+  GroupedGemmProblem q = p;
+  if (lo < kWarpTile16Rows) {
+    q.min_rows = lo;
+    q.split_rows = min(hi, kWarpTile16Rows);
+    cudaError_t e = launch_grouped_gemm_hmma(q, 16, stream);
+    if (e != cudaSuccess || hi <= kWarpTile16Rows) return e;
+  }
+  q.min_rows = max(lo, kWarpTile16Rows);
+  q.split_rows = hi;
+  return launch_grouped_gemm_hmma(q, 32, stream);
+}
+
 cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream) {
   GroupedGemmProblem q = p;
   const double mean_rows = (double)p.R / (double)p.E;
   if (!grouped_gemm_reads_bounds(p.R, p.E)) {
     // 16-row tiles up to 8 rows per expert on average (decode); 32-row tiles above,
     // so that an expert of up to 32 rows streams its weights through one work item
+    // (splitting off the experts of up to 16 rows onto 16-row tiles, as below, measured
+    // no gain at 16 rows per expert: GMM1 1297 -> 1296 us, GMM2 726 -> 733 us)
     q.split_rows = 0x7fffffff;
     return launch_grouped_gemm_hmma(q, mean_rows <= 8.0 ? 16 : 32, stream);
   }
@@ -42,9 +65,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmProblem& p, cudaStream_t stream
     q.split_rows = 0;
     return launch_grouped_gemm_tc(q, stream);
   }
-  q.split_rows = kSplitRows;
-  cudaError_t err = launch_grouped_gemm_hmma(q, 32, stream);
+  cudaError_t err = launch_warp_share(q, 0, kSplitRows, stream);
   if (err != cudaSuccess) return err;
+  q.split_rows = kSplitRows;
   return launch_grouped_gemm_tc(q, stream);
 }
 
@@ -61,7 +84,7 @@ cudaError_t launch_gemm1_swiglu(const GroupedGemmProblem& g1, int I, int topK, c
     if (mean_rows < kPairsOnlyRows) {
       // the small experts' GMM1 first: their rows are complete when the pairs start
       q.split_rows = kSplitRows;
-      cudaError_t e = launch_grouped_gemm_hmma(q, 32, stream);
+      cudaError_t e = launch_warp_share(q, 0, kSplitRows, stream);
       if (e != cudaSuccess) return e;
     }
     q.topK = topK;  // a row's token is its route / topK

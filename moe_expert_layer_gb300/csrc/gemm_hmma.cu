@@ -96,6 +96,7 @@ struct GemmArgs {
   int32_t* status;
   int E, N, Kd;
   int split_rows;  // this engine serves the experts with at most split_rows rows
+  int min_rows;    // ... and more than min_rows rows
   const int32_t* gather_route;  // null: tiled token boxes; else row d gathers token gather_route[d] / topK
   int topK;
   const uint8_t* w_tiles;  // null: weights through the tensor map; else the tile layout
@@ -234,8 +235,8 @@ struct Item {
 // take it).  Experts without items leave the prefix flat, and the binary search in
 // decode_item (last expert whose first item is <= j) skips them.
 template <int T>
-__device__ __forceinline__ int own_items(int cnt, int split_rows, int n_cb) {
-  return cnt <= split_rows ? (cnt + T - 1) / T * n_cb : 0;
+__device__ __forceinline__ int own_items(int cnt, int min_rows, int split_rows, int n_cb) {
+  return cnt > min_rows && cnt <= split_rows ? (cnt + T - 1) / T * n_cb : 0;
 }
 
 // Work item j -> (expert, channel block, first row, rows).  Items are ordered
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     for (int e = e0; e < e1; ++e) {
       const int hi = __ldg(args.cumsum + e), lo = e ? __ldg(args.cumsum + e - 1) : 0;
       s_end[e] = hi;
-      local += own_items<T>(hi - lo, args.split_rows, n_cb);
+      local += own_items<T>(hi - lo, args.min_rows, args.split_rows, n_cb);
     }
     int incl = local;
 #pragma unroll
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     for (int e = e0; e < e1; ++e) {
       s_pref[e] = run;
       const int lo = e ? s_end[e - 1] : 0;
-      run += own_items<T>(s_end[e] - lo, args.split_rows, n_cb);
+      run += own_items<T>(s_end[e] - lo, args.min_rows, args.split_rows, n_cb);
     }
     if (e0 < E && e1 == E) s_pref[E] = run;
   } else if (lane == 0) {
@@ -631,6 +632,7 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.N = p.N;
   a.Kd = p.Kd;
   a.split_rows = p.split_rows;
+  a.min_rows = p.min_rows;
   a.gather_route = p.gather_route;
   a.topK = p.topK;
   a.w_tiles = p.w_kb ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;

@@ -57,6 +57,7 @@ struct GroupedGemmProblem {
   int32_t* status;                  // device status word
   int split_rows;                   // experts with <= split_rows rows run on the warp-MMA engine,
                                     // the others on the tcgen05 pairs (set by launch_grouped_gemm)
+  int min_rows;                     // the warp-MMA engine skips experts of <= min_rows rows (0: none)
   const int32_t* bounds;            // [E][kBoundSegments] activation bounds, or null
   // GMM1 only, set by launch_gemm1_swiglu: SwiGLU + requant fused into the tcgen05 pairs
   const float* sw_pts1;             // [M] token scales (null: a plain GEMM)
