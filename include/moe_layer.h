@@ -78,8 +78,11 @@ typedef struct {
  *     is padded with zeros to a multiple of 256).  Tile (e, nb, kb) starts at byte
  *     ((e * NB + nb) * KB + kb) * 16384; inside it, W[e][nb*128 + r][kb*128 + c]
  *     (r, c in [0, 128)) sits at byte r * 128 + (((c / 16) ^ (r % 8)) * 16) + c % 16,
- *     and the bytes of reduction steps kb*128 + c >= D are zero.  This is the image
- *     a 128-byte-swizzled tensor copy of the 128 x 128 box leaves in shared memory.
+ *     stored in excess-128 form: the byte is W + 128 (W's two's-complement byte with
+ *     its top bit flipped), and the bytes of reduction steps kb*128 + c >= D hold
+ *     0x80, the code of 0.  This is the image a 128-byte-swizzled tensor copy of the
+ *     128 x 128 box leaves in shared memory, with the sign bits flipped so that the
+ *     GEMMs widen four weights to binary16 with one instruction less.
  */
 #define MOE_WEIGHTS_ROWS 0
 #define MOE_WEIGHTS_TILES 1

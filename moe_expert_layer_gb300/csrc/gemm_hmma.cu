@@ -105,9 +105,10 @@ struct GemmArgs {
 
 // 4 int8 (one 32-bit word) -> two half2 {b0,b1}, {b2,b3}, exactly.
 // Byte v+128 placed in the mantissa of 0x6400 (=1024) gives 1024+v+128;
-// subtracting 1152 leaves v.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
+// subtracting 1152 leaves v.  flip = 0x80808080 for two's-complement bytes
+// (v+128 = v ^ 0x80), 0 for bytes stored as v+128 (the weight tiles).
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t flip, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ flip;
   uint32_t a = __byte_perm(u, 0x6464u, 0x5140u);
   uint32_t b = __byte_perm(u, 0x6464u, 0x5342u);
   const uint32_t bias = 0x64806480u;  // half2(1152, 1152)
@@ -129,8 +130,9 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 // One 64-deep k-half of one stage for one warp: A fragments from the int8 weight tile
 // (widened in registers), B fragments from the binary16 row tile, NTL live n8 tiles.
 template <class Cfg, int NTL>
-__device__ __forceinline__ void hmma_half_stage(const uint8_t* xh, const uint8_t* ws, int half, int warp_m, int warp_n,
-                                                int g, int tq, int pg, float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
+__device__ __forceinline__ void hmma_half_stage(const uint8_t* xh, const uint8_t* ws, uint32_t wflip, int half,
+                                                int warp_m, int warp_n, int g, int tq, int pg,
+                                                float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
   // Plain shared-memory reads (ordered after the stage's barrier wait by its memory
   // clobber) let the compiler issue every load of the stage before the first MMA.
   auto lds = [](const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); };
@@ -154,8 +156,8 @@ __device__ __forceinline__ void hmma_half_stage(const uint8_t* xh, const uint8_t
 #pragma unroll
     for (int sl = 0; sl < 4; ++sl) {
       uint32_t a0, a2, a1, a3;
-      i8x4_to_f16x4(aw_lo[sl], a0, a2);  // row perm(g):   k 4sl,4sl+1 | 4sl+2,4sl+3
-      i8x4_to_f16x4(aw_hi[sl], a1, a3);  // row 8+perm(g)
+      i8x4_to_f16x4(aw_lo[sl], wflip, a0, a2);  // row perm(g):   k 4sl,4sl+1 | 4sl+2,4sl+3
+      i8x4_to_f16x4(aw_hi[sl], wflip, a1, a3);  // row 8+perm(g)
 #pragma unroll
       for (int nt = 0; nt < NTL; ++nt) {
         const uint4& bv = bfrag[nt][sl >> 1];
@@ -169,28 +171,28 @@ __device__ __forceinline__ void hmma_half_stage(const uint8_t* xh, const uint8_t
 
 // A whole stage (all 64-deep k quarters) with NTL live n8 tiles.
 template <class Cfg, int NTL>
-__device__ __forceinline__ void hmma_stage(const uint8_t* xs, const uint8_t* ws, int warp_m, int warp_n, int g, int tq,
-                                           int pg, float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
+__device__ __forceinline__ void hmma_stage(const uint8_t* xs, const uint8_t* ws, uint32_t wflip, int warp_m, int warp_n,
+                                           int g, int tq, int pg, float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
 #pragma unroll
   for (int q = 0; q < kQuarters; ++q)
-    hmma_half_stage<Cfg, NTL>(xs + q * Cfg::X_HALF_BYTES, ws + (q >> 1) * Cfg::W_SUB_BYTES, q & 1, warp_m, warp_n, g,
-                              tq, pg, accf);
+    hmma_half_stage<Cfg, NTL>(xs + q * Cfg::X_HALF_BYTES, ws + (q >> 1) * Cfg::W_SUB_BYTES, wflip, q & 1, warp_m,
+                              warp_n, g, tq, pg, accf);
 }
 
 // Dispatch on the live n8 tiles of the item (rows beyond the item's rows are
 // skipped, so the MMA work follows the real row count).
 template <class Cfg>
-__device__ __forceinline__ void hmma_stage_live(int live_nt, const uint8_t* xs, const uint8_t* ws, int warp_m,
-                                                int warp_n, int g, int tq, int pg,
+__device__ __forceinline__ void hmma_stage_live(int live_nt, const uint8_t* xs, const uint8_t* ws, uint32_t wflip,
+                                                int warp_m, int warp_n, int g, int tq, int pg,
                                                 float (&accf)[Cfg::P][Cfg::MT][Cfg::NT][4]) {
   if (Cfg::NT >= 4 && live_nt >= 4) {
-    hmma_stage<Cfg, (Cfg::NT >= 4 ? 4 : 1)>(xs, ws, warp_m, warp_n, g, tq, pg, accf);
+    hmma_stage<Cfg, (Cfg::NT >= 4 ? 4 : 1)>(xs, ws, wflip, warp_m, warp_n, g, tq, pg, accf);
   } else if (Cfg::NT >= 3 && live_nt == 3) {
-    hmma_stage<Cfg, (Cfg::NT >= 3 ? 3 : 1)>(xs, ws, warp_m, warp_n, g, tq, pg, accf);
+    hmma_stage<Cfg, (Cfg::NT >= 3 ? 3 : 1)>(xs, ws, wflip, warp_m, warp_n, g, tq, pg, accf);
   } else if (live_nt >= 2) {
-    hmma_stage<Cfg, 2>(xs, ws, warp_m, warp_n, g, tq, pg, accf);
+    hmma_stage<Cfg, 2>(xs, ws, wflip, warp_m, warp_n, g, tq, pg, accf);
   } else if (live_nt == 1) {
-    hmma_stage<Cfg, 1>(xs, ws, warp_m, warp_n, g, tq, pg, accf);
+    hmma_stage<Cfg, 1>(xs, ws, wflip, warp_m, warp_n, g, tq, pg, accf);
   }
 }
 
@@ -281,7 +283,7 @@ __device__ __forceinline__ Item decode_item(int j, const int* s_pref, const int*
 
 // GATHER: token rows gathered by index (args.gather_route) instead of tiled boxes of
 // expert-major rows; a separate instantiation, so the tiled kernel carries none of it.
-template <int T, bool GATHER>
+template <int T, bool GATHER, bool TILES>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                                                                        const __grid_constant__ CUtensorMap tm_x,
                                                                        const __grid_constant__ CUtensorMap tm_x8,
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         uint8_t* ws = xs + Cfg::X_BYTES;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full_bar[slot], tx);
-          if (args.w_tiles) {
+          if (TILES) {
             // the stage's two 128-deep tiles are adjacent: one contiguous copy
             const size_t t0 = ((size_t)it.e * n_cb + it.cb) * args.w_kb + 2 * kb;
             bulk_load(ws, args.w_tiles + t0 * (size_t)Cfg::W_SUB_BYTES, (uint32_t)Cfg::W_BYTES, &full_bar[slot]);
@@ -446,6 +448,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int warp_m = wig % Cfg::WARPS_M, warp_n = wig / Cfg::WARPS_M;
     const int g = lane >> 2, tq = lane & 3;
     const int pg = mrow_perm(g);
+    constexpr uint32_t wflip = TILES ? 0u : 0x80808080u;  // tile bytes hold v + 128
     __half* stile = reinterpret_cast<__half*>(smem_gen + S * Cfg::STAGE_BYTES);
     constexpr int kPartWarp = Cfg::MT * Cfg::NT * 4 * 32;  // ints per warp
     int* spart_base = reinterpret_cast<int*>(smem_gen + S * Cfg::STAGE_BYTES + Cfg::EPI_BYTES) + wig * kPartWarp + lane;
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           const uint8_t* xs = smem_gen + slot * Cfg::STAGE_BYTES;
           const uint8_t* ws = xs + Cfg::X_BYTES;
           // one uniform branch per stage on the number of live n8 tiles
-          hmma_stage_live<Cfg>(live_nt, xs, ws, warp_m, warp_n, g, tq, pg, accf);
+          hmma_stage_live<Cfg>(live_nt, xs, ws, wflip, warp_m, warp_n, g, tq, pg, accf);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty_bar[slot]);
           ++consumed;
@@ -599,7 +602,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 // ------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------
-template <int T, bool GATHER>
+template <int T, bool GATHER, bool TILES>
 cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   using Cfg = GemmCfg<T>;
   CUtensorMap tw, tx;
@@ -618,7 +621,7 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   static PerContextOnce attr_set;
   const int dev = current_device();
   if (attr_set.needed(dev)) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<T, GATHER>,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<T, GATHER, TILES>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     attr_set.done(dev);
@@ -635,9 +638,9 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.min_rows = p.min_rows;
   a.gather_route = p.gather_route;
   a.topK = p.topK;
-  a.w_tiles = p.w_kb ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;
+  a.w_tiles = TILES ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;
   a.w_kb = p.w_kb;
-  grouped_gemm_kernel<T, GATHER><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
+  grouped_gemm_kernel<T, GATHER, TILES><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
   return cudaGetLastError();
 }
 
@@ -645,8 +648,12 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
 
 cudaError_t launch_grouped_gemm_hmma(const GroupedGemmProblem& p, int T, cudaStream_t stream) {
   const bool g = p.gather_route != nullptr;
-  if (T == 32) return g ? launch_t<32, true>(p, stream) : launch_t<32, false>(p, stream);
-  return g ? launch_t<16, true>(p, stream) : launch_t<16, false>(p, stream);
+  if (p.w_kb) {
+    if (T == 32) return g ? launch_t<32, true, true>(p, stream) : launch_t<32, false, true>(p, stream);
+    return g ? launch_t<16, true, true>(p, stream) : launch_t<16, false, true>(p, stream);
+  }
+  if (T == 32) return g ? launch_t<32, true, false>(p, stream) : launch_t<32, false, false>(p, stream);
+  return g ? launch_t<16, true, false>(p, stream) : launch_t<16, false, false>(p, stream);
 }
 
 }  // namespace moe

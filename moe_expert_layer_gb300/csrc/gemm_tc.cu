@@ -406,9 +406,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 
 // 4 int8 (one 32-bit word) -> two half2 {b0,b1}, {b2,b3}, exactly.
 // Byte v+128 placed in the mantissa of 0x6400 (=1024) gives 1024+v+128;
-// subtracting 1152 leaves v.
+// subtracting 1152 leaves v.  kFlip = 0x80808080 takes two's-complement bytes
+// (v+128 = v ^ 0x80); kFlip = 0 takes bytes already stored as v+128 (the weight
+// tiles), one instruction less per word.
+template <uint32_t kFlip>
 __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
+  const uint32_t u = w ^ kFlip;
   const uint32_t a = __byte_perm(u, 0x6464u, 0x5140u);
   const uint32_t b = __byte_perm(u, 0x6464u, 0x5342u);
   const uint32_t bias = 0x64806480u;  // half2(1152, 1152)
@@ -571,12 +574,15 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // FUSE: kFuseNone, or kFuseSwiglu (GMM1 with SwiGLU: args.sw_*), each its own
 // instantiation, so the plain kernel's drains carry none of the SwiGLU state (its
 // register spills went from 28 to 4 bytes).
+// TILES: the weights come as tiles (args.w_tiles), whose bytes hold v + 128; else
+// through the tensor map as two's-complement int8.
 enum { kFuseNone = 0, kFuseSwiglu = 1 };
-template <bool GATHER, int FUSE>
+template <bool GATHER, int FUSE, bool TILES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                              const Args args) {
   constexpr bool kSw = FUSE == kFuseSwiglu;
+  constexpr uint32_t kWFlip = TILES ? 0u : 0x80808080u;
   static_assert(!(GATHER && FUSE != kFuseNone), "fusion runs on the tiled operand");
   constexpr int S = kStages, SW = kWStages;
   extern __shared__ uint8_t smem_raw[];
@@ -695,7 +701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // channel block) reads the expert's last block instead: finite int8 values
           // whose output channels are never stored, and never a tile past the buffer.
           const uint8_t* wt = nullptr;
-          if (args.w_tiles) {
+          if (TILES) {
             const int nbk = args.N / kBM;
             const int nb = min(it.cb * (kPairCh / kBM) + (int)rank, nbk - 1);
             wt = args.w_tiles + ((size_t)it.e * nbk + nb) * (size_t)args.w_kb * kWBytes;
@@ -893,10 +899,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint4 w4 = lds128(wrow + (((4 * h + q) ^ (r & 7)) << 4));
-              i8x4_to_f16x4(w4.x, v[8 * q + 0], v[8 * q + 1]);
-              i8x4_to_f16x4(w4.y, v[8 * q + 2], v[8 * q + 3]);
-              i8x4_to_f16x4(w4.z, v[8 * q + 4], v[8 * q + 5]);
-              i8x4_to_f16x4(w4.w, v[8 * q + 6], v[8 * q + 7]);
+              i8x4_to_f16x4<kWFlip>(w4.x, v[8 * q + 0], v[8 * q + 1]);
+              i8x4_to_f16x4<kWFlip>(w4.y, v[8 * q + 2], v[8 * q + 3]);
+              i8x4_to_f16x4<kWFlip>(w4.z, v[8 * q + 4], v[8 * q + 5]);
+              i8x4_to_f16x4<kWFlip>(w4.w, v[8 * q + 6], v[8 * q + 7]);
             }
             if (h == 1) {
               // the weight k-block is in registers: hand it back to the producer
@@ -932,10 +938,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // one thread that issues the MMAs sets the kernel's pace, and SwiGLU work beside it
     // slows its issue (prefill GMM1 + SwiGLU: 713 us with every drain warp on rows,
     // 696 us without the issuer's sub-partition; fewer sub-partitions lengthen the tail).
-    constexpr int kRowWarps = kNumDrainWarps - kNumDrainWarps / 4;
-    const bool row_warp = quarter != (kMmaWarp & 3);
+    // On those three, three of the four column groups take rows: the rows' issue slots
+    // slow the converter warp of the same sub-partition, whose stages the MMAs wait for
+    // (696 -> 690 us; two groups 701 us, one 775 us: the rows then pile up at the end).
+    constexpr int kRowGroups = 3;
+    static_assert(kRowGroups <= kNumDrainWarps / 4, "column groups of drain warps");
+    constexpr int kRowWarps = 3 * kRowGroups;
+    auto takes_rows = [](int w) { return (w & 3) != (kMmaWarp & 3) && ((w - kDrainWarp0) >> 2) < kRowGroups; };
+    const bool row_warp = takes_rows(warp);
     int row_rank = 0;
-    for (int w = kDrainWarp0; w < warp; ++w) row_rank += (w & 3) != (kMmaWarp & 3) ? 1 : 0;
+    for (int w = kDrainWarp0; w < warp; ++w) row_rank += takes_rows(w) ? 1 : 0;
     const int sw_stride = (int)gridDim.x * kRowWarps;
     const int sw_valid = s_end[E - 1];
     int sw_row = row_warp ? (int)blockIdx.x * kRowWarps + row_rank : sw_valid;
@@ -1096,7 +1108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool GATHER, int FUSE>
+template <bool GATHER, int FUSE, bool TILES>
 cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   CUtensorMap tw, tx;
   if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.w, (uint64_t)p.Kd, (uint64_t)p.E * p.N, kBK,
@@ -1113,10 +1125,10 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
     // the CTA is launched with; a build that launches with another count would
     // leave the drains' increase waiting forever, so it is refused here.
     cudaFuncAttributes fa;
-    cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_pair_kernel<GATHER, FUSE>);
+    cudaError_t err = cudaFuncGetAttributes(&fa, grouped_gemm_pair_kernel<GATHER, FUSE, TILES>);
     if (err != cudaSuccess) return err;
     if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<GATHER, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(grouped_gemm_pair_kernel<GATHER, FUSE, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemBytes);
     if (err != cudaSuccess) return err;
     checked.done(dev);
@@ -1133,7 +1145,7 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.bounds = p.bounds;
   a.gather_route = p.gather_route;
   a.topK = p.topK;
-  a.w_tiles = p.w_kb ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;
+  a.w_tiles = TILES ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;
   a.w_kb = p.w_kb;
   a.sw_pts1 = p.sw_pts1;
   a.sw_sorted = p.sw_sorted;
@@ -1149,7 +1161,7 @@ cudaError_t launch_pair(const GroupedGemmProblem& p, cudaStream_t stream) {
   if (!a.prof) return cudaErrorInvalidValue;
 #endif
   const int grid = sm_count() & ~1;  // whole pairs, one CTA per SM
-  grouped_gemm_pair_kernel<GATHER, FUSE><<<grid, kThreads, kSmemBytes, stream>>>(tw, tx, a);
+  grouped_gemm_pair_kernel<GATHER, FUSE, TILES><<<grid, kThreads, kSmemBytes, stream>>>(tw, tx, a);
   return cudaGetLastError();
 }
 
@@ -1164,7 +1176,7 @@ bool pair_grid_coresident() {
   if (queried.needed(dev)) {
     // the kernel's attributes (dynamic shared memory) are set by its first launch; set
     // them here too so the query sees the launch's configuration
-    if (cudaFuncSetAttribute(grouped_gemm_pair_kernel<false, kFuseSwiglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(grouped_gemm_pair_kernel<false, kFuseSwiglu, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return false;
     cudaLaunchConfig_t cfg = {};
@@ -1172,7 +1184,7 @@ bool pair_grid_coresident() {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<false, kFuseSwiglu>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<false, kFuseSwiglu, true>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       clusters = 0;
     }
@@ -1182,12 +1194,17 @@ bool pair_grid_coresident() {
   return ok[dev];
 }
 
-cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream) {
+template <bool TILES>
+cudaError_t launch_pair_layout(const GroupedGemmProblem& p, cudaStream_t stream) {
   if (p.gather_route) {
     if (p.sw_q2) return cudaErrorInvalidValue;  // the fused SwiGLU runs on the tiled operand
-    return launch_pair<true, kFuseNone>(p, stream);
+    return launch_pair<true, kFuseNone, TILES>(p, stream);
   }
-  return p.sw_q2 ? launch_pair<false, kFuseSwiglu>(p, stream) : launch_pair<false, kFuseNone>(p, stream);
+  return p.sw_q2 ? launch_pair<false, kFuseSwiglu, TILES>(p, stream) : launch_pair<false, kFuseNone, TILES>(p, stream);
+}
+
+cudaError_t launch_grouped_gemm_tc(const GroupedGemmProblem& p, cudaStream_t stream) {
+  return p.w_kb ? launch_pair_layout<true>(p, stream) : launch_pair_layout<false>(p, stream);
 }
 
 }  // namespace moe

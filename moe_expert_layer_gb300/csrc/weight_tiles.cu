@@ -2,8 +2,9 @@
 // W[E][N][D] rewritten once as 16 KiB tiles of 128 channels x 128 reduction bytes,
 // each tile contiguous and already in the 128-byte-swizzled order that a tensor copy
 // of the same box leaves in shared memory, so the GEMMs move it with one untiled bulk
-// copy.  The tiles stand in for the pre-packed weight of the PTO-ISA MegaMoE operator
-// page (section "3. GMM1"), laid out offline for GB300's copy engine.
+// copy; each weight v is stored as the byte v + 128.  The tiles stand in for the
+// pre-packed weight of the PTO-ISA MegaMoE operator page (section "3. GMM1"), laid
+// out offline for GB300's copy engine.
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -27,9 +28,12 @@ __global__ void pack_weight_tiles_kernel(const int4* __restrict__ w, int N, int 
     const int nb = (int)(eb % NB);
     const size_t e = eb / NB;
     const int kc = kb * (kWTileDepth / 16) + c;  // source chunk along D
-    int4 v = make_int4(0, 0, 0, 0);
+    int4 v = make_int4(0, 0, 0, 0);  // depth padding: the code of 0
     if (kc < d16) v = __ldg(w + ((e * N + (size_t)nb * kWTileRows + r) * (size_t)d16 + kc));
-    tiles[i] = v;
+    // each byte v stored as v + 128 (the sign bit flipped), the form the GEMMs widen
+    // to binary16 with one instruction less per four weights
+    constexpr int kExcess = (int)0x80808080u;
+    tiles[i] = make_int4(v.x ^ kExcess, v.y ^ kExcess, v.z ^ kExcess, v.w ^ kExcess);
   }
 }
 

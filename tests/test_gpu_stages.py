@@ -27,11 +27,13 @@ def _dims(w, layout=0):
 def tiles_ref(w):
     """The weight-tile layout of include/moe_layer.h written out with numpy: w [E][N][D]
     int8 -> tiles (e, nb, kb) of 128 channels x 128 reduction bytes, depth zero-padded to
-    a multiple of 256, 16-byte chunk c of tile row r stored at chunk c ^ (r % 8)."""
+    a multiple of 256, 16-byte chunk c of tile row r stored at chunk c ^ (r % 8), every
+    byte in excess-128 form (w + 128, the padding's zeros as 0x80)."""
     E, N, D = w.shape
     KB = 2 * ((D + 255) // 256)
     pad = np.zeros((E, N, KB * 128), np.int8)
     pad[:, :, :D] = w
+    pad = (pad.view(np.uint8) ^ 0x80).view(np.int8)
     t = pad.reshape(E, N // 128, 128, KB, 8, 16).transpose(0, 1, 3, 2, 4, 5)  # e, nb, kb, r, chunk, byte
     out = np.empty_like(t)
     r = np.arange(128)
@@ -435,7 +437,7 @@ def test_gmm1_swiglu_no_expert_on_the_pairs():
                                    (3, 256, 320)])
 def test_pack_weight_tiles_layout(E, N, D):
     """moe_pack_weight_tiles writes exactly the documented tile layout (bit for bit),
-    zeros in the depth padding included."""
+    the excess-128 bytes and the depth padding's 0x80 included."""
     w = synth.int8_sym127(E * N + D, 5, (E, N, D))
     # GMM2 form: N = K (multiple of 128), D = I (multiple of 64)
     d = moe.dims(1, N, D, E, 1)
