@@ -340,11 +340,11 @@ def roofline_of(w, stage_ms, alg, peaks):
 
 def launches_per_step(w):
     """Our kernels per layer call: the sort (fused into the quant kernel up to 4096
-    routes, one kernel up to 8192, three above), the quant, each GEMM (one engine up
+    routes, one kernel up to 8192, two above), the quant, each GEMM (one engine up
     to 24 rows per expert on average and from 256 on; between, the warp-MMA engine on
     16-row and on 32-row tiles, then the tcgen05 pairs), SwiGLU (inside GMM1 when
     fused_swiglu), combine."""
-    sort_launches = 0 if w.R <= 4096 else (1 if w.R <= 8192 else 3)
+    sort_launches = 0 if w.R <= 4096 else (1 if w.R <= 8192 else 2)
     gemm_launches = 1 if (w.R / w.E <= 24.0 or w.R / w.E >= 256.0) else 3
     return sort_launches + 1 + 2 * gemm_launches + (0 if fused_swiglu(w) else 1) + 1
 

@@ -281,7 +281,7 @@ int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, const int32_t* 
  * reserved the whole device up front, a loop where cudaMalloc's implicit
  * synchronisation is not allowed).  It computes exactly what moe_route_sort
  * computes, with the same checks and error codes, but takes no workspace: its
- * scratch is a fixed 512 KiB array in the library's own device memory, which
+ * scratch is a fixed 256 KiB array in the library's own device memory, which
  * every GPU that loads the library holds until the process exits.
  *   - Supports M * topK <= MOE_ROUTE_SORT_NOALLOC_MAX_ROUTES (and the usual
  *     E <= 1023); larger sizes return MOE_ERR_SHAPE and launch nothing.
@@ -292,8 +292,8 @@ int32_t moe_quant_tokens(const moe_dims_t* d, const uint16_t* x, const int32_t* 
  *     again after a cudaDeviceReset (or after the primary context was released
  *     and created anew), which loads the library's device code at a new address.
  *     Make that first call before any stream capture.
- *   - The multi-block sort it runs above 8192 routes uses at most 64 CTAs (the
- *     regular sort up to 2048), sized to the fixed scratch.
+ *   - The multi-block sort it runs above 8192 routes uses at most 64 CTAs, as
+ *     moe_route_sort does, sized to the fixed scratch.
  *   - All calls share the one scratch array: calls that may overlap on the GPU
  *     (different streams without ordering between them) race and must not be
  *     issued.  Calls ordered on one stream are safe; nothing in the scratch needs

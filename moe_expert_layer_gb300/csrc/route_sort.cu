@@ -8,8 +8,10 @@
 //
 // The page's NPU merge sort (TSORT32 + TMRGSORT) is replaced by a counting sort,
 // which is the natural GPU form for small integer keys: a per-block histogram,
-// one scan over (expert, block), and a stable scatter in which each warp ranks
-// its routes with __match_any_sync and a per-warp count table.  The order
+// a scan over (expert, block), and a stable scatter in which each warp ranks its
+// routes with __match_any_sync and a per-warp count table.  Above one block's
+// routes that is two launches: the histograms, then the scatter, each of whose
+// blocks scans the histograms for its own offsets.  The order
 // within an expert is the route order, so every output is unique (bit-exact).
 // Bucket E collects routes with an expert id outside [0, E); they land after
 // all valid routes with expandedRowIdx = -1.
@@ -174,39 +176,35 @@ __global__ void __launch_bounds__(kSortThreads) route_hist_kernel(const int32_t*
   for (int j = threadIdx.x; j <= E; j += kSortThreads) block_hist[blockIdx.x * (E + 1) + j] = hist[j];
 }
 
-__global__ void __launch_bounds__(kSortThreads) route_scan_kernel(const int32_t* __restrict__ block_hist,
-                                                                  int nb, int E,
-                                                                  int32_t* __restrict__ tokens_per_expert,
-                                                                  int32_t* __restrict__ cumsum,
-                                                                  int32_t* __restrict__ block_off) {
-  __shared__ int warp_sums[32];
-  const int j = threadIdx.x;
-  int total = 0;
-  if (j <= E)
-    for (int b = 0; b < nb; ++b) total += block_hist[b * (E + 1) + j];
-  const int start = block_exclusive_scan(total, warp_sums);
-  if (j < E) {
-    tokens_per_expert[j] = total;
-    cumsum[j] = start + total;
-  }
-  if (j <= E) {
-    int run = start;
-    for (int b = 0; b < nb; ++b) {
-      block_off[b * (E + 1) + j] = run;
-      run += block_hist[b * (E + 1) + j];
-    }
-  }
-}
-
+// Every block scans the (bucket, block) histograms itself: bucket j's total over
+// all blocks and its count in the blocks before this one, then the exclusive scan
+// of the totals over buckets; block 0 also writes the counts and their prefix.
 __global__ void __launch_bounds__(kSortThreads) route_scatter_kernel(
-    const int32_t* __restrict__ expert_idx, int R, int E, int chunk, const int32_t* __restrict__ block_off,
+    const int32_t* __restrict__ expert_idx, int R, int E, int chunk, const int32_t* __restrict__ block_hist,
+    int nb, int32_t* __restrict__ tokens_per_expert, int32_t* __restrict__ cumsum,
     int32_t* __restrict__ sorted_src_route, int32_t* __restrict__ expanded_row_idx) {
   extern __shared__ int smem_i[];
   int* base = smem_i;  // this block's first expanded row of each bucket
+  int* warp_sums = smem_i + 2048;
   uint16_t* hist = reinterpret_cast<uint16_t*>(smem_i + 2048 + 32);
   const int pitch = table_pitch(E);
   const int r0 = blockIdx.x * chunk, r1 = min(R, r0 + chunk);
-  for (int j = threadIdx.x; j <= E; j += kSortThreads) base[j] = block_off[blockIdx.x * (E + 1) + j];
+  {
+    const int j = threadIdx.x;  // E + 1 <= kSortThreads buckets
+    int total = 0, before = 0;
+    if (j <= E)
+      for (int b = 0; b < nb; ++b) {
+        const int c = __ldg(block_hist + b * (E + 1) + j);
+        total += c;
+        before += b < (int)blockIdx.x ? c : 0;
+      }
+    const int start = block_exclusive_scan(total, warp_sums);
+    if (j <= E) base[j] = start + before;
+    if (blockIdx.x == 0 && j < E) {
+      tokens_per_expert[j] = total;
+      cumsum[j] = start + total;
+    }
+  }
   const int rpw = range_per_warp(chunk);
   int b[kMaxGroups], rank[kMaxGroups];
   load_and_rank(expert_idx, r0, r1, E, rpw, hist, pitch, b, rank);
@@ -248,7 +246,7 @@ size_t route_sort_workspace_bytes(int R, int E, int max_blocks) {
   if (R <= kSingleBlockMaxRoutes) return 0;
   const int chunk = sort_chunk(R, max_blocks);
   const size_t nb = (size_t)((R + chunk - 1) / chunk);
-  return 2 * nb * (size_t)(E + 1) * sizeof(int32_t);
+  return nb * (size_t)(E + 1) * sizeof(int32_t);  // the per-block histograms
 }
 
 cudaError_t launch_route_sort(const int32_t* expert_idx, int R, int E, int32_t* sorted_src_route,
@@ -273,10 +271,9 @@ cudaError_t launch_route_sort(const int32_t* expert_idx, int R, int E, int32_t* 
   const int chunk = sort_chunk(R, max_blocks);
   const int nb = (R + chunk - 1) / chunk;
   int32_t* block_hist = static_cast<int32_t*>(workspace);
-  int32_t* block_off = block_hist + (size_t)nb * (E + 1);
   route_hist_kernel<<<nb, kSortThreads, (size_t)(E + 1) * 4, stream>>>(expert_idx, R, E, chunk, block_hist);
-  route_scan_kernel<<<1, kSortThreads, 0, stream>>>(block_hist, nb, E, tokens_per_expert, cumsum, block_off);
-  route_scatter_kernel<<<nb, kSortThreads, smem, stream>>>(expert_idx, R, E, chunk, block_off, sorted_src_route,
+  route_scatter_kernel<<<nb, kSortThreads, smem, stream>>>(expert_idx, R, E, chunk, block_hist, nb,
+                                                           tokens_per_expert, cumsum, sorted_src_route,
                                                            expanded_row_idx);
   return cudaGetLastError();
 }

@@ -5,8 +5,8 @@
 // already handed all device memory to its own pool, a server that reserved
 // the whole device up front for its caches, or a latency-critical loop in which
 // a cudaMalloc (which can synchronise the device) is not allowed.  For them,
-// the sort's scratch (per-block histograms and per-block insertion offsets of
-// the multi-block path) lives in a fixed array in this library's device memory
+// the sort's scratch (the per-block histograms of the multi-block path) lives in
+// a fixed array in this library's device memory
 // instead of a caller-provided workspace.  The caller still passes the inputs
 // and outputs.
 //
@@ -28,10 +28,10 @@
 namespace {
 
 // Multi-block path: at most kMaxBlocks blocks (8192 routes each at the largest R),
-// E + 1 <= 1024 buckets, two tables.
+// E + 1 <= 1024 buckets, one histogram per block.
 constexpr int kMaxBlocks = 64;
 static_assert(MOE_ROUTE_SORT_NOALLOC_MAX_ROUTES <= kMaxBlocks * 8192, "blocks of the largest sort");
-constexpr size_t kScratchInts = 2u * kMaxBlocks * 1024u;  // 128 Ki int32 = 512 KiB
+constexpr size_t kScratchInts = kMaxBlocks * 1024u;  // 64 Ki int32 = 256 KiB
 
 static __device__ __align__(256) int32_t g_route_sort_scratch[kScratchInts];
 
@@ -74,8 +74,8 @@ extern "C" int32_t moe_route_sort_noalloc(const moe_dims_t* d, const int32_t* ex
   if ((rc = moe::check_device()) != MOE_OK) return rc;
   int32_t* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_LAUNCH;
-  // The kernels write every scratch entry they later read (histogram, then
-  // offsets), so the previous call's contents need no clearing.
+  // The kernels write every scratch entry they later read (the histograms), so
+  // the previous call's contents need no clearing.
   return moe::launch_status(moe::launch_route_sort(expert_idx, (int)R, d->E, sorted_src_route, expanded_row_idx,
                                                    tokens_per_expert, cumsum, scratch,
                                                    static_cast<cudaStream_t>(stream), kMaxBlocks));

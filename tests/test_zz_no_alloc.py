@@ -50,7 +50,7 @@ def _oracle(ei, E):
 CASES = [
     # (M, topK, E, routing, seed): large route counts take the multi-block path whose
     # scratch is the fixed array; the largest case fills it exactly (R at the limit,
-    # E = 1023: 64 blocks of 8192 routes, 2 * 64 * 1024 scratch entries), the next one
+    # E = 1023: 64 blocks of 8192 routes, 64 * 1024 scratch entries), the next one
     # sits one route below the limit; the last case is a small single-block sort
     (8192, 6, 64, "uniform", 4),
     (2048, 8, 256, "zipf", 3),
