@@ -27,6 +27,11 @@
 // needs no dispatched copy of the tokens; the layer itself keeps the dispatched
 // rows, which measured faster.
 //
+// Warps.  16 MMA warps in two groups of 8 (group g computes the stages in ring
+// slots s % 2 == g), one TMA producer warp, and two epilogue warps that scale,
+// convert and store each item from the int32 sums both groups add into shared
+// memory at the item's end, so that no MMA warp stops for an epilogue.
+//
 // Tiling.  One CTA computes 128 channels x T rows of one expert.  The work list
 // (expert, row tile) is derived by each CTA from cumsum; CTAs whose index lies
 // beyond the number of row tiles exit at once.  The reduction is swapped so that
@@ -44,7 +49,10 @@ namespace {
 constexpr int kGroupWarps = 8;                        // MMA warps per group
 constexpr int kGroups = 2;                            // group g computes the stages in slots s % kGroups == g
 constexpr int kConsumerWarps = kGroups * kGroupWarps;
-constexpr int kGemmThreads = (kConsumerWarps + 1) * 32;  // + 1 TMA producer warp
+// Epilogue warps (after the TMA producer warp).  Two keep the CTA at 19 warps and the
+// MMA warps at 96 registers; four (21 warps) left them 80 under the launch bound.
+constexpr int kEpiWarps = 2;
+constexpr int kGemmThreads = (kConsumerWarps + 1 + kEpiWarps) * 32;
 constexpr int kBN = 128;         // channels per work item
 constexpr int kBK = 256;         // reduction depth per pipeline stage
 constexpr int kSubK = 128;       // weight sub-tile depth (one 128-byte swizzled TMA box)
@@ -76,9 +84,10 @@ struct GemmCfg {
   static constexpr int W_BYTES = (kBK / kSubK) * W_SUB_BYTES;
   static constexpr int STAGE_BYTES = X_BYTES + W_BYTES;
   static constexpr int EPI_BYTES = T * kBN * 2;
-  static constexpr int PART_BYTES = kGroupWarps * MT * NT * 4 * 32 * 4;  // one group's partials
+  static constexpr int PART_BYTES = kGroupWarps * MT * NT * 4 * 32 * 4;  // the item's int32 sums
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + PART_BYTES + 1024;
   static_assert(WARPS_M * WARPS_N == kGroupWarps, "warp grid");
+  static_assert(T <= 32, "one lane per row of the epilogue's row copies");
   // stage n is computed by group n % kGroups: with STAGES a multiple of kGroups every
   // ring slot always belongs to the same group, which then waits on every phase of its
   // slots in order (a group never tests the parity of a phase it skipped)
@@ -214,8 +223,21 @@ __device__ __forceinline__ void drain_chunk(float (&accf)[Cfg::P][Cfg::MT][Cfg::
 }
 
 __device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32)); }
-// the 8 warps of the group that runs an item's epilogue (one group at a time)
-__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kGroupWarps * 32)); }
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kEpiWarps * 32)); }
+// The epilogue warps' barrier with an OR over their votes: the same answer in every
+// epilogue warp, so they leave their loop together.
+__device__ __forceinline__ bool epilogue_bar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 2, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u), "n"(kEpiWarps * 32)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ bool wait_part(uint64_t* bar, uint32_t parity, int32_t* status) {
   if (mbar_wait_bounded(bar, parity)) return true;
@@ -293,8 +315,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[S];
   __shared__ __align__(8) uint64_t empty_bar[S];
-  __shared__ __align__(8) uint64_t part_full_bar;   // partials hand-off to the epilogue group
-  __shared__ __align__(8) uint64_t part_empty_bar;  // the epilogue group has read them
+  __shared__ __align__(8) uint64_t part_full_bar;   // both groups' partials are in the item's sums
+  __shared__ __align__(8) uint64_t part_empty_bar;  // the epilogue warps have read (and cleared) them
   __shared__ int s_pref[kMaxExperts + 1];  // first work item of each expert
   __shared__ int s_end[kMaxExperts];       // cumsum
   __shared__ int s_wsum[kConsumerWarps];
@@ -330,7 +352,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       run += own_items<T>(s_end[e] - lo, args.min_rows, args.split_rows, n_cb);
     }
     if (e0 < E && e1 == E) s_pref[E] = run;
-  } else if (lane == 0) {
+  } else if (warp == kConsumerWarps && lane == 0) {
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_x);
     prefetch_tmap(&tm_x8);
@@ -338,8 +360,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], kGroupWarps);  // one group consumes each stage
     }
-    mbar_init(&part_full_bar, kGroupWarps);
-    mbar_init(&part_empty_bar, kGroupWarps);
+    mbar_init(&part_full_bar, kConsumerWarps);
+    mbar_init(&part_empty_bar, kEpiWarps);
     s_abort = 0;
     s_issued = 0;
     fence_barrier_init();
@@ -349,6 +371,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
+  __half* stile = reinterpret_cast<__half*>(smem_gen + S * Cfg::STAGE_BYTES);  // [T][kBN] output staging
+  int* sums = reinterpret_cast<int*>(smem_gen + S * Cfg::STAGE_BYTES + Cfg::EPI_BYTES);  // fragment order
+  constexpr int kPartWarp = Cfg::MT * Cfg::NT * 4 * 32;  // sums per consumer-warp slice
+  for (int i = threadIdx.x; i < Cfg::PART_BYTES / 16; i += kGemmThreads)
+    reinterpret_cast<int4*>(sums)[i] = make_int4(0, 0, 0, 0);  // the first item's sums start at zero
 
   if (GATHER) {
     // Gathered stages leave the rows past a tile's last 4-row group, and quarters
@@ -361,8 +388,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       for (int i = threadIdx.x; i < Cfg::X_BYTES / 16; i += kGemmThreads) xz[i] = make_int4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
-    __syncthreads();
   }
+  __syncthreads();
 
   if (warp == kConsumerWarps) {
     // ================= TMA producer warp =================
@@ -439,35 +466,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     }
   producer_done:
     if (lane == 0) s_issued = issued;
-  } else {
+  } else if (warp < kConsumerWarps) {
     // ================= MMA consumer warps =================
     // Group grp (8 warps) computes the stages held in ring slots s with
-    // s % kGroups == grp (both 64-deep halves); the groups' exact int32 partial sums
-    // are added in the epilogue.
+    // s % kGroups == grp (both 64-deep halves); at the item's end both groups add
+    // their exact int32 partial sums into the item's sums (shared memory) and go on.
     const int grp = warp / kGroupWarps, wig = warp % kGroupWarps;
     const int warp_m = wig % Cfg::WARPS_M, warp_n = wig / Cfg::WARPS_M;
     const int g = lane >> 2, tq = lane & 3;
     const int pg = mrow_perm(g);
     constexpr uint32_t wflip = TILES ? 0u : 0x80808080u;  // tile bytes hold v + 128
-    __half* stile = reinterpret_cast<__half*>(smem_gen + S * Cfg::STAGE_BYTES);
-    constexpr int kPartWarp = Cfg::MT * Cfg::NT * 4 * 32;  // ints per warp
-    int* spart_base = reinterpret_cast<int*>(smem_gen + S * Cfg::STAGE_BYTES + Cfg::EPI_BYTES) + wig * kPartWarp + lane;
-    int* spart = spart_base;
+    int* spart = sums + wig * kPartWarp + lane;
     int slot = 0;
     uint32_t phase = 0;
     int consumed = 0, n_items = 0, e_hint = 0;
     bool ok = true;
     for (int j = blockIdx.x; j < total && ok; j += gridDim.x) {
       const Item it = decode_item<T>(j, s_pref, s_end, E, n_cb, e_hint);
-      // channel scales of this item, loaded early so the k-loop hides their latency
-      const float* sc = args.scale + (size_t)it.e * args.N + it.cb * kBN;
-      float s_lo[Cfg::MT], s_hi[Cfg::MT];
-#pragma unroll
-      for (int mt = 0; mt < Cfg::MT; ++mt) {
-        const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
-        s_lo[mt] = __ldg(sc + m);
-        s_hi[mt] = __ldg(sc + m + 8);
-      }
       float accf[Cfg::P][Cfg::MT][Cfg::NT][4];
       int acci[Cfg::MT][Cfg::NT][4];
 #pragma unroll
@@ -508,86 +523,108 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
       }
       if (own % 2 != 0) drain_chunk<Cfg>(accf, acci);
-      // ---- epilogue.  One group runs the item's epilogue; the other hands its int32
-      // partials over through shared memory (part_full) and moves on to the next
-      // item; the epilogue group adds them, scales, converts, stages [T][128]
-      // binary16 and stores it coalesced.
-      // The epilogue group is the one that computes the item's last stage: the other
-      // group's partials are then ready when it gets there, so neither group idles
-      // at the hand-off (with the groups taking turns instead, every other item's
-      // epilogue group waited a stage for the other's partials while its next
-      // stages, and behind them the in-order producer, stalled: mid GMM2 745 -> 725 us).
-      // Each warp owns one slice of the partials buffer; a sender rewrites its slice
-      // only after the epilogue group has read the previous item's (part_empty).
-      // Item n's epilogue ends (its staging-tile reads included) before the next
-      // epilogue starts: with an even stage count per item the same group runs every
-      // epilogue, with an odd one the groups alternate and the sender of item n + 1
-      // is item n's epilogue group, which sends only after that epilogue.
-      const int epi_grp = ((n_items * nk + nk - 1) % S) % kGroups;
-      if (grp != epi_grp) {
-        if (n_items > 0) {
-          bool free = lane == 0 ? wait_part(&part_empty_bar, (n_items - 1) & 1, args.status) : true;
-          free = __shfl_sync(0xffffffffu, free ? 1 : 0, 0) != 0;
-          ok = ok && free;
-        }
-        if (ok) {
-#pragma unroll
-          for (int mt = 0; mt < Cfg::MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < Cfg::NT; ++nt)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) spart[((mt * Cfg::NT + nt) * 4 + i) * 32] = acci[mt][nt][i];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&part_full_bar);
-      } else {
-        bool got = wait_part(&part_full_bar, n_items & 1, args.status);
-        got = __all_sync(0xffffffffu, got);
-        int v[Cfg::MT][Cfg::NT][4];
+      // ---- hand-off: both groups add their partials into the item's sums
+      // (shared-memory atomics, exact and in any order) once the epilogue warps have
+      // read and cleared the previous item's, and go on to the next item at once.
+      // (When the group that computed an item's last stage also ran its epilogue,
+      // the other handing it the partials, an even stage count per item made that
+      // the same group every time, and the in-order producer waited on it: the mid
+      // workload's GMM1 / GMM2 took 1295 / 726 us, 1224 / 662 us with epilogue warps.)
+      if (n_items > 0) {
+        bool free = lane == 0 ? wait_part(&part_empty_bar, (n_items - 1) & 1, args.status) : true;
+        free = __shfl_sync(0xffffffffu, free ? 1 : 0, 0) != 0;
+        ok = ok && free;
+      }
+      if (ok) {
 #pragma unroll
         for (int mt = 0; mt < Cfg::MT; ++mt)
 #pragma unroll
           for (int nt = 0; nt < Cfg::NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              int sum = acci[mt][nt][i];
+            for (int i = 0; i < 4; ++i) atomicAdd(spart + ((mt * Cfg::NT + nt) * 4 + i) * 32, acci[mt][nt][i]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&part_full_bar);
+      ++n_items;
+    }
+    (void)consumed;
+  } else {
+    // ================= epilogue warps =================
+    // Per item: the sums of consumer slices kSlices*ew .. kSlices*ew + kSlices - 1 (the
+    // fragments those MMA warps hold) are read and cleared, scaled, converted and
+    // staged as [T][128] binary16; then one warp hands each row (256 bytes) to an
+    // asynchronous bulk copy to global memory and waits only until the copies have
+    // read the staging tile.
+    const int ew = warp - kConsumerWarps - 1;
+    const int g = lane >> 2, tq = lane & 3;
+    const int pg = mrow_perm(g);
+    constexpr int kSlices = kGroupWarps / kEpiWarps;
+    static_assert(kGroupWarps % kEpiWarps == 0, "consumer slices per epilogue warp");
+    int n_items = 0, e_hint = 0;
+    for (int j = blockIdx.x; j < total; j += gridDim.x) {
+      const Item it = decode_item<T>(j, s_pref, s_end, E, n_cb, e_hint);
+      const float* sc = args.scale + (size_t)it.e * args.N + it.cb * kBN;
+      bool got = lane == 0 ? wait_part(&part_full_bar, n_items & 1, args.status) : true;
+      got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      if (!got) s_abort = 1;
+      // leave together on a failed wait or an abort (the previous item's row copies
+      // have read the staging tile once every epilogue warp is past this barrier)
+      if (epilogue_bar_or(!got || *(volatile int*)&s_abort)) break;
+      __half h[kSlices][Cfg::MT][Cfg::NT][4];
 #pragma unroll
-              for (int q = 1; q < kGroups; ++q)
-                sum += got ? spart_base[(q - 1) * kGroupWarps * kPartWarp + ((mt * Cfg::NT + nt) * 4 + i) * 32] : 0;
-              v[mt][nt][i] = sum;
+      for (int sl = 0; sl < kSlices; ++sl) {
+        const int wig = ew * kSlices + sl;
+        const int warp_m = wig % Cfg::WARPS_M;
+        int* sp = sums + wig * kPartWarp + lane;
+#pragma unroll
+        for (int mt = 0; mt < Cfg::MT; ++mt) {
+          const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
+          const float s_lo = __ldg(sc + m), s_hi = __ldg(sc + m + 8);
+#pragma unroll
+          for (int nt = 0; nt < Cfg::NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              int* q = sp + ((mt * Cfg::NT + nt) * 4 + i) * 32;
+              const int v = *q;
+              *q = 0;
+              h[sl][mt][nt][i] = f2h_sat(__fmul_rn(__int2float_rn(v), i < 2 ? s_lo : s_hi));
             }
-        __syncwarp();  // the slice is read (the sums above use every loaded value)
-        if (lane == 0) mbar_arrive(&part_empty_bar);
-        ok = ok && got;
-        epilogue_bar();  // the previous epilogue's staging-tile reads are done
-        if (ok) {
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&part_empty_bar);  // the sums are read and cleared
+      {
+#pragma unroll
+        for (int sl = 0; sl < kSlices; ++sl) {
+          const int wig = ew * kSlices + sl;
+          const int warp_m = wig % Cfg::WARPS_M, warp_n = wig / Cfg::WARPS_M;
 #pragma unroll
           for (int mt = 0; mt < Cfg::MT; ++mt) {
             const int m = warp_m * Cfg::MT * 16 + mt * 16 + pg;
 #pragma unroll
             for (int nt = 0; nt < Cfg::NT; ++nt) {
               const int n = warp_n * Cfg::NT * 8 + nt * 8 + 2 * tq;
-              stile[n * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(v[mt][nt][0]), s_lo[mt]));
-              stile[(n + 1) * kBN + m] = f2h_sat(__fmul_rn(__int2float_rn(v[mt][nt][1]), s_lo[mt]));
-              stile[n * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(v[mt][nt][2]), s_hi[mt]));
-              stile[(n + 1) * kBN + m + 8] = f2h_sat(__fmul_rn(__int2float_rn(v[mt][nt][3]), s_hi[mt]));
+              stile[n * kBN + m] = h[sl][mt][nt][0];
+              stile[(n + 1) * kBN + m] = h[sl][mt][nt][1];
+              stile[n * kBN + m + 8] = h[sl][mt][nt][2];
+              stile[(n + 1) * kBN + m + 8] = h[sl][mt][nt][3];
             }
           }
         }
-        epilogue_bar();
-        ok = ok && !*(volatile int*)&s_abort;
-        if (ok) {
-          const int4* src = reinterpret_cast<const int4*>(stile);
-          __half* dst = args.C + (size_t)it.row0 * args.N + it.cb * kBN;
-          for (int i = wig * 32 + lane; i < it.rows * (kBN / 8); i += kGroupWarps * 32) {
-            const int r = i / (kBN / 8), c = i % (kBN / 8);
-            reinterpret_cast<int4*>(dst + (size_t)r * args.N)[c] = src[r * (kBN / 8) + c];
-          }
-        }
+      }
+      fence_proxy_async_smem();  // the tile's writes before the bulk copies read it
+      epilogue_bar();
+      if (ew == 0) {
+        // row r < rows (<= T <= 32) by lane r: N and the channel block are multiples
+        // of 128, so both ends of every row copy are 16-byte aligned
+        if (lane < it.rows)
+          bulk_store(args.C + (size_t)(it.row0 + lane) * args.N + it.cb * kBN, stile + lane * kBN, kBN * 2);
+        bulk_commit_group();
+        bulk_wait_read_all();  // the tile is free for the next item
       }
       ++n_items;
     }
-    (void)consumed;
+    bulk_wait_all();  // every row copy this thread issued has landed
   }
 
   __syncthreads();
