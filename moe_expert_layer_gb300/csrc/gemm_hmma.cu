@@ -28,9 +28,10 @@
 // rows, which measured faster.
 //
 // Warps.  16 MMA warps in two groups of 8 (group g computes the stages in ring
-// slots s % 2 == g), one TMA producer warp, and two epilogue warps that scale,
-// convert and store each item from the int32 sums both groups add into shared
-// memory at the item's end, so that no MMA warp stops for an epilogue.
+// slots s % 2 == g), TMA producer warps (one per group for 16-row tiles, else one),
+// and two epilogue warps that scale, convert and store each item from the int32
+// sums both groups add into shared memory at the item's end, so that no MMA warp
+// stops for an epilogue.
 //
 // Tiling.  One CTA computes 128 channels x T rows of one expert.  The work list
 // (expert, row tile) is derived by each CTA from cumsum; CTAs whose index lies
@@ -49,10 +50,11 @@ namespace {
 constexpr int kGroupWarps = 8;                        // MMA warps per group
 constexpr int kGroups = 2;                            // group g computes the stages in slots s % kGroups == g
 constexpr int kConsumerWarps = kGroups * kGroupWarps;
-// Epilogue warps (after the TMA producer warp).  Two keep the CTA at 19 warps and the
-// MMA warps at 96 registers; four (21 warps) left them 80 under the launch bound.
+constexpr int kMaxProducerWarps = kGroups;  // TMA producer warps (per tile shape: 1 or kGroups)
+// Epilogue warps (after the producers).  Two keep the CTA at 19-20 warps and the MMA
+// warps at 96 registers; four epilogue warps (21-22 warps) would leave them 80 under
+// the launch bound.
 constexpr int kEpiWarps = 2;
-constexpr int kGemmThreads = (kConsumerWarps + 1 + kEpiWarps) * 32;
 constexpr int kBN = 128;         // channels per work item
 constexpr int kBK = 256;         // reduction depth per pipeline stage
 constexpr int kSubK = 128;       // weight sub-tile depth (one 128-byte swizzled TMA box)
@@ -65,10 +67,14 @@ struct TileShape;
 // round-robin to them). 16-row tiles have 2 fragments per warp and take 4 partials
 // so that 8 MMA chains are in flight; 32-row tiles have 4 fragments and measure
 // faster with a single partial (fewer registers, no fold in the epilogue).
+// PRODUCERS: TMA producer warps.  With one per MMA group each fills only its group's
+// ring slots, so a group that falls behind holds back its own stages' loads and not the
+// other's: decode GMM1 / GMM2 1067 / 557 -> 1044 / 542 us on 16-row tiles; on 32-row
+// tiles (mid: 1225 / 660 -> 1233 / 683 us, consumer-bound) one producer stays.
 template <>
-struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 4, P = 4; };
+struct TileShape<16> { static constexpr int WM = 8, WN = 1, STAGES = 4, P = 4, PRODUCERS = 2; };
 template <>
-struct TileShape<32> { static constexpr int WM = 8, WN = 1, STAGES = 4, P = 1; };
+struct TileShape<32> { static constexpr int WM = 8, WN = 1, STAGES = 4, P = 1, PRODUCERS = 1; };
 
 template <int T>
 struct GemmCfg {
@@ -78,6 +84,9 @@ struct GemmCfg {
   static constexpr int MT = kBN / (16 * WARPS_M);  // m16 tiles per warp
   static constexpr int NT = T / (8 * WARPS_N);     // n8 tiles per warp
   static constexpr int P = TileShape<T>::P;
+  static constexpr int PRODUCERS = TileShape<T>::PRODUCERS;
+  static constexpr int THREADS = (kConsumerWarps + PRODUCERS + kEpiWarps) * 32;
+  static_assert(PRODUCERS == 1 || PRODUCERS == kGroups, "one producer, or one per MMA group");
   static constexpr int X_HALF_BYTES = T * 128;     // one k quarter: [T][64] binary16, 128-B swizzled rows
   static constexpr int X_BYTES = kQuarters * X_HALF_BYTES;
   static constexpr int W_SUB_BYTES = kBN * kSubK;  // [128][128] int8, 128-B swizzled rows
@@ -306,7 +315,7 @@ __device__ __forceinline__ Item decode_item(int j, const int* s_pref, const int*
 // GATHER: token rows gathered by index (args.gather_route) instead of tiled boxes of
 // expert-major rows; a separate instantiation, so the tiled kernel carries none of it.
 template <int T, bool GATHER, bool TILES>
-__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
+__global__ void __launch_bounds__(GemmCfg<T>::THREADS, 1) grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w,
                                                                        const __grid_constant__ CUtensorMap tm_x,
                                                                        const __grid_constant__ CUtensorMap tm_x8,
                                                                        const GemmArgs args) {
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   __shared__ int s_pref[kMaxExperts + 1];  // first work item of each expert
   __shared__ int s_end[kMaxExperts];       // cumsum
   __shared__ int s_wsum[kConsumerWarps];
-  __shared__ int s_abort, s_issued;
+  __shared__ int s_abort, s_issued[kMaxProducerWarps];  // per producer: 1 + its last stage issued
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = args.E, n_cb = args.N / kBN;
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     mbar_init(&part_full_bar, kConsumerWarps);
     mbar_init(&part_empty_bar, kEpiWarps);
     s_abort = 0;
-    s_issued = 0;
+    for (int q = 0; q < kMaxProducerWarps; ++q) s_issued[q] = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   __half* stile = reinterpret_cast<__half*>(smem_gen + S * Cfg::STAGE_BYTES);  // [T][kBN] output staging
   int* sums = reinterpret_cast<int*>(smem_gen + S * Cfg::STAGE_BYTES + Cfg::EPI_BYTES);  // fragment order
   constexpr int kPartWarp = Cfg::MT * Cfg::NT * 4 * 32;  // sums per consumer-warp slice
-  for (int i = threadIdx.x; i < Cfg::PART_BYTES / 16; i += kGemmThreads)
+  for (int i = threadIdx.x; i < Cfg::PART_BYTES / 16; i += Cfg::THREADS)
     reinterpret_cast<int4*>(sums)[i] = make_int4(0, 0, 0, 0);  // the first item's sums start at zero
 
   if (GATHER) {
@@ -385,19 +394,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     // cannot disturb anything.
     for (int s = 0; s < S; ++s) {
       int4* xz = reinterpret_cast<int4*>(smem_gen + s * Cfg::STAGE_BYTES);
-      for (int i = threadIdx.x; i < Cfg::X_BYTES / 16; i += kGemmThreads) xz[i] = make_int4(0, 0, 0, 0);
+      for (int i = threadIdx.x; i < Cfg::X_BYTES / 16; i += Cfg::THREADS) xz[i] = make_int4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
-    // ================= TMA producer warp =================
+  if (warp >= kConsumerWarps && warp < kConsumerWarps + Cfg::PRODUCERS) {
+    // ================= TMA producer warps =================
+    // Producer q loads the stages n with n % PRODUCERS == q (with one per group, ring
+    // slots s % kGroups == q, those of MMA group q) and walks past the others.
+    const int q_own = warp - kConsumerWarps;
     constexpr bool gather = GATHER;
     int e_hint = 0;
     int slot = 0;
     uint32_t phase = 0;
-    int issued = 0;
+    int issued = 0;  // stages issued (one producer), else 1 + the last one's global index
+    int n = 0;       // global stage index (one producer per group)
     for (int j = blockIdx.x; j < total; j += gridDim.x) {
       const Item it = decode_item<T>(j, s_pref, s_end, E, n_cb, e_hint);
       const int w_row = it.e * args.N + it.cb * kBN;
@@ -418,6 +431,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         tok.w = __ldg(args.gather_route + min(r0 + 3, last)) / args.topK;
       }
       for (int kb = 0; kb < nk; ++kb) {
+        if constexpr (Cfg::PRODUCERS > 1) {
+          if (n++ % Cfg::PRODUCERS != q_own) {
+            if (++slot == S) {
+              slot = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+        }
         const int kx = kb * kBK;
         // quarters of this stage inside K (K % 128 == 0: a tail stage has 2); the
         // tiled boxes read zero fill past K, the gathers are not issued there
@@ -457,7 +479,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             tma_gather4(xs + q * Cfg::X_HALF_BYTES + r * 512, &tm_x, kx + 64 * q, tok, &full_bar[slot]);
           }
         }
-        ++issued;
+        if constexpr (Cfg::PRODUCERS > 1) issued = n;  // n is already past this stage
+        else ++issued;
         if (++slot == S) {
           slot = 0;
           phase ^= 1u;
@@ -465,7 +488,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       }
     }
   producer_done:
-    if (lane == 0) s_issued = issued;
+    if (lane == 0) s_issued[q_own] = issued;
   } else if (warp < kConsumerWarps) {
     // ================= MMA consumer warps =================
     // Group grp (8 warps) computes the stages held in ring slots s with
@@ -555,7 +578,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     // staged as [T][128] binary16; then one warp hands each row (256 bytes) to an
     // asynchronous bulk copy to global memory and waits only until the copies have
     // read the staging tile.
-    const int ew = warp - kConsumerWarps - 1;
+    const int ew = warp - kConsumerWarps - Cfg::PRODUCERS;
     const int g = lane >> 2, tq = lane & 3;
     const int pg = mrow_perm(g);
     constexpr int kSlices = kGroupWarps / kEpiWarps;
@@ -629,10 +652,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
   __syncthreads();
   if (s_abort && threadIdx.x == kConsumerWarps * 32) {
-    // let loads still in flight land before the CTA's shared memory is released: the
-    // last S issued stages are the latest phase of each slot
-    const int issued = s_issued;
-    for (int n = max(0, issued - S); n < issued; ++n) mbar_wait_bounded(&full_bar[n % S], (uint32_t)((n / S) & 1));
+    // let loads still in flight land before the CTA's shared memory is released: each
+    // producer's last S / PRODUCERS issued stages are the latest phase of its slots
+    // (with one producer, s_issued counts its stages, which are all of them in order)
+    for (int q = 0; q < Cfg::PRODUCERS; ++q) {
+      const int last = s_issued[q] - 1;  // -1: nothing issued
+      for (int n = last; n >= 0 && n > last - S; n -= Cfg::PRODUCERS)
+        mbar_wait_bounded(&full_bar[n % S], (uint32_t)((n / S) & 1));
+    }
   }
 }
 
@@ -677,7 +704,7 @@ cudaError_t launch_t(const GroupedGemmProblem& p, cudaStream_t stream) {
   a.topK = p.topK;
   a.w_tiles = TILES ? reinterpret_cast<const uint8_t*>(p.w) : nullptr;
   a.w_kb = p.w_kb;
-  grouped_gemm_kernel<T, GATHER, TILES><<<sm_count(), kGemmThreads, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
+  grouped_gemm_kernel<T, GATHER, TILES><<<sm_count(), Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(tw, tx, tx8, a);
   return cudaGetLastError();
 }
 
