@@ -83,3 +83,23 @@ def test_single_thread_oracle_baseline():
     assert res["tiny"]["cores"] == 1 and res["tiny"]["value"] > 0
     import oracle
     assert oracle.max_threads() > 1 or os.cpu_count() == 1  # the previous count is restored
+
+
+def test_launches_per_step_follow_the_engine_choice():
+    """The bench's count of our kernels per layer step (its `gpu_launches` claim) for
+    every workload, written out from the engine rules it restates: the sort fused into
+    the quant kernel up to 4096 routes and two launches above 8192; one GEMM engine up to
+    24 rows per expert on average and from 256 on, three launches per GEMM between (the
+    warp-MMA share on 16-row and on 32-row tiles, then the tcgen05 pairs); SwiGLU inside
+    GMM1 above 24 rows per expert.  The ncu launch lists show the same kernels per step
+    (prefill 6, skewed 10, decode 5)."""
+    import synth
+    expect = {
+        "tiny": 0 + 1 + 2 * 1 + 1 + 1,     # 32 routes, 4 rows per expert
+        "decode": 0 + 1 + 2 * 1 + 1 + 1,   # 1024 routes, 4 rows per expert
+        "mid": 0 + 1 + 2 * 1 + 1 + 1,      # 4096 routes, 16 rows per expert
+        "skewed": 2 + 1 + 2 * 3 + 0 + 1,   # 16384 routes, 64 rows per expert: split, fused SwiGLU
+        "prefill": 2 + 1 + 2 * 1 + 0 + 1,  # 49152 routes, 768 rows per expert: pairs only
+    }
+    for name, n in expect.items():
+        assert bench.launches_per_step(synth.CONFIGS[name]) == n, name
