@@ -267,6 +267,8 @@ def _stage_inputs(w):
 
 GEMM_CASES = [
     synth.Workload("g_dec", 60, 512, 128, 16, 2, "uniform", 59),            # warp-MMA engine, 16-row tiles
+    synth.Workload("g_dec_odd", 60, 768, 64, 16, 2, "uniform", 60),         # 16-row tiles, odd stage counts (3, 1):
+                                                                            # the two producers' stages alternate across items
     synth.Workload("g_small", 40, 256, 128, 8, 2, "uniform", 51),           # warp-MMA engine, 32-row tiles
     synth.Workload("g_mid", 160, 512, 192, 16, 2, "biased", 52),            # warp-MMA engine, 32-row tiles, ragged
     synth.Workload("g_mid_tc", 320, 512, 192, 16, 2, "biased", 57),         # tcgen05 pairs, small N tiles, 128-channel tail
