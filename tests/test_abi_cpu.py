@@ -53,6 +53,17 @@ def test_workspace_size_and_shape_checks(lib):
         assert moe.moe_layer_workspace_size(bad) == 0
 
 
+def test_route_sort_workspace_is_one_histogram_per_block(lib):
+    """The multi-block sort's scratch: one (E + 1)-bucket int32 histogram per block of
+    1024 routes (the scatter blocks scan them themselves), nothing up to 8192 routes."""
+    import moe_expert_layer_gb300 as moe
+    assert moe.moe_route_sort_workspace_size(moe.dims(1024, 256, 256, 8, 8)) == 0  # 8192 routes: one block
+    assert moe.moe_route_sort_workspace_size(moe.dims(8192, 4096, 1408, 64, 6)) == 48 * 65 * 4  # prefill
+    assert moe.moe_route_sort_workspace_size(moe.dims(2048, 7168, 2048, 256, 8)) == 16 * 257 * 4  # skewed
+    # past 64 blocks of 1024 routes the blocks grow (2048 routes each for 131072 routes)
+    assert moe.moe_route_sort_workspace_size(moe.dims(16384, 256, 256, 1023, 8)) == 64 * 1024 * 4
+
+
 def test_entry_points_reject_before_touching_the_device(lib):
     import moe_expert_layer_gb300 as moe
     d = moe.dims(16, 256, 256, 8, 2)
